@@ -1,0 +1,235 @@
+/*
+ * mis.h — C ABI of the GB300 (sm_103a) Multiple-Item Scoring prefill hot path.
+ *
+ * Multiple-Item Scoring (MIS) packs one shared prefix and N candidate items
+ * into one sequence and scores every item in a single prefill pass:
+ *
+ *     <prefix><DELIM><item 1><DELIM><item 2><DELIM> ... <item N><DELIM>
+ *
+ * ("Turbocharging LinkedIn's recommendation systems with SGLang", section
+ * "Multi-item-scoring: Our innovation with SGLang"; "From Generation to
+ * Scoring: Scaling LLM-Based Semantic Labeling at LinkedIn", Section 4.1,
+ * eq. 3). Under the mask of eq. (4) of the latter, prefix tokens attend
+ * causally to each other, every item token attends to the whole prefix and
+ * causally inside its own item, never to another item. The label readout of
+ * its Section 3.3 (eq. 2) takes the next-token distribution at each item's
+ * readout row; "Scaling JEV-like Decision Models with SGLang" (section "Why a
+ * Decision Workload Deserves a Scoring Interface") fixes that it is normalised
+ * over the full vocabulary before the requested label columns are read.
+ *
+ * Conventions for every call
+ *   - Every function returns mis_status_t; no exception or C++ type crosses
+ *     the boundary. mis_status_string() names a code.
+ *   - "device" pointers are CUDA global-memory addresses on the current
+ *     device; "host" pointers are ordinary CPU memory. The caller owns every
+ *     buffer, device or host, and allocates all of them; the library
+ *     allocates no device memory. The only library-owned object is the
+ *     host-side plan struct of mis_plan_create().
+ *   - Calls that take a stream are stream-ordered and asynchronous: they
+ *     enqueue work on `stream` (a cudaStream_t passed as void*, NULL = the
+ *     legacy default stream) and return. Host input arrays may be reused as
+ *     soon as the call returns. Device inputs are never modified.
+ *   - Argument errors are detected on the host before anything is enqueued
+ *     and leave outputs untouched. Faults found on the device (an index out
+ *     of range, a wait that ran out of time) are recorded in a status word at
+ *     the start of the call's workspace; read it with mis_get_device_status().
+ *   - Indices, lengths and counts are int32 (packed length T < 2^31).
+ *   - bf16 tensors are IEEE bfloat16 stored as uint16.
+ */
+#ifndef MIS_GB300_H
+#define MIS_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MIS_ABI_VERSION 1
+
+typedef enum {
+  MIS_OK = 0,
+  MIS_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad count, bad id   */
+  MIS_ERR_SHAPE = 2,          /* inconsistent lengths / offsets / strides      */
+  MIS_ERR_UNSUPPORTED = 3,    /* valid but not built (head_dim, K, d ...)      */
+  MIS_ERR_WORKSPACE = 4,      /* workspace missing, misaligned or too small    */
+  MIS_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed             */
+  MIS_ERR_DEVICE_TIMEOUT = 6, /* a kernel wait ran out of time and bailed out  */
+  MIS_ERR_DEVICE_INDEX = 7    /* a device-side index was out of range          */
+} mis_status_t;
+
+const char* mis_status_string(int status);
+int mis_abi_version(void);
+
+/* ------------------------------------------------------------------------
+ * Layout (host). Packs B requests into the delimiter layout above.
+ *
+ * Inputs (host):
+ *   prefix_tokens[B] — P_b, prefix tokens of request b, excluding the DELIM
+ *   n_items[B]       — N_b >= 0 items of request b
+ *   item_lens[sum N] — L_i >= 0 tokens of each item excluding its DELIM,
+ *                      request after request
+ * Outputs (host, caller-allocated):
+ *   cu_seqlens[B+1]  — request b occupies packed rows [cu[b], cu[b+1])
+ *   prefix_len[B]    — S_b = P_b + 1: the shared set Q of eq. (4) is the
+ *                      prefix plus its leading DELIM
+ *   item_ptr[B+1]    — items of request b are [item_ptr[b], item_ptr[b+1])
+ *   item_offsets[M]  — absolute first row of item i's set I_i (its tokens
+ *                      followed by its trailing DELIM); the set ends where the
+ *                      next item starts, or at the request end
+ *   delim_positions[M] — absolute row of item i's trailing DELIM, the row
+ *                      that reads prefix + item i (the readout row)
+ *   position_ids     — may be NULL; else [position_cap] receives the reused
+ *                      positions of Section 4.1: 0..S_b-1 on Q, S_b + d at
+ *                      offset d of every item set (all items start at S_b)
+ * Errors: MIS_ERR_INVALID_ARG (null array, negative length, B < 1),
+ *         MIS_ERR_SHAPE (T or a position would overflow int32, or
+ *         position_cap < T).
+ * ------------------------------------------------------------------------ */
+mis_status_t mis_layout_size(int32_t B, const int32_t* prefix_tokens, const int32_t* n_items,
+                             const int32_t* item_lens, int64_t* T_out, int64_t* M_out);
+
+mis_status_t mis_build_layout(int32_t B, const int32_t* prefix_tokens, const int32_t* n_items,
+                              const int32_t* item_lens, int32_t* cu_seqlens, int32_t* prefix_len,
+                              int32_t* item_ptr, int32_t* item_offsets, int32_t* delim_positions,
+                              int32_t* position_ids, int64_t position_cap);
+
+/* ------------------------------------------------------------------------
+ * Attention descriptor (all arrays host memory, read during planning only).
+ *   B, T         — requests and packed rows; cu_seqlens[B] must equal T
+ *   Hq, Hkv      — query / key-value heads; Hq % Hkv == 0; query head h
+ *                  reads kv head h / (Hq / Hkv)
+ *   D            — head dim, 64 or 128
+ *   scale        — softmax scale; 0 selects 1/sqrt(D)
+ *   cu_seqlens   — [B+1], 0 = cu[0] < cu[1] < ... (every request non-empty)
+ *   prefix_len   — [B], 1 <= S_b <= request length: rows [cu[b], cu[b]+S_b)
+ *                  form Q. S_b = request length with no items is plain
+ *                  causal attention.
+ *   item_ptr     — [B+1] CSR into item_offsets, or NULL when no request
+ *                  has items
+ *   item_offsets — absolute first row of each item set, strictly increasing
+ *                  inside a request, the first equal to cu[b] + S_b; each
+ *                  set is non-empty and the last ends at cu[b+1]
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t B, T, Hq, Hkv, D;
+  float scale;
+  const int32_t* cu_seqlens;
+  const int32_t* prefix_len;
+  const int32_t* item_ptr;
+  const int32_t* item_offsets;
+} mis_attn_desc;
+
+typedef struct mis_plan_s* mis_plan_t;
+
+typedef struct {
+  int64_t n_qtiles;        /* (request, 128-row query tile) pairs              */
+  int64_t n_tiles;         /* non-empty (query tile, 128-key tile) blocks      */
+  int64_t n_full;          /* ... of which every entry is visible              */
+  int64_t n_partial;       /* ... of which some entries are masked             */
+  int64_t n_causal_tiles;  /* blocks a causal mask of the same cu_seqlens keeps */
+  int64_t visible_pairs;   /* unmasked (row, key) pairs, per head              */
+  int64_t workspace_bytes; /* device workspace the plan occupies               */
+} mis_plan_stats;
+
+/* Bytes of device workspace mis_plan_create() needs for this descriptor (0
+ * when the descriptor is invalid; mis_plan_create() then says why). */
+size_t mis_plan_workspace_size(const mis_attn_desc* desc);
+
+/* Validate the descriptor, build the mask-aware tile schedule on the host
+ * (per query tile: the key tiles of the prefix plus the band of its own
+ * items, each flagged full or partial; fully masked tiles are never listed —
+ * "From Generation to Scoring" Section 4.2, "FlashInfer kernels skip fully
+ * masked tiles"; "Turbocharging ...", "Implemented skip tiles"), and upload
+ * it into `workspace` (device, 256-byte aligned, >= mis_plan_workspace_size
+ * bytes) on `stream`. The workspace must stay untouched while the plan is in
+ * use. *out receives a host-side handle, freed by mis_plan_destroy().
+ * workspace == NULL (with ws_bytes == 0) makes a host-only plan: no device
+ * call is made, stats and the tile map can be read, and launching it returns
+ * MIS_ERR_WORKSPACE.
+ * Errors: MIS_ERR_INVALID_ARG / MIS_ERR_SHAPE / MIS_ERR_UNSUPPORTED on the
+ * descriptor, MIS_ERR_WORKSPACE, MIS_ERR_CUDA on the upload. */
+mis_status_t mis_plan_create(const mis_attn_desc* desc, void* workspace, size_t ws_bytes,
+                             void* stream, mis_plan_t* out);
+mis_status_t mis_plan_get_stats(mis_plan_t plan, mis_plan_stats* out);
+/* Canonical tile map: int32 quadruples (request, q-tile, k-tile, 1 = full /
+ * 2 = partial) for every non-empty 128x128 block, sorted by (request, q-tile,
+ * k-tile). Writes min(cap, n) quadruples to host_out (may be NULL when cap is
+ * 0); *n_out receives n. */
+mis_status_t mis_plan_tile_map(mis_plan_t plan, int32_t* host_out, size_t cap, size_t* n_out);
+mis_status_t mis_plan_destroy(mis_plan_t plan);
+
+/* ------------------------------------------------------------------------
+ * MIS attention forward ("From Generation to Scoring", eq. 4 and Section
+ * 4.2; "Turbocharging ...", section "FlashInfer changes").
+ *   q   — device bf16, row j of head h at q[j*q_row_stride + h*D + 0..D-1]
+ *   k,v — device bf16, [T, Hkv, D] with their own row strides
+ *   o   — device bf16 output, o[j*o_row_stride + h*D + ...]
+ *   lse — device fp32 [Hq, T] natural-log softmax normaliser of the scaled
+ *         scores (lse[h*T + j]), or NULL
+ * Strides are in elements; each must be >= Hq*D (q, o) or Hkv*D (k, v) and a
+ * multiple of 8; q, k, v, o must be 16-byte aligned. O rows of one call are
+ * written exactly once; nothing else in o changes.
+ * The plan form runs a plan from mis_plan_create(); the one-shot form plans,
+ * launches and frees the host plan in one call (workspace as for
+ * mis_plan_create()).
+ * ------------------------------------------------------------------------ */
+mis_status_t mis_attention_fwd_plan(mis_plan_t plan, const void* q, const void* k, const void* v,
+                                    void* o, float* lse, int64_t q_row_stride,
+                                    int64_t k_row_stride, int64_t v_row_stride,
+                                    int64_t o_row_stride, void* stream);
+
+mis_status_t mis_attention_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int64_t q_row_stride, int64_t k_row_stride, int64_t v_row_stride,
+                               int64_t o_row_stride, const mis_attn_desc* desc, void* workspace,
+                               size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Label scoring at the readout rows ("From Generation to Scoring", Section
+ * 3.3 and eq. 2; "Turbocharging ...", section "SGLang changes": an N x K
+ * matrix of label log-probs; "Scaling JEV-like Decision Models with SGLang",
+ * "Send a Scoring Request": apply_softmax normalises across labels per item).
+ *   hidden          — device bf16 [T, d], row stride hidden_row_stride (>= d,
+ *                     multiple of 8); the final-normed hidden states
+ *   w_lm            — device bf16 [V, d] row-major LM head (row v = token v)
+ *   delim_positions — device int32 [M], readout row of each item, in [0, T)
+ *   label_token_ids — host int32 [K], 0 <= id < V, caller order, repeats ok
+ *   out_logprobs    — device fp32 [M, K]: z_i[label] - logsumexp_v z_i[v],
+ *                     z_i = W_lm h_i over the full vocabulary
+ *   out_renorm      — device fp32 [M, K] softmax over the K label logits of
+ *                     each item (eq. 2 when K = 2), or NULL
+ * Constraints: d a multiple of 64 (<= 8192), 1 <= K <= 16, 1 <= V, M >= 0.
+ * The full logits never reach global memory: each 128 x 256 logit tile lives
+ * in tensor memory and leaves only a (max, sum-of-exp) pair per item.
+ * Workspace: device, 256-byte aligned, >= mis_label_scores_workspace_size().
+ * A readout row outside [0, T) sets MIS_ERR_DEVICE_INDEX in the workspace
+ * status and scores a zero hidden row instead.
+ * ------------------------------------------------------------------------ */
+size_t mis_label_scores_workspace_size(int32_t M, int32_t d, int32_t V, int32_t K);
+
+mis_status_t mis_label_scores(const void* hidden, int64_t hidden_row_stride, int32_t T,
+                              const void* w_lm, int32_t d, int32_t V,
+                              const int32_t* delim_positions, int32_t M,
+                              const int32_t* label_token_ids, int32_t K, float* out_logprobs,
+                              float* out_renorm, void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Device status of the last call that used `workspace` (a plan workspace or
+ * a scoring workspace). Synchronises `stream`, then returns MIS_OK,
+ * MIS_ERR_DEVICE_TIMEOUT or MIS_ERR_DEVICE_INDEX. Each call clears the word
+ * when it starts.
+ * ------------------------------------------------------------------------ */
+mis_status_t mis_get_device_status(const void* workspace, void* stream);
+
+/* Upper bound, in nanoseconds, on any single wait inside the kernels
+ * (default 200 ms). A wait that runs out sets MIS_ERR_DEVICE_TIMEOUT, lets
+ * every role of the block drain its own copies and tensor-memory work, frees
+ * tensor memory and returns. Small values exist for tests of that path.
+ * Process-wide; returns the previous value. */
+uint64_t mis_set_wait_limit_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MIS_GB300_H */

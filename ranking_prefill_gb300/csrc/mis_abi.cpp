@@ -1,0 +1,254 @@
+// C ABI of the MIS library: argument checks, plan lifecycle, tensor maps,
+// device status. No C++ exception crosses this boundary.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "mis_internal.h"
+
+namespace mis {
+
+namespace {
+
+std::atomic<uint64_t> g_wait_limit_ns{200ull * 1000 * 1000};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+// bf16 tiled tensor map with 128-byte swizzle; dims/box innermost first.
+CUtensorMap make_tmap_bf16(const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides_bytes, const uint32_t* box, bool* ok) {
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof(m));
+  auto fn = encode_fn();
+  if (!fn) { *ok = false; return m; }
+  cuuint64_t gd[5];
+  cuuint64_t gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bx[i] = box[i]; es[i] = 1; }
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
+  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
+                  gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) *ok = false;
+  return m;
+}
+
+}  // namespace mis
+
+struct mis_plan_s {
+  mis::HostPlan p;
+};
+
+using namespace mis;
+
+extern "C" {
+
+const char* mis_status_string(int status) {
+  switch (status) {
+    case MIS_OK: return "ok";
+    case MIS_ERR_INVALID_ARG: return "invalid argument";
+    case MIS_ERR_SHAPE: return "inconsistent shape, offsets or strides";
+    case MIS_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MIS_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MIS_ERR_CUDA: return "CUDA call failed";
+    case MIS_ERR_DEVICE_TIMEOUT: return "a device wait ran out of time";
+    case MIS_ERR_DEVICE_INDEX: return "a device-side index was out of range";
+    default: return "unknown status";
+  }
+}
+
+int mis_abi_version(void) { return MIS_ABI_VERSION; }
+
+uint64_t mis_set_wait_limit_ns(uint64_t ns) { return g_wait_limit_ns.exchange(ns); }
+
+size_t mis_plan_workspace_size(const mis_attn_desc* desc) {
+  try {
+    HostPlan p;
+    if (build_plan(desc, &p) != MIS_OK) return 0;
+    return p.total;
+  } catch (...) {
+    return 0;
+  }
+}
+
+mis_status_t mis_plan_create(const mis_attn_desc* desc, void* workspace, size_t ws_bytes,
+                             void* stream, mis_plan_t* out) {
+  if (!out) return MIS_ERR_INVALID_ARG;
+  *out = nullptr;
+  mis_plan_s* h = nullptr;
+  try {
+    h = new mis_plan_s();
+    mis_status_t st = build_plan(desc, &h->p);
+    if (st != MIS_OK) { delete h; return st; }
+    HostPlan& p = h->p;
+    if (!workspace && ws_bytes == 0) {   // host-only plan: inspection, no launches
+      *out = h;
+      return MIS_OK;
+    }
+    if (!workspace || !aligned256(workspace) || ws_bytes < p.total) { delete h; return MIS_ERR_WORKSPACE; }
+    p.workspace = workspace;
+    // one host image of the workspace after the status words, one copy
+    std::vector<uint8_t> img(p.total - kStatusBytes, 0);
+    auto put = [&](size_t off, const void* src, size_t n) {
+      if (n) std::memcpy(img.data() + (off - kStatusBytes), src, n);
+    };
+    put(p.off_req, p.req.data(), p.req.size() * sizeof(ReqInfo));
+    put(p.off_seg, p.seg_start.data(), p.seg_start.size() * sizeof(int32_t));
+    put(p.off_work, p.work.data(), p.work.size() * sizeof(WorkItem));
+    put(p.off_klist, p.klist.data(), p.klist.size() * sizeof(uint32_t));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (cudaMemsetAsync(ws, 0, kStatusBytes, s) != cudaSuccess ||
+        cudaMemcpyAsync(ws + kStatusBytes, img.data(), img.size(), cudaMemcpyHostToDevice, s) !=
+            cudaSuccess) {
+      delete h;
+      return MIS_ERR_CUDA;
+    }
+    // A copy from pageable memory returns once the source has been staged, so
+    // `img` may be released when this function returns.
+    *out = h;
+    return MIS_OK;
+  } catch (...) {
+    delete h;
+    return MIS_ERR_INVALID_ARG;
+  }
+}
+
+mis_status_t mis_plan_get_stats(mis_plan_t plan, mis_plan_stats* out) {
+  if (!plan || !out) return MIS_ERR_INVALID_ARG;
+  *out = plan->p.stats;
+  return MIS_OK;
+}
+
+mis_status_t mis_plan_tile_map(mis_plan_t plan, int32_t* host_out, size_t cap, size_t* n_out) {
+  if (!plan || !n_out || (cap && !host_out)) return MIS_ERR_INVALID_ARG;
+  const std::vector<int32_t>& tm = plan->p.tile_map;
+  const size_t n = tm.size() / 4;
+  *n_out = n;
+  const size_t w = cap < n ? cap : n;
+  if (w) std::memcpy(host_out, tm.data(), w * 4 * sizeof(int32_t));
+  return MIS_OK;
+}
+
+mis_status_t mis_plan_destroy(mis_plan_t plan) {
+  delete plan;
+  return MIS_OK;
+}
+
+mis_status_t mis_attention_fwd_plan(mis_plan_t plan, const void* q, const void* k, const void* v,
+                                    void* o, float* lse, int64_t qs, int64_t ks, int64_t vs,
+                                    int64_t os, void* stream) {
+  if (!plan) return MIS_ERR_INVALID_ARG;
+  const HostPlan& p = plan->p;
+  if (!p.workspace) return MIS_ERR_WORKSPACE;
+  if (!q || !k || !v || !o) return MIS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return MIS_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return MIS_ERR_INVALID_ARG;
+  const int64_t wq = (int64_t)p.Hq * p.D, wk = (int64_t)p.Hkv * p.D;
+  if (qs < wq || os < wq || ks < wk || vs < wk) return MIS_ERR_SHAPE;
+  if ((qs | ks | vs | os) & 7) return MIS_ERR_SHAPE;
+  try {
+    return launch_attention(p, q, k, v, o, lse, qs, ks, vs, os, stream);
+  } catch (...) {
+    return MIS_ERR_CUDA;
+  }
+}
+
+mis_status_t mis_attention_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int64_t qs, int64_t ks, int64_t vs, int64_t os,
+                               const mis_attn_desc* desc, void* workspace, size_t ws_bytes,
+                               void* stream) {
+  mis_plan_t plan = nullptr;
+  mis_status_t st = mis_plan_create(desc, workspace, ws_bytes, stream, &plan);
+  if (st != MIS_OK) return st;
+  st = mis_attention_fwd_plan(plan, q, k, v, o, lse, qs, ks, vs, os, stream);
+  mis_plan_destroy(plan);
+  return st;
+}
+
+size_t mis_label_scores_workspace_size(int32_t M, int32_t d, int32_t V, int32_t K) {
+  if (M < 0 || d <= 0 || V <= 0 || K <= 0) return 0;
+  return score_workspace_size(M, d, V, K);
+}
+
+mis_status_t mis_label_scores(const void* hidden, int64_t hidden_row_stride, int32_t T,
+                              const void* w_lm, int32_t d, int32_t V,
+                              const int32_t* delim_positions, int32_t M,
+                              const int32_t* label_token_ids, int32_t K, float* out_logprobs,
+                              float* out_renorm, void* workspace, size_t ws_bytes, void* stream) {
+  if (M < 0 || T < 1 || V < 1 || d < 1 || K < 1) return MIS_ERR_INVALID_ARG;
+  if (K > 16) return MIS_ERR_UNSUPPORTED;
+  if (d % 64 || d > 8192) return MIS_ERR_UNSUPPORTED;
+  if (!label_token_ids) return MIS_ERR_INVALID_ARG;
+  for (int l = 0; l < K; ++l)
+    if (label_token_ids[l] < 0 || label_token_ids[l] >= V) return MIS_ERR_INVALID_ARG;
+  if (M > 0) {
+    if (!hidden || !w_lm || !delim_positions || !out_logprobs) return MIS_ERR_INVALID_ARG;
+    if (!aligned16(hidden) || !aligned16(w_lm)) return MIS_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(delim_positions) | reinterpret_cast<uintptr_t>(out_logprobs) |
+         reinterpret_cast<uintptr_t>(out_renorm)) & 3u)
+      return MIS_ERR_INVALID_ARG;
+    if (hidden_row_stride < d || (hidden_row_stride & 7)) return MIS_ERR_SHAPE;
+  }
+  if (!workspace || !aligned256(workspace)) return MIS_ERR_WORKSPACE;
+  if (ws_bytes < score_workspace_size(M, d, V, K)) return MIS_ERR_WORKSPACE;
+  ScoreArgs a;
+  a.hidden = hidden; a.hidden_stride = hidden_row_stride; a.T = T;
+  a.w_lm = w_lm; a.d = d; a.V = V;
+  a.delim = delim_positions; a.M = M;
+  for (int l = 0; l < 16; ++l) a.labels[l] = l < K ? label_token_ids[l] : -1;
+  a.K = K;
+  a.out_logprobs = out_logprobs; a.out_renorm = out_renorm;
+  a.workspace = workspace; a.ws_bytes = ws_bytes;
+  try {
+    return launch_score(a, stream);
+  } catch (...) {
+    return MIS_ERR_CUDA;
+  }
+}
+
+mis_status_t mis_get_device_status(const void* workspace, void* stream) {
+  if (!workspace) return MIS_ERR_INVALID_ARG;
+  uint32_t w[2] = {0, 0};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(w, workspace, sizeof(w), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MIS_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MIS_ERR_CUDA;
+  if (w[0] & kDevTimeout) return MIS_ERR_DEVICE_TIMEOUT;
+  if (w[0] & kDevIndex) return MIS_ERR_DEVICE_INDEX;
+  return MIS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// Internal declarations shared by the host-side translation units of the
+// MIS library. Nothing here is part of the C ABI (include/mis.h is).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "../../include/mis.h"
+
+namespace mis {
+
+// Attention tiling: 128 query rows x 128 keys per block.
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+
+// Workspace layout: the first 256 bytes hold the device status words.
+constexpr size_t kStatusBytes = 256;
+// Bits of the device status word (workspace offset 0).
+constexpr uint32_t kDevTimeout = 1u;
+constexpr uint32_t kDevIndex = 2u;
+
+// Key-tile list entry: absolute first key row | (needs element mask << 31).
+constexpr uint32_t kNeedMask = 0x80000000u;
+
+struct ReqInfo {   // one request of the packed batch, absolute rows
+  int32_t s0;      // first row
+  int32_t e0;      // one past the last row
+  int32_t pend;    // s0 + S_b: rows [s0, pend) form the shared set Q
+  int32_t pad;
+};
+
+struct WorkItem {  // one (request, 128-row query tile)
+  int32_t req;
+  int32_t q0;      // absolute first query row
+  int32_t kofs;    // first entry in the key-tile list
+  int32_t nk;      // number of key tiles
+};
+
+struct HostPlan {
+  int32_t B = 0, T = 0, Hq = 0, Hkv = 0, D = 0;
+  float scale = 0.f;
+  std::vector<ReqInfo> req;
+  std::vector<int32_t> seg_start;  // [T] first row of the set (Q or I_i) holding each row
+  std::vector<WorkItem> work;      // heaviest first
+  std::vector<uint32_t> klist;
+  std::vector<int32_t> tile_map;   // canonical quadruples
+  mis_plan_stats stats{};
+  // byte offsets inside the device workspace
+  size_t off_req = 0, off_seg = 0, off_work = 0, off_klist = 0, total = 0;
+  void* workspace = nullptr;       // device base, set by mis_plan_create
+};
+
+// Validates the descriptor and fills everything but `workspace`.
+mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p);
+
+// Per-device properties the launchers need (cached).
+int num_sms();
+
+// Process-wide wait limit for the kernels' bounded waits.
+uint64_t wait_limit_ns();
+
+// Kernel launchers (defined in the .cu files). Return MIS_ERR_CUDA on launch
+// failure. Pointers are already validated.
+mis_status_t launch_attention(const HostPlan& p, const void* q, const void* k, const void* v,
+                              void* o, float* lse, int64_t qs, int64_t ks, int64_t vs, int64_t os,
+                              void* stream);
+
+struct ScoreArgs {
+  const void* hidden; int64_t hidden_stride; int32_t T;
+  const void* w_lm; int32_t d; int32_t V;
+  const int32_t* delim; int32_t M;
+  int32_t labels[16]; int32_t K;
+  float* out_logprobs; float* out_renorm;
+  void* workspace; size_t ws_bytes;
+};
+size_t score_workspace_size(int32_t M, int32_t d, int32_t V, int32_t K);
+mis_status_t launch_score(const ScoreArgs& a, void* stream);
+
+}  // namespace mis

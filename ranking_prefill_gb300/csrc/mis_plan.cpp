@@ -1,0 +1,208 @@
+// Host-side layout packing and mask-aware tile planning for MIS attention.
+//
+// The mask is eq. (4) of "From Generation to Scoring: Scaling LLM-Based
+// Semantic Labeling at LinkedIn" (Section 4.1): with Q the shared rows and
+// I_i the rows of item i (both contiguous, disjoint), key k is visible from
+// row j iff k <= j and (k in Q or j, k in the same I_i). Because every set is
+// contiguous, the visible keys of row j are at most two intervals:
+//     [s0, min(pend, j+1))  and  [lo(j), j]
+// where lo(j) is the first row of the set holding j (s0 for rows of Q). The
+// planner walks 128-row query tiles and lists only the key tiles that meet
+// one of those intervals for some row of the tile, so fully masked tiles cost
+// neither FLOPs nor bytes (Section 4.2: "the FlashInfer kernels skip fully
+// masked tiles"; "Turbocharging LinkedIn's recommendation systems with
+// SGLang", "Implemented skip tiles for FA2 and FA3 multi-item scoring").
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <limits>
+
+#include "mis_internal.h"
+
+namespace mis {
+
+namespace {
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
+  if (!d || !p) return MIS_ERR_INVALID_ARG;
+  if (d->B < 1 || d->T < 1 || d->Hq < 1 || d->Hkv < 1) return MIS_ERR_INVALID_ARG;
+  if (!d->cu_seqlens || !d->prefix_len) return MIS_ERR_INVALID_ARG;
+  if (d->Hq % d->Hkv) return MIS_ERR_SHAPE;
+  if (d->D != 64 && d->D != 128) return MIS_ERR_UNSUPPORTED;
+  if (!(d->scale >= 0.f) || std::isinf(d->scale)) return MIS_ERR_INVALID_ARG;
+  // the grid is (query tiles) x Hq blocks and the key-tile flag uses bit 31
+  if ((int64_t)d->T * d->Hq > (int64_t)1 << 40) return MIS_ERR_SHAPE;
+
+  const int32_t B = d->B, T = d->T;
+  const int32_t* cu = d->cu_seqlens;
+  if (cu[0] != 0 || cu[B] != T) return MIS_ERR_SHAPE;
+  for (int b = 0; b < B; ++b)
+    if (cu[b + 1] <= cu[b]) return MIS_ERR_SHAPE;
+
+  p->B = B; p->T = T; p->Hq = d->Hq; p->Hkv = d->Hkv; p->D = d->D;
+  p->scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt((float)d->D);
+  p->req.assign(B, ReqInfo{});
+  p->seg_start.assign(T, 0);
+  p->work.clear(); p->klist.clear(); p->tile_map.clear();
+  p->stats = mis_plan_stats{};
+
+  // ---- sets Q and I_i: validate and record lo(j) for every row ----
+  for (int b = 0; b < B; ++b) {
+    const int32_t s0 = cu[b], e0 = cu[b + 1], S = d->prefix_len[b];
+    if (S < 1 || S > e0 - s0) return MIS_ERR_SHAPE;
+    const int32_t pend = s0 + S;
+    p->req[b] = ReqInfo{s0, e0, pend, 0};
+    for (int32_t j = s0; j < pend; ++j) p->seg_start[j] = s0;
+    int32_t i0 = 0, i1 = 0;
+    if (d->item_ptr) {
+      i0 = d->item_ptr[b]; i1 = d->item_ptr[b + 1];
+      if (i0 < 0 || i1 < i0 || (b == 0 && i0 != 0)) return MIS_ERR_SHAPE;
+      if (i1 > i0 && !d->item_offsets) return MIS_ERR_INVALID_ARG;
+    }
+    if (i1 == i0) {
+      if (pend != e0) return MIS_ERR_SHAPE;      // rows after Q would belong to no set
+      continue;
+    }
+    if (d->item_offsets[i0] != pend) return MIS_ERR_SHAPE;
+    for (int32_t i = i0; i < i1; ++i) {
+      const int32_t a = d->item_offsets[i];
+      const int32_t e = (i + 1 < i1) ? d->item_offsets[i + 1] : e0;
+      if (a < pend || e <= a || e > e0) return MIS_ERR_SHAPE;
+      for (int32_t j = a; j < e; ++j) p->seg_start[j] = a;
+    }
+  }
+
+  // ---- tiles ----
+  struct Tmp { int32_t req, q0, kofs, nk; int64_t cost; int64_t order; };
+  std::vector<Tmp> tmp;
+  int64_t visible = 0, causal_tiles = 0;
+  for (int b = 0; b < B; ++b) {
+    const ReqInfo& R = p->req[b];
+    const int32_t L = R.e0 - R.s0;
+    // visible pairs: rows of Q see [s0, j]; rows of item set a see Q plus [a, j]
+    for (int32_t j = R.s0; j < R.e0; ++j) {
+      const int32_t lo = p->seg_start[j];
+      visible += (j < R.pend) ? (j - R.s0 + 1) : ((int64_t)(R.pend - R.s0) + (j - lo + 1));
+    }
+    const int32_t nqt = (L + kBM - 1) / kBM;
+    for (int32_t t = 0; t < nqt; ++t) {
+      const int32_t r0 = R.s0 + t * kBM;
+      const int32_t r1 = std::min(r0 + kBM, R.e0);
+      causal_tiles += ((r1 - 1 - R.s0) / kBN) + 1;
+      const int32_t lo_min = p->seg_start[r0];       // lo(j) never decreases with j
+      const int32_t lo_max = p->seg_start[r1 - 1];
+      // interval 1: keys of Q up to the last row; interval 2: [lo_min, r1)
+      const int32_t qa = 0, qb = (std::min(R.pend, r1) - R.s0 + kBN - 1) / kBN;  // [qa, qb)
+      const int32_t ba = (lo_min - R.s0) / kBN, bb = (r1 - 1 - R.s0) / kBN + 1;  // [ba, bb)
+      Tmp w{b, r0, (int32_t)p->klist.size(), 0, 0, (int64_t)tmp.size()};
+      auto emit = [&](int32_t u) {
+        const int32_t c0 = R.s0 + u * kBN;
+        const int32_t c1 = std::min(c0 + kBN, R.e0);
+        // full iff every (j in [r0,r1), k in [c0,c1)) is visible:
+        //   causal part: c1 - 1 <= r0;
+        //   set part: keys at or past pend must be >= lo(j) for every row.
+        const bool full = (c1 - 1 <= r0) && (c1 <= R.pend || std::max(c0, R.pend) >= lo_max);
+        // a clipped key tile loads rows of the next request: mask it too
+        const bool need_mask = !full || (c0 + kBN > R.e0);
+        p->klist.push_back((uint32_t)c0 | (need_mask ? kNeedMask : 0u));
+        p->tile_map.insert(p->tile_map.end(), {b, t, u, full ? 1 : 2});
+        if (full) ++p->stats.n_full; else ++p->stats.n_partial;
+        ++w.nk;
+        w.cost += need_mask ? 5 : 4;   // masked tiles spend extra ALU in the softmax
+      };
+      for (int32_t u = qa; u < qb; ++u) emit(u);
+      for (int32_t u = std::max(ba, qb); u < bb; ++u) emit(u);
+      tmp.push_back(w);
+    }
+  }
+  if (p->klist.size() > (size_t)std::numeric_limits<int32_t>::max()) return MIS_ERR_SHAPE;
+  // heaviest query tiles first (longest-processing-time order), stable
+  std::stable_sort(tmp.begin(), tmp.end(),
+                   [](const Tmp& a, const Tmp& b) { return a.cost > b.cost; });
+  p->work.reserve(tmp.size());
+  for (const Tmp& w : tmp) p->work.push_back(WorkItem{w.req, w.q0, w.kofs, w.nk});
+
+  p->stats.n_qtiles = (int64_t)p->work.size();
+  p->stats.n_tiles = p->stats.n_full + p->stats.n_partial;
+  p->stats.n_causal_tiles = causal_tiles;
+  p->stats.visible_pairs = visible;
+
+  // ---- workspace layout ----
+  size_t off = kStatusBytes;
+  p->off_req = off;   off = align_up(off + sizeof(ReqInfo) * B, 256);
+  p->off_seg = off;   off = align_up(off + sizeof(int32_t) * (size_t)T, 256);
+  p->off_work = off;  off = align_up(off + sizeof(WorkItem) * p->work.size(), 256);
+  p->off_klist = off; off = align_up(off + sizeof(uint32_t) * std::max<size_t>(p->klist.size(), 1), 256);
+  p->total = off;
+  p->stats.workspace_bytes = (int64_t)off;
+  return MIS_OK;
+}
+
+}  // namespace mis
+
+// ---------------------------------------------------------------------------
+// Layout packing (C ABI). Rows of request b: P_b prefix tokens, the leading
+// DELIM, then for each item its L_i tokens and a trailing DELIM
+// ("Turbocharging ...", section "Multi-item-scoring: Our innovation with
+// SGLang"). Position ids follow Section 4.1 of "From Generation to Scoring":
+// the shared rows get 0..S_b-1 and offset d of every item set gets S_b + d.
+// ---------------------------------------------------------------------------
+extern "C" mis_status_t mis_layout_size(int32_t B, const int32_t* prefix_tokens,
+                                        const int32_t* n_items, const int32_t* item_lens,
+                                        int64_t* T_out, int64_t* M_out) {
+  if (B < 1 || !prefix_tokens || !n_items) return MIS_ERR_INVALID_ARG;
+  int64_t T = 0, M = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    if (prefix_tokens[b] < 0 || n_items[b] < 0) return MIS_ERR_INVALID_ARG;
+    T += (int64_t)prefix_tokens[b] + 1;
+    M += n_items[b];
+  }
+  if (M > 0 && !item_lens) return MIS_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < M; ++i) {
+    if (item_lens[i] < 0) return MIS_ERR_INVALID_ARG;
+    T += (int64_t)item_lens[i] + 1;
+  }
+  if (T >= ((int64_t)1 << 31) - mis::kBN) return MIS_ERR_SHAPE;
+  if (T_out) *T_out = T;
+  if (M_out) *M_out = M;
+  return MIS_OK;
+}
+
+extern "C" mis_status_t mis_build_layout(int32_t B, const int32_t* prefix_tokens,
+                                         const int32_t* n_items, const int32_t* item_lens,
+                                         int32_t* cu_seqlens, int32_t* prefix_len,
+                                         int32_t* item_ptr, int32_t* item_offsets,
+                                         int32_t* delim_positions, int32_t* position_ids,
+                                         int64_t position_cap) {
+  int64_t T = 0, M = 0;
+  mis_status_t st = mis_layout_size(B, prefix_tokens, n_items, item_lens, &T, &M);
+  if (st != MIS_OK) return st;
+  if (!cu_seqlens || !prefix_len || !item_ptr) return MIS_ERR_INVALID_ARG;
+  if (M > 0 && (!item_offsets || !delim_positions)) return MIS_ERR_INVALID_ARG;
+  if (position_ids && position_cap < T) return MIS_ERR_SHAPE;
+  int32_t row = 0, it = 0;
+  cu_seqlens[0] = 0;
+  item_ptr[0] = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    const int32_t S = prefix_tokens[b] + 1;
+    prefix_len[b] = S;
+    if (position_ids)
+      for (int32_t t = 0; t < S; ++t) position_ids[row + t] = t;
+    row += S;
+    for (int32_t n = 0; n < n_items[b]; ++n, ++it) {
+      const int32_t len = item_lens[it] + 1;     // item tokens + trailing DELIM
+      item_offsets[it] = row;
+      if (position_ids)
+        for (int32_t t = 0; t < len; ++t) position_ids[row + t] = S + t;
+      row += len;
+      delim_positions[it] = row - 1;
+    }
+    cu_seqlens[b + 1] = row;
+    item_ptr[b + 1] = it;
+  }
+  return MIS_OK;
+}

@@ -1,0 +1,360 @@
+// Label scoring at the MIS readout rows, sm_103a.
+//
+// For every item i with readout row r_i (its trailing DELIM):
+//   z_i = W_lm h_{r_i}  over the whole vocabulary,
+//   logprob[i, l] = z_i[label_l] - logsumexp_v z_i[v],
+//   renorm[i, :]  = softmax over the K label logits (eq. 2 for K = 2).
+// ("From Generation to Scoring: Scaling LLM-Based Semantic Labeling at
+// LinkedIn", Section 3.3; "Scaling JEV-like Decision Models with SGLang",
+// "Why a Decision Workload Deserves a Scoring Interface": label extraction
+// keeps the vocabulary projection and the full-distribution normalisation;
+// "Turbocharging LinkedIn's recommendation systems with SGLang", "SGLang
+// changes": an N x K matrix of label log-probs.)
+//
+// Three launches:
+//   1. gather  — copy the M readout rows of `hidden` into a dense [M_pad, d]
+//                bf16 block (M_pad a multiple of 128, zero rows after M);
+//   2. partial — grid (item tile, vocab chunk). Each block multiplies one
+//                128-item tile against a run of 256-token vocab tiles on the
+//                tensor cores (tcgen05.mma 128x256x16, both operands staged by
+//                TMA with 128-byte swizzle, fp32 accumulators in TMEM, two
+//                accumulators so the epilogue of tile t overlaps the MMAs of
+//                tile t+1). The epilogue reads each item's 256 logits from its
+//                TMEM lane, folds them into a running (max, sum of exp) and
+//                keeps the logits of requested labels. Logits never reach
+//                global memory; only one (max, sum) pair per item and chunk;
+//   3. combine — merge the pairs of all chunks into logsumexp, write the
+//                label log-probs and the label-renormalised scores.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "mis_internal.h"
+#include "mis_ptx.cuh"
+
+namespace mis {
+
+CUtensorMap make_tmap_bf16(const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides_bytes, const uint32_t* box, bool* ok);
+
+namespace {
+
+using namespace dev;
+
+constexpr int kItemTile = 128;   // MMA M: items
+constexpr int kVocabTile = 256;  // MMA N: vocabulary entries
+constexpr int kKStep = 64;       // d elements per stage (one 128-byte swizzle row)
+constexpr int kStages = 4;
+constexpr int kABytes = kItemTile * kKStep * 2;    // 16 KB
+constexpr int kBBytes = kVocabTile * kKStep * 2;   // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kData = kStages * kStageBytes;
+constexpr int kSmem = kData + 256 + 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct ScoreLayout {       // byte offsets inside the scoring workspace
+  size_t gathered, part, zlab, total;
+  int32_t m_pad, n_vtiles, max_chunks;
+};
+
+ScoreLayout score_layout(int32_t M, int32_t d, int32_t V, int32_t K) {
+  ScoreLayout L;
+  L.m_pad = (int32_t)align_up((size_t)std::max(M, 1), kItemTile);
+  L.n_vtiles = (V + kVocabTile - 1) / kVocabTile;
+  L.max_chunks = L.n_vtiles;
+  size_t off = kStatusBytes;
+  L.gathered = off; off = align_up(off + (size_t)L.m_pad * d * 2, 1024);
+  L.part = off;     off = align_up(off + (size_t)L.m_pad * L.max_chunks * 2 * sizeof(float), 256);
+  L.zlab = off;     off = align_up(off + (size_t)L.m_pad * std::max(K, 1) * sizeof(float), 256);
+  L.total = off;
+  return L;
+}
+
+struct ScoreParams {
+  int32_t M, V, K, n_vtiles, tiles_per_chunk, n_chunks, n_kb;
+  int32_t labels[16];
+  float* part;        // [m_pad][n_chunks][2] = (max in log2 units, sum of 2^(z*log2e - max))
+  float* zlab;        // [m_pad][K] label logits
+  uint32_t* status;
+  uint64_t wait_ns;
+};
+
+// ------------------------------------------------------------------ gather
+__global__ void __launch_bounds__(128)
+mis_gather_rows_kernel(const __nv_bfloat16* __restrict__ hidden, int64_t stride, int32_t T,
+                       const int32_t* __restrict__ rows, int32_t M, int32_t d,
+                       __nv_bfloat16* __restrict__ out, uint32_t* status) {
+  const int i = blockIdx.x;
+  int32_t r = -1;
+  if (i < M) {
+    r = rows[i];
+    if (r < 0 || r >= T) {
+      if (threadIdx.x == 0) raise_status(status, kDevIndex, (uint32_t)i);
+      r = -1;
+    }
+  }
+  const int n16 = d / 8;                              // 16-byte chunks per row
+  uint4* dst = reinterpret_cast<uint4*>(out + (int64_t)i * d);
+  if (r < 0) {
+    for (int c = threadIdx.x; c < n16; c += blockDim.x) dst[c] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(hidden + (int64_t)r * stride);
+  for (int c = threadIdx.x; c < n16; c += blockDim.x) dst[c] = src[c];
+}
+
+// ----------------------------------------------------------------- partial
+__global__ void __launch_bounds__(256, 1)
+mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
+                         const __grid_constant__ CUtensorMap wmap, const ScoreParams p) {
+  constexpr int bF = 0, bE = kStages, bAF = 2 * kStages, bAE = bAF + 2, bDR = bAE + 2,
+                nBar = bDR + 1;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kData);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + nBar);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  volatile uint32_t* skip_flag = tmem_slot + 2;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x;
+  const int chunk = blockIdx.y;
+  const int v_first = chunk * p.tiles_per_chunk;
+  const int v_last = min(v_first + p.tiles_per_chunk, p.n_vtiles);
+  const int nt = v_last - v_first;
+  const int nkb = p.n_kb;
+
+  if (threadIdx.x == 0) {
+    *skip_flag = (*(volatile uint32_t*)p.status & kDevTimeout) ? 1u : 0u;
+    *abort_flag = 0;
+    for (int s = 0; s < kStages; ++s) { mbar_init(bar(bF + s), 1); mbar_init(bar(bE + s), 1); }
+    for (int s = 0; s < 2; ++s) { mbar_init(bar(bAF + s), 1); mbar_init(bar(bAE + s), 128); }
+    mbar_init(bar(bDR), 1);
+    fence_mbar_init();
+    fence_proxy_async();
+  }
+  __syncthreads();
+  if (*skip_flag || nt <= 0) return;
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Waiter W{abort_flag, p.status, p.wait_ns};
+  const int total_steps = nt * nkb;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&amap); tma_prefetch_desc(&wmap);
+      int issued = 0;
+      for (int step = 0; step < total_steps; ++step) {
+        const int st = step % kStages;
+        if (step >= kStages && !wait(bar(bE + st), ((step / kStages) - 1) & 1, W, 0x100)) break;
+        const int t = v_first + step / nkb, kb = step % nkb;
+        uint8_t* sA = smem + st * kStageBytes;
+        uint8_t* sB = sA + kABytes;
+        mbar_arrive_expect_tx(bar(bF + st), kStageBytes);
+        tma_load_2d(smem_u32(sA), &amap, bar(bF + st), kb * kKStep, mt * kItemTile);
+        tma_load_2d(smem_u32(sB), &wmap, bar(bF + st), kb * kKStep, t * kVocabTile);
+        issued = step + 1;
+      }
+      for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
+        wait_drain(bar(bF + i % kStages), (i / kStages) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(kItemTile, kVocabTile, false);
+      bool ok = true;
+      for (int ti = 0; ok && ti < nt; ++ti) {
+        const int buf = ti & 1;
+        if (ti >= 2 && !wait(bar(bAE + buf), ((ti >> 1) - 1) & 1, W, 0x200)) break;
+        tc_fence_after();
+        const uint32_t dacc = tmem + buf * kVocabTile;
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int step = ti * nkb + kb;
+          const int st = step % kStages;
+          if (!wait(bar(bF + st), (step / kStages) & 1, W, 0x300)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t aA = smem_u32(smem + st * kStageBytes);
+          const uint32_t aB = aA + kABytes;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ss(dacc, sdesc_sw128(aA + ks * 32, 16, 1024), sdesc_sw128(aB + ks * 32, 16, 1024),
+                   idesc, (kb | ks) != 0);
+          mma_commit(bar(bE + st));
+        }
+        if (ok) mma_commit(bar(bAF + buf));
+      }
+      mma_commit(bar(bDR));
+      wait_drain(bar(bDR), 0);
+    }
+  } else if (warp >= 4) {
+    const int sw = warp - 4;
+    const int row = sw * 32 + lane;
+    const int item = mt * kItemTile + row;
+    const uint32_t tl = tmem + ((uint32_t)(sw * 32) << 16);
+    float m2 = -INFINITY, s = 0.f;
+    bool ok = true;
+    for (int ti = 0; ti < nt; ++ti) {
+      const int buf = ti & 1;
+      ok = wait(bar(bAF + buf), (ti >> 1) & 1, W, 0x400);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int v0 = (v_first + ti) * kVocabTile;
+      const uint32_t tacc = tl + buf * kVocabTile;
+#pragma unroll 1
+      for (int c = 0; c < kVocabTile / 32; ++c) {
+        uint32_t zr[32];
+        tmem_ld32(tacc + c * 32, zr);
+        tmem_ld_wait();
+        const int vbase = v0 + c * 32;
+        float cm = -INFINITY;
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const float z = (vbase + x < p.V) ? __uint_as_float(zr[x]) * kLog2e : -INFINITY;
+          zr[x] = __float_as_uint(z);
+          cm = fmaxf(cm, z);
+        }
+        if (cm > m2) {
+          s *= ex2(m2 - cm);
+          m2 = cm;
+        }
+        float cs = 0.f;
+#pragma unroll
+        for (int x = 0; x < 32; ++x) cs += ex2(__uint_as_float(zr[x]) - m2);
+        s += cs;
+      }
+      for (int l = 0; l < p.K; ++l) {
+        const int lab = p.labels[l];
+        if (lab >= v0 && lab < v0 + kVocabTile) {
+          const uint32_t z = tmem_ld1(tacc + (lab - v0));
+          tmem_ld_wait();
+          if (item < p.M) p.zlab[(int64_t)item * p.K + l] = __uint_as_float(z);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(bAE + buf));
+    }
+    if (ok) {
+      float* pp = p.part + ((int64_t)item * p.n_chunks + chunk) * 2;
+      pp[0] = m2;
+      pp[1] = s;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ----------------------------------------------------------------- combine
+__global__ void __launch_bounds__(128)
+mis_score_combine_kernel(const ScoreParams p, float* __restrict__ out,
+                         float* __restrict__ renorm) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= p.M) return;
+  if (*(volatile uint32_t*)p.status & kDevTimeout) return;
+  const float* pp = p.part + (int64_t)i * p.n_chunks * 2;
+  float m = -INFINITY, s = 0.f;
+  for (int c = 0; c < p.n_chunks; ++c) {
+    const float mc = pp[2 * c], sc = pp[2 * c + 1];
+    if (mc == -INFINITY) continue;
+    if (mc > m) { s = s * exp2f(m - mc) + sc; m = mc; }
+    else s += sc * exp2f(mc - m);
+  }
+  const float lse = (m + log2f(s)) * kLn2;
+  const float* zl = p.zlab + (int64_t)i * p.K;
+  float zmax = -INFINITY;
+  for (int l = 0; l < p.K; ++l) {
+    out[(int64_t)i * p.K + l] = zl[l] - lse;
+    zmax = fmaxf(zmax, zl[l]);
+  }
+  if (renorm) {
+    float den = 0.f;
+    for (int l = 0; l < p.K; ++l) den += expf(zl[l] - zmax);
+    for (int l = 0; l < p.K; ++l) renorm[(int64_t)i * p.K + l] = expf(zl[l] - zmax) / den;
+  }
+}
+
+// Vocab tiles per block: the smallest makespan in tile units, counting one
+// extra tile per block for pipeline fill and the unoverlapped last epilogue.
+int pick_tiles_per_chunk(int n_mtiles, int n_vtiles, int n_sm) {
+  int best = n_vtiles;
+  long best_cost = -1;
+  for (int tpc = 1; tpc <= n_vtiles; ++tpc) {
+    const long chunks = (n_vtiles + tpc - 1) / tpc;
+    const long blocks = chunks * n_mtiles;
+    const long waves = (blocks + n_sm - 1) / n_sm;
+    const long cost = waves * (tpc + 1);
+    if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = tpc; }
+  }
+  return best;
+}
+
+}  // namespace
+
+size_t score_workspace_size(int32_t M, int32_t d, int32_t V, int32_t K) {
+  return score_layout(M, d, V, K).total;
+}
+
+mis_status_t launch_score(const ScoreArgs& a, void* stream) {
+  const ScoreLayout L = score_layout(a.M, a.d, a.V, a.K);
+  if (a.ws_bytes < L.total) return MIS_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return MIS_ERR_CUDA;
+  if (a.M == 0) return MIS_OK;
+
+  __nv_bfloat16* gathered = reinterpret_cast<__nv_bfloat16*>(ws + L.gathered);
+  mis_gather_rows_kernel<<<L.m_pad, 128, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(a.hidden), a.hidden_stride, a.T, a.delim, a.M, a.d,
+      gathered, status);
+  if (cudaGetLastError() != cudaSuccess) return MIS_ERR_CUDA;
+
+  bool ok = true;
+  const uint64_t adims[2] = {(uint64_t)a.d, (uint64_t)L.m_pad};
+  const uint64_t astr[1] = {(uint64_t)a.d * 2};
+  const uint32_t abox[2] = {(uint32_t)kKStep, (uint32_t)kItemTile};
+  const uint64_t wdims[2] = {(uint64_t)a.d, (uint64_t)a.V};
+  const uint64_t wstr[1] = {(uint64_t)a.d * 2};
+  const uint32_t wbox[2] = {(uint32_t)kKStep, (uint32_t)kVocabTile};
+  CUtensorMap am = make_tmap_bf16(gathered, 2, adims, astr, abox, &ok);
+  CUtensorMap wm = make_tmap_bf16(a.w_lm, 2, wdims, wstr, wbox, &ok);
+  if (!ok) return MIS_ERR_CUDA;
+
+  const int n_mtiles = L.m_pad / kItemTile;
+  ScoreParams p;
+  p.M = a.M; p.V = a.V; p.K = a.K;
+  p.n_vtiles = L.n_vtiles;
+  p.tiles_per_chunk = pick_tiles_per_chunk(n_mtiles, L.n_vtiles, num_sms());
+  p.n_chunks = (L.n_vtiles + p.tiles_per_chunk - 1) / p.tiles_per_chunk;
+  p.n_kb = a.d / kKStep;
+  for (int l = 0; l < 16; ++l) p.labels[l] = l < a.K ? a.labels[l] : -1;
+  p.part = reinterpret_cast<float*>(ws + L.part);
+  p.zlab = reinterpret_cast<float*>(ws + L.zlab);
+  p.status = status;
+  p.wait_ns = wait_limit_ns();
+
+  if (cudaFuncSetAttribute(mis_score_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmem) != cudaSuccess)
+    return MIS_ERR_CUDA;
+  mis_score_partial_kernel<<<dim3(n_mtiles, p.n_chunks), 256, kSmem, st>>>(am, wm, p);
+  if (cudaGetLastError() != cudaSuccess) return MIS_ERR_CUDA;
+  mis_score_combine_kernel<<<(a.M + 127) / 128, 128, 0, st>>>(p, a.out_logprobs, a.out_renorm);
+  return cudaGetLastError() == cudaSuccess ? MIS_OK : MIS_ERR_CUDA;
+}
+
+}  // namespace mis

@@ -1,0 +1,160 @@
+"""Host-side checks of the C-ABI library (no GPU needed).
+
+* the shared library loads and exports every function include/mis.h declares;
+* mis_build_layout equals the oracle's packing bit for bit;
+* the planner's tile map and visible-pair count equal the oracle's
+  element-by-element classification bit for bit;
+* malformed descriptors and arguments return the documented status codes
+  before any device work is enqueued.
+"""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+from ranking_prefill_gb300 import lib, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(lib.LIB_PATH):
+        from ranking_prefill_gb300 import build
+        build.build()
+    return lib.load()
+
+
+def test_exports_every_declared_symbol(L):
+    hdr = open(os.path.join(ROOT, "include", "mis.h")).read()
+    declared = set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(mis_\w+)\s*\(", hdr, flags=re.M))
+    assert declared == set(lib.EXPORTS), declared ^ set(lib.EXPORTS)
+    for name in declared:
+        assert hasattr(L, name)
+    assert L.mis_abi_version() == 1
+    for st in range(8):
+        assert lib.mis_status_string(st) != "unknown status"
+
+
+def _shapes_cases():
+    yield synth.draw_shapes(synth.WORKLOADS["tiny"])
+    yield synth.draw_shapes(synth.WORKLOADS["qwen3-0.6b-layer"])
+    yield synth.draw_shapes(synth.WORKLOADS["decision-256"])
+    yield synth.draw_shapes(synth.WORKLOADS["8b-large"])
+    rng = np.random.default_rng(123)
+    for _ in range(30):
+        B = int(rng.integers(1, 5))
+        p = rng.integers(0, 300, B)
+        n = rng.integers(0, 12, B)
+        lens = rng.integers(0, 70, int(n.sum()))
+        yield synth.custom_shapes(p, n, lens)
+
+
+def test_layout_bit_exact(L):
+    for s in _shapes_cases():
+        got = lib.mis_build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+        ref = O.build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+        for f in ("cu_seqlens", "prefix_len", "item_ptr", "item_offsets", "delim_positions",
+                  "position_ids"):
+            assert np.array_equal(getattr(got, f), getattr(ref, f)), f
+
+
+def _plan(lay, hq=4, hkv=2, D=64):
+    return lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, hq, hkv, D)
+
+
+def test_tile_map_and_pairs_bit_exact(L):
+    cases = list(_shapes_cases())
+    for s in cases:
+        lay = O.build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+        p = lib.Plan.host_only(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, 4, 2, 64)
+        got = p.tile_map()
+        ref = O.tile_map(lay, 128, 128)
+        assert got.shape == ref.shape and np.array_equal(got, ref)
+        st = p.stats()
+        assert st["n_full"] == int((ref[:, 3] == O.FULL).sum())
+        assert st["n_partial"] == int((ref[:, 3] == O.PARTIAL).sum())
+        if lay.T <= 6000:
+            assert st["visible_pairs"] == O.pair_count(lay)
+
+
+def test_causal_plan_is_plain_causal(L):
+    lens = [1, 127, 128, 129, 300]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    p = lib.Plan.host_only(cu, lens, None, None, 4, 2, 128)
+    ref = O.tile_map(O.causal_layout(lens), 128, 128)
+    assert np.array_equal(p.tile_map(), ref)
+    st = p.stats()
+    assert st["n_tiles"] == st["n_causal_tiles"]
+    assert st["visible_pairs"] == sum(L_ * (L_ + 1) // 2 for L_ in lens)
+
+
+def test_workspace_size_and_validation(L):
+    s = synth.draw_shapes(synth.WORKLOADS["tiny"])
+    lay = lib.mis_build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+    p = _plan(lay)
+    assert p.workspace_size() > 0
+    # descriptor errors
+    def status(**kw):
+        args = dict(cu=lay.cu_seqlens, pl=lay.prefix_len, ip=lay.item_ptr, io=lay.item_offsets,
+                    hq=4, hkv=2, D=64)
+        args.update(kw)
+        pl = lib.Plan(args["cu"], args["pl"], args["ip"], args["io"], args["hq"], args["hkv"], args["D"])
+        h = C.c_void_p()
+        return L.mis_plan_create(C.byref(pl.desc), None, 0, None, C.byref(h))
+    assert status() == lib.MIS_OK                      # host-only plan
+    assert status(hq=3) == lib.MIS_ERR_SHAPE
+    assert status(D=96) == lib.MIS_ERR_UNSUPPORTED
+    assert status(pl=[0]) == lib.MIS_ERR_SHAPE
+    assert status(pl=[300]) == lib.MIS_ERR_SHAPE
+    bad = lay.item_offsets.copy(); bad[3] += 1
+    assert status(io=bad) == lib.MIS_OK                    # still a valid partition
+    bad = lay.item_offsets.copy(); bad[0] += 1
+    assert status(io=bad) == lib.MIS_ERR_SHAPE            # first item must follow Q
+    bad = lay.item_offsets.copy(); bad[4] = bad[3]
+    assert status(io=bad) == lib.MIS_ERR_SHAPE            # empty item set
+    assert status(ip=None, io=None) == lib.MIS_ERR_SHAPE  # rows after Q belong to nothing
+    assert status(ip=None, io=None, pl=[lay.T]) == lib.MIS_OK   # plain causal is valid
+    pl = _plan(lay)
+    pl.desc.T = lay.T + 1                                  # cu_seqlens[B] != T
+    h = C.c_void_p()
+    assert L.mis_plan_create(C.byref(pl.desc), None, 0, None, C.byref(h)) == lib.MIS_ERR_SHAPE
+    cu = lay.cu_seqlens.copy(); cu[0] = 1
+    assert status(cu=cu) == lib.MIS_ERR_SHAPE
+    # misaligned workspace
+    h = C.c_void_p()
+    assert L.mis_plan_create(C.byref(p.desc), C.c_void_p(0x1001), 1 << 30, None, C.byref(h)) == \
+        lib.MIS_ERR_WORKSPACE
+
+
+def test_label_scores_argument_errors(L):
+    labels = np.array([1, 2], np.int32)
+    def call(M=4, d=128, V=1000, K=2, lab=labels, ws=None, wsb=0):
+        return L.mis_label_scores(C.c_void_p(0x1000), d, 100, C.c_void_p(0x2000), d, V,
+                                  C.c_void_p(0x3000), M, lab.ctypes.data_as(C.POINTER(C.c_int32)),
+                                  K, C.c_void_p(0x4000), None, ws, wsb, None)
+    assert call() == lib.MIS_ERR_WORKSPACE
+    assert call(d=96) == lib.MIS_ERR_UNSUPPORTED
+    assert call(K=17, lab=np.arange(17, dtype=np.int32)) == lib.MIS_ERR_UNSUPPORTED
+    assert call(lab=np.array([1, 1000], np.int32)) == lib.MIS_ERR_INVALID_ARG
+    assert call(lab=np.array([-1, 3], np.int32)) == lib.MIS_ERR_INVALID_ARG
+    assert call(M=-1) == lib.MIS_ERR_INVALID_ARG
+    assert call(ws=C.c_void_p(0x10010), wsb=1 << 40) == lib.MIS_ERR_WORKSPACE   # misaligned
+    need = lib.mis_label_scores_workspace_size(4, 128, 1000, 2)
+    assert need > 0
+    assert call(ws=C.c_void_p(0x100000), wsb=need - 1) == lib.MIS_ERR_WORKSPACE
+    assert lib.mis_label_scores_workspace_size(4, 128, 0, 2) == 0
+
+
+def test_layout_argument_errors(L):
+    with pytest.raises(lib.MisError) as e:
+        lib.mis_build_layout([-1], [0], [])
+    assert e.value.status == lib.MIS_ERR_INVALID_ARG
+    with pytest.raises(lib.MisError):
+        lib.mis_build_layout([4], [2], [3, -2])
+    with pytest.raises(lib.MisError) as e:
+        lib.mis_build_layout([2 ** 31 - 2], [0], [])
+    assert e.value.status == lib.MIS_ERR_SHAPE

@@ -1,0 +1,108 @@
+"""GPU parity of mis_label_scores against the fp64 oracle (through the C ABI).
+
+Full element-by-element checks on small and medium cases (ragged vocabulary
+tails, item counts around the 128-item tile, d = 64..1024, K = 1..16,
+repeated and edge label ids), the full qwen3-0.6b-layer workload, and
+seeded item samples of the large ones. Tolerance: max-abs 1e-2 on log-probs
+and on the label-renormalised scores.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from ranking_prefill_gb300 import lib, synth
+from gpu_helpers import SCORE_TOL, f64, run_scores
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(hidden, w, delim, labels, items=None, T=None):
+    out, ren, ws = run_scores(hidden.cuda(), w.cuda(), torch.as_tensor(delim, dtype=torch.int32).cuda(),
+                              labels, T=T)
+    assert lib.mis_get_device_status(ws) == lib.MIS_OK
+    lp, rn, _ = O.label_scores(f64(hidden), f64(w), np.asarray(delim), labels, items=items)
+    sel = slice(None) if items is None else np.asarray(items)
+    g_lp, g_rn = f64(out)[sel], f64(ren)[sel]
+    assert np.isfinite(g_lp).all() and np.isfinite(g_rn).all()
+    e1, e2 = np.abs(g_lp - lp).max(), np.abs(g_rn - rn).max()
+    assert e1 <= SCORE_TOL, f"logprob err {e1}"
+    assert e2 <= SCORE_TOL, f"renorm err {e2}"
+    return e1
+
+
+def test_tiny_workload():
+    w = synth.WORKLOADS["tiny"]
+    s = synth.draw_shapes(w)
+    lay = O.build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+    v = synth.draw_values(w.seed, lay.T, w.hq, w.hkv, w.head_dim, w.d_model, w.vocab)
+    _check(v["hidden"], v["w_lm"], lay.delim_positions, s.label_sets[0].tolist())
+
+
+@pytest.mark.parametrize("M,d,V,labels", [
+    (1, 64, 1000, [0]),
+    (100, 256, 4097, [4096, 0, 17]),
+    (128, 512, 2048, [5, 5, 2047, 1000]),
+    (129, 128, 777, list(range(16))),
+    (300, 1024, 5000, [1234, 4321]),
+])
+def test_random_cases(M, d, V, labels):
+    g = torch.Generator().manual_seed(M * 7 + d)
+    T = M + 37
+    hidden = torch.randn(T, d, generator=g).to(torch.bfloat16)
+    w = (torch.randn(V, d, generator=g) * 0.05).to(torch.bfloat16)
+    delim = np.random.default_rng(M).choice(T, size=M, replace=M > T).astype(np.int32)
+    _check(hidden, w, delim, labels)
+
+
+def test_strided_hidden_rows():
+    g = torch.Generator().manual_seed(3)
+    T, d, V = 90, 256, 3000
+    buf = torch.randn(T, d + 64, generator=g).to(torch.bfloat16)
+    hidden = buf[:, :d]                       # row stride d + 64
+    w = (torch.randn(V, d, generator=g) * 0.05).to(torch.bfloat16)
+    delim = np.arange(5, 85, 3, dtype=np.int32)
+    out, ren, ws = run_scores(buf.cuda()[:, :d], w.cuda(), torch.as_tensor(delim).cuda(), [1, 2])
+    lp, rn, _ = O.label_scores(f64(hidden), f64(w), delim, [1, 2])
+    assert np.abs(f64(out) - lp).max() <= SCORE_TOL
+
+
+def test_index_out_of_range_reports_status():
+    g = torch.Generator().manual_seed(4)
+    hidden = torch.randn(50, 128, generator=g).to(torch.bfloat16).cuda()
+    w = (torch.randn(600, 128, generator=g) * 0.05).to(torch.bfloat16).cuda()
+    delim = torch.tensor([3, 50, 7], dtype=torch.int32).cuda()       # 50 is outside [0, 50)
+    out, ren, ws = run_scores(hidden, w, delim, [1, 2])
+    assert lib.mis_get_device_status(ws) == lib.MIS_ERR_DEVICE_INDEX
+    # the valid rows are still scored
+    lp, _, _ = O.label_scores(f64(hidden), f64(w), [3, 0, 7], [1, 2])
+    assert np.abs(f64(out)[[0, 2]] - lp[[0, 2]]).max() <= SCORE_TOL
+
+
+def test_zero_items():
+    out, ren, ws = run_scores(torch.zeros(4, 64, dtype=torch.bfloat16).cuda(),
+                              torch.zeros(10, 64, dtype=torch.bfloat16).cuda(),
+                              torch.zeros(0, dtype=torch.int32).cuda(), [1])
+    assert lib.mis_get_device_status(ws) == lib.MIS_OK
+
+
+def test_qwen3_layer_full():
+    w = synth.WORKLOADS["qwen3-0.6b-layer"]
+    s = synth.draw_shapes(w)
+    lay = O.build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+    v = synth.draw_values(w.seed, lay.T, w.hq, w.hkv, w.head_dim, w.d_model, w.vocab,
+                          want=("hidden", "w_lm"))
+    _check(v["hidden"], v["w_lm"], lay.delim_positions, s.label_sets[0].tolist())
+
+
+@pytest.mark.parametrize("name", ["8b-large", "decision-256", "varlen-16"])
+def test_large_workloads_sampled_items(name):
+    w = synth.WORKLOADS[name]
+    s = synth.draw_shapes(w)
+    lay = O.build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+    v = synth.draw_values(w.seed, lay.T, w.hq, w.hkv, w.head_dim, w.d_model, w.vocab,
+                          want=("hidden", "w_lm"))
+    rng = np.random.default_rng(w.seed)
+    items = sorted(set(rng.choice(lay.M, size=min(96, lay.M), replace=False).tolist()) | {0, lay.M - 1})
+    for labels in s.label_sets:
+        _check(v["hidden"], v["w_lm"], lay.delim_positions, labels.tolist(), items=items)
