@@ -130,6 +130,17 @@ def make_workload(name: str):
     return w, shapes, vals, T, M
 
 
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """The slowest rank's value (all ranks get it); identity without a group."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def useful_flops(pairs: int, hq: int, D: int) -> float:
     return 4.0 * hq * D * pairs
 
@@ -217,11 +228,7 @@ def run_ours(args, rank, world, dist):
     attn_ms = [r["a0"].elapsed_time(r["a1"]) for r in recs]
     score_ms = [r["a1"].elapsed_time(r["s1"]) for r in recs]
     total_ms = float(sum(step_ms))
-    if dist is not None:
-        import torch.distributed as tdist
-        tt = torch.tensor([total_ms], device=dev)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     ms_per_step = total_ms / args.steps
     items_per_s = world * M * args.steps / (total_ms / 1e3)
 
@@ -347,11 +354,7 @@ def run_e2e(args, w, shapes, vals, labels, dev, stream, dist, world):
         b.record(stream)
         torch.cuda.synchronize()
     ms = a.elapsed_time(b)
-    if dist is not None:
-        import torch.distributed as tdist
-        tt = torch.tensor([ms], device=dev)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, dist, dev)
     assert bool(torch.isfinite(out_host).all())
     return {"value": round(world * M * steps / (ms / 1e3), 1), "unit": "items/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
