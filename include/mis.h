@@ -229,6 +229,43 @@ mis_status_t mis_get_device_status(const void* workspace, void* stream);
  * Process-wide; returns the previous value. */
 uint64_t mis_set_wait_limit_ns(uint64_t ns);
 
+/* ------------------------------------------------------------------------
+ * Allocation-free label scoring. The pages have no counterpart of this call;
+ * it exists for callers that cannot call cudaMalloc, such as a plugin inside
+ * an inference engine that has already reserved all free device memory and
+ * offers no allocator, or a latency-critical path that must not take the
+ * device-wide synchronisation cudaMalloc/cudaFree can cause.
+ *
+ * Same inputs, outputs and results as mis_label_scores(), but no workspace:
+ * the scratch (gathered readout rows, per-chunk logsumexp pairs, label
+ * logits, status words) lives in one static device array of
+ * MIS_NOALLOC_SCRATCH_BYTES inside the library. The call allocates nothing
+ * and calls no allocating routine.
+ *   - Size limit: any (M, d, V, K) whose mis_label_scores_workspace_size() is
+ *     at most MIS_NOALLOC_SCRATCH_BYTES (for example M <= 512 items with
+ *     d <= 4096, V <= 262144, K <= 16); larger calls return
+ *     MIS_ERR_UNSUPPORTED before anything is enqueued.
+ *   - Every GPU that loads the library holds the array until process exit.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls on a device share the array, which keeps the last call's
+ *     contents. Calls that overlap on the GPU (different streams, or host
+ *     threads without ordering) race and corrupt each other's results;
+ *     serialise them on one stream.
+ *   - device_status: optional device uint32[2] that receives this call's
+ *     device status words after the kernels ([0] bit 1 = a wait timed out,
+ *     bit 2 = a readout row was outside [0, T); [1] = first failing site);
+ *     NULL skips the copy.
+ * ------------------------------------------------------------------------ */
+#define MIS_NOALLOC_SCRATCH_BYTES (8650752) /* 8.25 MiB */
+
+mis_status_t mis_label_scores_noalloc(const void* hidden, int64_t hidden_row_stride, int32_t T,
+                                      const void* w_lm, int32_t d, int32_t V,
+                                      const int32_t* delim_positions, int32_t M,
+                                      const int32_t* label_token_ids, int32_t K,
+                                      float* out_logprobs, float* out_renorm,
+                                      uint32_t* device_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

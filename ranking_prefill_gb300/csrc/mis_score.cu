@@ -30,6 +30,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "mis_internal.h"
 #include "mis_ptx.cuh"
@@ -358,3 +359,102 @@ mis_status_t launch_score(const ScoreArgs& a, void* stream) {
 }
 
 }  // namespace mis
+
+// ---------------------------------------------------------------------------
+// Allocation-free label scoring (mis_label_scores_noalloc).
+//
+// Some callers of this library cannot call cudaMalloc: for example a plugin
+// running inside an inference engine that has already reserved all free
+// device memory for its own pools (KV cache, activations) and hands out no
+// allocator, or a latency-critical path that must not pay the implicit
+// device-wide synchronisation cudaMalloc/cudaFree can cause. They cannot
+// provide the scoring workspace either, so this entry point keeps it in one
+// file-scope device array of MIS_NOALLOC_SCRATCH_BYTES instead.
+//
+// Costs and rules of that choice:
+//  * every GPU that loads this library holds the array until the process
+//    exits;
+//  * the device address is looked up once per device (cudaGetSymbolAddress,
+//    with that device current) on the first call made on that device, so
+//    make that first call before any stream capture;
+//  * all calls on a device share the array and it keeps the last call's
+//    contents: calls that overlap on the GPU (other streams, or host threads
+//    without stream ordering between them) race and corrupt each other.
+//    Each call clears the status words first and rewrites everything else it
+//    reads (gathered rows including the zero padding, every (item, chunk)
+//    pair, every label logit) before reading it.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MIS_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (set up once).
+mis_status_t noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MIS_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MIS_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return MIS_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return MIS_OK;
+}
+
+}  // namespace
+
+extern "C" mis_status_t mis_label_scores_noalloc(
+    const void* hidden, int64_t hidden_row_stride, int32_t T, const void* w_lm, int32_t d,
+    int32_t V, const int32_t* delim_positions, int32_t M, const int32_t* label_token_ids,
+    int32_t K, float* out_logprobs, float* out_renorm, uint32_t* device_status, void* stream) {
+  using namespace mis;
+  // the same argument rules as mis_label_scores
+  if (M < 0 || T < 1 || V < 1 || d < 1 || K < 1) return MIS_ERR_INVALID_ARG;
+  if (K > 16) return MIS_ERR_UNSUPPORTED;
+  if (d % 64 || d > 8192) return MIS_ERR_UNSUPPORTED;
+  if (!label_token_ids) return MIS_ERR_INVALID_ARG;
+  for (int l = 0; l < K; ++l)
+    if (label_token_ids[l] < 0 || label_token_ids[l] >= V) return MIS_ERR_INVALID_ARG;
+  auto misaligned = [](const void* p, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0;
+  };
+  if (M > 0) {
+    if (!hidden || !w_lm || !delim_positions || !out_logprobs) return MIS_ERR_INVALID_ARG;
+    if (misaligned(hidden, 16) || misaligned(w_lm, 16)) return MIS_ERR_INVALID_ARG;
+    if (misaligned(delim_positions, 4) || misaligned(out_logprobs, 4) ||
+        misaligned(out_renorm, 4) || misaligned(device_status, 4))
+      return MIS_ERR_INVALID_ARG;
+    if (hidden_row_stride < d || (hidden_row_stride & 7)) return MIS_ERR_SHAPE;
+  }
+  // sizes whose scratch would not fit the static array are refused
+  if (score_workspace_size(M, d, V, K) > (size_t)MIS_NOALLOC_SCRATCH_BYTES)
+    return MIS_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  mis_status_t st = noalloc_scratch(&scratch);
+  if (st != MIS_OK) return st;
+  ScoreArgs a;
+  a.hidden = hidden; a.hidden_stride = hidden_row_stride; a.T = T;
+  a.w_lm = w_lm; a.d = d; a.V = V;
+  a.delim = delim_positions; a.M = M;
+  for (int l = 0; l < 16; ++l) a.labels[l] = l < K ? label_token_ids[l] : -1;
+  a.K = K;
+  a.out_logprobs = out_logprobs; a.out_renorm = out_renorm;
+  a.workspace = scratch; a.ws_bytes = MIS_NOALLOC_SCRATCH_BYTES;
+  try {
+    st = launch_score(a, stream);
+  } catch (...) {
+    return MIS_ERR_CUDA;
+  }
+  if (st == MIS_OK && device_status &&
+      cudaMemcpyAsync(device_status, scratch, 2 * sizeof(uint32_t), cudaMemcpyDeviceToDevice,
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MIS_ERR_CUDA;
+  return st;
+}

@@ -32,7 +32,7 @@ EXPORTS = ["mis_status_string", "mis_abi_version", "mis_layout_size", "mis_build
            "mis_plan_workspace_size", "mis_plan_create", "mis_plan_get_stats",
            "mis_plan_tile_map", "mis_plan_destroy", "mis_attention_fwd_plan",
            "mis_attention_fwd", "mis_label_scores_workspace_size", "mis_label_scores",
-           "mis_get_device_status", "mis_set_wait_limit_ns"]
+           "mis_get_device_status", "mis_set_wait_limit_ns", "mis_label_scores_noalloc"]
 
 
 class MisError(RuntimeError):
@@ -89,6 +89,8 @@ def load(path: str = LIB_PATH):
                                        i32p, C.c_int32, vp, vp, vp, sz, vp]),
         "mis_get_device_status": (C.c_int, [vp, vp]),
         "mis_set_wait_limit_ns": (C.c_uint64, [C.c_uint64]),
+        "mis_label_scores_noalloc": (C.c_int, [vp, i64, C.c_int32, vp, C.c_int32, C.c_int32, vp,
+                                               C.c_int32, i32p, C.c_int32, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -297,6 +299,23 @@ def mis_label_scores(hidden, w_lm, delim_positions, label_token_ids: Sequence[in
                               _dptr(delim_positions), M, _ptr_i32(labels), len(labels),
                               _dptr(out_logprobs), _dptr(out_renorm), _dptr(workspace), nbytes,
                               _stream(stream)), "mis_label_scores")
+
+
+def mis_label_scores_noalloc(hidden, w_lm, delim_positions, label_token_ids: Sequence[int],
+                             out_logprobs, out_renorm=None, device_status=None,
+                             T: Optional[int] = None, stream=None):
+    """mis_label_scores without a workspace: for callers that cannot allocate
+    device memory. The library's static scratch is shared by every call on a
+    device, so calls must not overlap on the GPU."""
+    L = load()
+    labels = _i32(label_token_ids)
+    M = int(delim_positions.numel())
+    d, V = int(w_lm.shape[1]), int(w_lm.shape[0])
+    _check(L.mis_label_scores_noalloc(_dptr(hidden), hidden.stride(0),
+                                      int(hidden.shape[0]) if T is None else T, _dptr(w_lm), d, V,
+                                      _dptr(delim_positions), M, _ptr_i32(labels), len(labels),
+                                      _dptr(out_logprobs), _dptr(out_renorm), _dptr(device_status),
+                                      _stream(stream)), "mis_label_scores_noalloc")
 
 
 def mis_get_device_status(workspace, stream=None) -> int:
