@@ -229,6 +229,15 @@ mis_status_t mis_get_device_status(const void* workspace, void* stream);
  * Process-wide; returns the previous value. */
 uint64_t mis_set_wait_limit_ns(uint64_t ns);
 
+/* Failure injection for tests, without a GPU fault. While bit 0 (attention)
+ * or bit 1 (scoring) of `mask` is set, the tensor-core thread of every block
+ * launched by those calls first waits on a barrier that nothing arrives on,
+ * so the bounded wait runs out and the timeout path above runs for real:
+ * MIS_ERR_DEVICE_TIMEOUT in the workspace status, outputs not written, the
+ * context left usable. 0 (the default) turns it off. Process-wide; returns
+ * the previous mask. */
+uint32_t mis_inject_stall(uint32_t mask);
+
 /* ------------------------------------------------------------------------
  * Allocation-free label scoring. The pages have no counterpart of this call;
  * it exists for callers that cannot call cudaMalloc, such as a plugin inside

@@ -16,6 +16,7 @@ namespace mis {
 namespace {
 
 std::atomic<uint64_t> g_wait_limit_ns{200ull * 1000 * 1000};
+std::atomic<uint32_t> g_inject_stall{0};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
@@ -37,6 +38,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
+uint32_t inject_stall_mask() { return g_inject_stall.load(); }
 
 int num_sms() {
   int dev = 0, n = 0;
@@ -92,6 +94,8 @@ const char* mis_status_string(int status) {
 int mis_abi_version(void) { return MIS_ABI_VERSION; }
 
 uint64_t mis_set_wait_limit_ns(uint64_t ns) { return g_wait_limit_ns.exchange(ns); }
+
+uint32_t mis_inject_stall(uint32_t mask) { return g_inject_stall.exchange(mask); }
 
 size_t mis_plan_workspace_size(const mis_attn_desc* desc) {
   try {

@@ -11,15 +11,24 @@
 // of the former: attention work O(Lq^2 + N Lq Lbar) instead of the causal
 // O((Lq + N Lbar)^2)).
 //
-// One block = one (query tile, query head). Warp roles:
-//   warp 0     : TMA producer (Q once, then K/V tiles through a ring of stages)
-//   warp 1     : TMEM allocator and the single thread that issues tcgen05.mma
-//                  S = Q K^T  (SS: both operands in shared memory)
-//                  O += P V   (TS: P from tensor memory, V in shared memory)
-//   warps 4..7 : softmax, one TMEM lane (= one query row) per thread; the row
-//                max and sum stay inside the thread, so no shuffles are needed.
-// Tensor memory (512 columns): S0 | S1 | O | P0 | P1. S is double buffered so
-// the tensor core computes S_{t+1} while the softmax works on S_t.
+// One block = one query tile and a pair of query heads that share a kv head
+// (GQA), or one head when the group size is odd. The pair shares every K/V
+// tile the block loads. Warp roles (384 threads):
+//   warp 0      : TMA producer (both Q tiles once, then K and V tiles through
+//                 separate rings: K is released as soon as both S products
+//                 are issued, V after both PV products)
+//   warp 1      : TMEM allocator and the single thread issuing tcgen05.mma:
+//                   S_h = Q_h K^T  (SS: both operands in shared memory)
+//                   O_h += P_h V   (TS: P_h from tensor memory, V MN-major)
+//                 in the order S_0(j), PV_1(j-1), S_1(j), PV_0(j), so each
+//                 head's softmax overlaps the other head's products
+//   warps 4..7  : softmax of head 0, warps 8..11: softmax of head 1. One TMEM
+//                 lane (= one query row) per thread: the row max and sum stay
+//                 in the thread, no shuffles.
+// Tensor memory (512 columns): S_0 | S_1 | O_0 | O_1. P_h (bf16 pairs) is
+// written over the first half of S_h once S_h has been read. Because S_h(j)
+// is committed after PV_h(j-1) was issued, "S_h(j) ready" also means O_h and
+// the previous P_h are free, so the softmax never waits on a PV.
 // The running maximum is only moved (and O rescaled in TMEM) when it grows by
 // more than 2^8; the final division by the row sum makes the result exact for
 // any reference maximum.
@@ -27,7 +36,6 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
-#include <cstdio>
 
 #include "mis_internal.h"
 #include "mis_ptx.cuh"
@@ -43,16 +51,15 @@ using namespace dev;
 
 template <int D>
 struct AttnCfg {
-  static constexpr int kStages = (D == 128) ? 3 : 4;
   static constexpr int kBox = kBN * 64 * 2;            // one 64-column box, 128 rows: 16 KB
-  static constexpr int kQBytes = kBM * D * 2;
-  static constexpr int kTile = kBN * D * 2;            // K or V tile
-  static constexpr int kStageBytes = 2 * kTile;
-  static constexpr int kData = kQBytes + kStages * kStageBytes;
+  static constexpr int kTile = kBN * D * 2;            // a Q, K or V tile
+  static constexpr int kKStages = (D == 128) ? 3 : 4;
+  static constexpr int kVStages = (D == 128) ? 2 : 4;
+  static constexpr int kData = (2 + kKStages + kVStages) * kTile;
   static constexpr int kSmem = kData + 512 + 1024;     // barriers + alignment slack
 };
 
-constexpr uint32_t kColS0 = 0, kColO = 256, kColP0 = 384;
+constexpr int kThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -66,27 +73,40 @@ struct AttnParams {
   int64_t o_stride;
   int32_t T;
   int32_t group;        // Hq / Hkv
+  int32_t heads;        // query heads per block: 2 (a GQA pair) or 1
   float scale_log2;     // softmax scale * log2(e)
   uint32_t* status;
   uint64_t wait_ns;
+  uint32_t stall;       // failure injection: wait on a barrier nothing arrives on
 };
 
+// Visibility of key column c of a tile from a row, with a = row - c0 (last
+// visible column), pq = pend - c0 (columns below pq are the shared set Q),
+// lc = lo - c0 (first column of the row's own set).
+__device__ __forceinline__ bool visible(int c, int a, int pq, int lc) {
+  return c <= a && (c < pq || c >= lc);
+}
+
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
   using C = AttnCfg<D>;
-  constexpr int NS = C::kStages;
+  constexpr int KS = C::kKStages, VS = C::kVStages;
   constexpr int NB = D / 64;                          // 64-column boxes per row
+  // TMEM columns: S_t at 128 t, O_t at 256 + D t
+  auto colS = [](int t) { return (uint32_t)(t * 128); };
+  auto colO = [](int t) { return (uint32_t)(256 + t * D); };
   // barrier slots
-  constexpr int bQ = 0, bKVF = 1, bKVE = bKVF + NS, bSF = bKVE + NS, bPF = bSF + 2,
-                bOD = bPF + 2, bDR = bOD + 1, nBar = bDR + 1;
+  constexpr int bQ = 0, bKF = 1, bKE = bKF + KS, bVF = bKE + KS, bVE = bVF + VS,
+                bSF = bVE + VS, bPF = bSF + 2, bOF = bPF + 2, bDR = bOF + 1, nBar = bDR + 1;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint8_t* sQ = smem;
-  uint8_t* sKV = smem + C::kQBytes;
+  uint8_t* sQ = smem;                                  // 2 tiles
+  uint8_t* sK = smem + 2 * C::kTile;                   // KS tiles
+  uint8_t* sV = sK + KS * C::kTile;                    // VS tiles
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kData);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + nBar);
   volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -95,8 +115,9 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WorkItem wi = p.work[blockIdx.x];
-  const int h = blockIdx.y;
-  const int g = h / p.group;
+  const int nh = p.heads;
+  const int h0 = blockIdx.y * nh;                      // first query head of the block
+  const int g = h0 / p.group;                          // shared kv head
   const ReqInfo R = p.req[wi.req];
   const int nk = wi.nk;
 
@@ -104,9 +125,10 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
     *skip_flag = (*(volatile uint32_t*)p.status & kDevTimeout) ? 1u : 0u;
     *abort_flag = 0;
     mbar_init(bar(bQ), 1);
-    for (int s = 0; s < NS; ++s) { mbar_init(bar(bKVF + s), 1); mbar_init(bar(bKVE + s), 1); }
+    for (int s = 0; s < KS; ++s) { mbar_init(bar(bKF + s), 1); mbar_init(bar(bKE + s), 1); }
+    for (int s = 0; s < VS; ++s) { mbar_init(bar(bVF + s), 1); mbar_init(bar(bVE + s), 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(bar(bSF + s), 1); mbar_init(bar(bPF + s), 128); }
-    mbar_init(bar(bOD), 1);
+    mbar_init(bar(bOF), 1);
     mbar_init(bar(bDR), 1);
     fence_mbar_init();
     fence_proxy_async();
@@ -122,160 +144,189 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Waiter W{abort_flag, p.status, p.wait_ns};
-
+  if (warp < 4) {
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&qmap); tma_prefetch_desc(&kmap); tma_prefetch_desc(&vmap);
-      mbar_arrive_expect_tx(bar(bQ), C::kQBytes);
-      for (int b = 0; b < NB; ++b)
-        tma_load_3d(smem_u32(sQ + b * C::kBox), &qmap, bar(bQ), b * 64, h, wi.q0);
-      int issued = 0;
+      mbar_arrive_expect_tx(bar(bQ), nh * C::kTile);
+      for (int t = 0; t < nh; ++t)
+        for (int b = 0; b < NB; ++b)
+          tma_load_3d(smem_u32(sQ + t * C::kTile + b * C::kBox), &qmap, bar(bQ), b * 64, h0 + t,
+                      wi.q0);
+      int k_issued = 0, v_issued = 0;
       for (int it = 0; it < nk; ++it) {
-        const int st = it % NS;
-        if (it >= NS && !wait(bar(bKVE + st), ((it / NS) - 1) & 1, W, 0x100 + it)) break;
         const int32_t c0 = (int32_t)(p.klist[wi.kofs + it] & ~kNeedMask);
-        uint8_t* sK = sKV + st * C::kStageBytes;
-        uint8_t* sV = sK + C::kTile;
-        mbar_arrive_expect_tx(bar(bKVF + st), C::kStageBytes);
-        for (int b = 0; b < NB; ++b) {
-          tma_load_3d(smem_u32(sK + b * C::kBox), &kmap, bar(bKVF + st), b * 64, g, c0);
-          tma_load_3d(smem_u32(sV + b * C::kBox), &vmap, bar(bKVF + st), b * 64, g, c0);
-        }
-        issued = it + 1;
+        const int sk = it % KS, sv = it % VS;
+        if (it >= KS && !wait(bar(bKE + sk), ((it / KS) - 1) & 1, W, 0x100 + it)) break;
+        mbar_arrive_expect_tx(bar(bKF + sk), C::kTile);
+        for (int b = 0; b < NB; ++b)
+          tma_load_3d(smem_u32(sK + sk * C::kTile + b * C::kBox), &kmap, bar(bKF + sk), b * 64, g, c0);
+        k_issued = it + 1;
+        if (it >= VS && !wait(bar(bVE + sv), ((it / VS) - 1) & 1, W, 0x180 + it)) break;
+        mbar_arrive_expect_tx(bar(bVF + sv), C::kTile);
+        for (int b = 0; b < NB; ++b)
+          tma_load_3d(smem_u32(sV + sv * C::kTile + b * C::kBox), &vmap, bar(bVF + sv), b * 64, g, c0);
+        v_issued = it + 1;
       }
       // drain: every copy this thread started has landed before the block exits
       wait_drain(bar(bQ), 0);
-      for (int i = (issued > NS ? issued - NS : 0); i < issued; ++i)
-        wait_drain(bar(bKVF + i % NS), (i / NS) & 1);
+      for (int i = (k_issued > KS ? k_issued - KS : 0); i < k_issued; ++i)
+        wait_drain(bar(bKF + i % KS), (i / KS) & 1);
+      for (int i = (v_issued > VS ? v_issued - VS : 0); i < v_issued; ++i)
+        wait_drain(bar(bVF + i % VS), (i / VS) & 1);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16(128, kBN, false);
       constexpr uint32_t idO = idesc_bf16(128, D, true);
-      const uint32_t aQ = smem_u32(sQ);
-      bool ok = wait(bar(bQ), 0, W, 0x200);
-      auto issue_s = [&](int it) -> bool {
-        const int st = it % NS;
-        if (!wait(bar(bKVF + st), (it / NS) & 1, W, 0x300 + it)) return false;
-        tc_fence_after();
-        const uint32_t aK = smem_u32(sKV + st * C::kStageBytes);
-        const uint32_t dS = tmem + kColS0 + (it & 1) * 128;
+      bool ok = true;
+      if (p.stall) ok = wait(bar(bDR), 0, W, 0x7ff);   // nothing arrives before the drain
+      if (ok) ok = wait(bar(bQ), 0, W, 0x200);
+      auto issue_s = [&](int t, int sk) {
+        const uint32_t aQ = smem_u32(sQ + t * C::kTile);
+        const uint32_t aK = smem_u32(sK + sk * C::kTile);
 #pragma unroll
         for (int b = 0; b < NB; ++b)
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t da = sdesc_sw128(aQ + b * C::kBox + ks * 32, 16, 1024);
-            const uint64_t db = sdesc_sw128(aK + b * C::kBox + ks * 32, 16, 1024);
-            mma_ss(dS, da, db, idS, (b | ks) != 0);
-          }
-        mma_commit(bar(bSF + (it & 1)));
-        return true;
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ss(tmem + colS(t), sdesc_sw128(aQ + b * C::kBox + ks * 32, 16, 1024),
+                   sdesc_sw128(aK + b * C::kBox + ks * 32, 16, 1024), idS, (b | ks) != 0);
+        mma_commit(bar(bSF + t));
       };
-      if (ok) ok = issue_s(0);
-      for (int it = 0; ok && it < nk; ++it) {
-        if (it + 1 < nk && !issue_s(it + 1)) break;
-        if (!wait(bar(bPF + (it & 1)), (it >> 1) & 1, W, 0x400 + it)) break;
-        tc_fence_after();
-        const int st = it % NS;
-        const uint32_t aV = smem_u32(sKV + st * C::kStageBytes + C::kTile);
-        const uint32_t aP = tmem + kColP0 + (it & 1) * 64;
+      auto issue_pv = [&](int t, int sv, bool acc) {
+        const uint32_t aV = smem_u32(sV + sv * C::kTile);
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks) {
           // V is MN-major (head dim contiguous): 8-key groups 1024 B apart,
-          // 64-column boxes kBox apart.
+          // 64-column boxes kBox apart. P_h sits in the first columns of S_h.
           const uint64_t db = sdesc_sw128(aV + ks * 16 * 128, C::kBox, 1024);
-          mma_ts(tmem + kColO, aP + ks * 8, db, idO, (it | ks) != 0);
+          mma_ts(tmem + colO(t), tmem + colS(t) + ks * 8, db, idO, (acc || ks != 0) ? 1u : 0u);
         }
-        mma_commit(bar(bKVE + st));
-        mma_commit(bar(bOD));
+      };
+      for (int it = 0; ok && it < nk; ++it) {
+        const int sk = it % KS, sv = it % VS;
+        if (!(ok = wait(bar(bKF + sk), (it / KS) & 1, W, 0x300 + it))) break;
+        tc_fence_after();
+        issue_s(0, sk);
+        if (nh == 2) {
+          if (it > 0) {
+            if (!(ok = wait(bar(bPF + 1), (it - 1) & 1, W, 0x400 + it))) break;
+            tc_fence_after();
+            issue_pv(1, (it - 1) % VS, it - 1 > 0);
+            mma_commit(bar(bVE + (it - 1) % VS));
+          }
+          issue_s(1, sk);
+        }
+        mma_commit(bar(bKE + sk));
+        if (!(ok = wait(bar(bVF + sv), (it / VS) & 1, W, 0x480 + it))) break;
+        if (!(ok = wait(bar(bPF + 0), it & 1, W, 0x500 + it))) break;
+        tc_fence_after();
+        issue_pv(0, sv, it > 0);
+        if (nh == 1) mma_commit(bar(bVE + sv));
       }
+      if (ok && nh == 2 && nk > 0) {
+        if (wait(bar(bPF + 1), (nk - 1) & 1, W, 0x580)) {
+          tc_fence_after();
+          issue_pv(1, (nk - 1) % VS, nk - 1 > 0);
+          mma_commit(bar(bVE + (nk - 1) % VS));
+        }
+      }
+      mma_commit(bar(bOF));
       // drain: all tensor-core work of this thread completes before dealloc
       mma_commit(bar(bDR));
       wait_drain(bar(bDR), 0);
     }
-  } else if (warp >= 4) {
+  }
+  } else {
+  if ((warp - 4) / 4 < nh) {
     // ------------------------------------------------------------- softmax
-    const int sw = warp - 4;
+    const int t = (warp - 4) / 4;                       // head of the pair
+    const int h = h0 + t;
+    const int sw = warp & 3;
     const int r = sw * 32 + lane;
     const int j = wi.q0 + r;
     const bool valid = j < R.e0;
-    const int jj = valid ? j : -1;                    // invalid rows see nothing
+    const int jj = valid ? j : -1;                      // invalid rows see nothing
     const int lo = valid ? p.seg_start[j] : 0x7fffffff;
     const uint32_t tl = tmem + ((uint32_t)(sw * 32) << 16);
+    const uint32_t tS = tl + colS(t), tO = tl + colO(t);
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int it = 0; it < nk; ++it) {
       const uint32_t e = p.klist[wi.kofs + it];
       const int32_t c0 = (int32_t)(e & ~kNeedMask);
-      const int b = it & 1;
-      ok = wait(bar(bSF + b), (it >> 1) & 1, W, 0x500 + it);
+      const bool masked = (e & kNeedMask) != 0;
+      const int a = jj - c0, pq = R.pend - c0, lc = lo - c0;
+      ok = wait(bar(bSF + t), it & 1, W, 0x600 + it);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
+      // the whole S row in registers: one load round trip per tile
       uint32_t su[kBN];
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) tmem_ld32(tl + kColS0 + b * 128 + c * 32, su + c * 32);
+      for (int c = 0; c < kBN / 32; ++c) tmem_ld32(tS + c * 32, su + c * 32);
       tmem_ld_wait();
-      if (e & kNeedMask) {
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          const int k = c0 + c;
-          const bool vis = (k <= jj) && (k < R.pend || k >= lo);
-          su[c] = vis ? su[c] : 0xff800000u;          // -inf
-        }
+      for (int c = 0; c < kBN / 32; ++c) reg_fence32(su + c * 32);
+      if (masked) {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c)
+          if (!visible(c, a, pq, lc)) su[c] = 0xff800000u;           // -inf
       }
-      float mx = __uint_as_float(su[0]);
+      // row max: eight independent chains
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, __uint_as_float(su[c]));
+      for (int x = 0; x < 8; ++x) mx8[x] = __uint_as_float(su[x]);
+#pragma unroll
+      for (int c = 8; c < kBN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(su[c]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m_ref, mx * sl2);
       const bool grow = m_new > m_ref + kRescaleThreshold;
-      // PV of the previous tile must be done before O is touched; waiting on
-      // every completion in turn also keeps this barrier's parity in step.
-      if (it > 0) {
-        ok = wait(bar(bOD), (it - 1) & 1, W, 0x600 + it);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-      }
-      if (__any_sync(0xffffffffu, grow)) {
-        const float alpha = grow ? ex2(m_ref - m_new) : 1.f;
-        if (it > 0) {
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(tl + kColO + c * 32, ov);
-            tmem_ld_wait();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * alpha);
-            tmem_st32(tl + kColO + c * 32, ov);
-          }
-          tmem_st_wait();
-        }
-        if (grow) { l *= alpha; m_ref = m_new; }
-      }
+      const bool any_grow = __any_sync(0xffffffffu, grow);
+      const float alpha = grow ? ex2(m_ref - m_new) : 1.f;
+      if (grow) { l *= alpha; m_ref = m_new; }
       const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float rs = 0.f;
-      uint32_t pk[kBN / 2];
+      // P = 2^(s*scale*log2e - m) as bf16 pairs over the first half of S_h
+      float rs8[8];
 #pragma unroll
-      for (int c = 0; c < kBN / 2; ++c) {
-        const float p0 = ex2(fmaf(__uint_as_float(su[2 * c]), sl2, -mb));
-        const float p1 = ex2(fmaf(__uint_as_float(su[2 * c + 1]), sl2, -mb));
-        rs += p0 + p1;
-        pk[c] = pack_bf16(p0, p1);
+      for (int x = 0; x < 8; ++x) rs8[x] = 0.f;
+#pragma unroll
+      for (int hf = 0; hf < kBN / 64; ++hf) {        // 64 columns -> 32 packed words
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = ex2(fmaf(__uint_as_float(su[hf * 64 + 2 * c]), sl2, -mb));
+          const float p1 = ex2(fmaf(__uint_as_float(su[hf * 64 + 2 * c + 1]), sl2, -mb));
+          rs8[c & 7] += p0 + p1;
+          pk[c] = pack_bf16(p0, p1);
+        }
+        tmem_st32(tS + hf * 32, pk);
       }
-      l += rs;
+      l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      if (any_grow && it > 0) {
+        // O_h holds the products up to tile it-1, all complete (see above);
+        // it is rescaled after P so that O and S are never live together
 #pragma unroll
-      for (int c = 0; c < kBN / 64; ++c)
-        tmem_st32(tl + kColP0 + b * 64 + c * 32, pk + c * 32);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tO + c * 32, ov);
+          tmem_ld_wait();
+          reg_fence32(ov);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * alpha);
+          tmem_st32(tO + c * 32, ov);
+        }
+      }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(bPF + b));
+      mbar_arrive(bar(bPF + t));
     }
     if (ok) {
-      ok = wait(bar(bOD), (nk - 1) & 1, W, 0x700);
+      ok = wait(bar(bOF), 0, W, 0x700);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
@@ -285,8 +336,9 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
-        tmem_ld32(tl + kColO + c * 32, ov);
+        tmem_ld32(tO + c * 32, ov);
         tmem_ld_wait();
+        reg_fence32(ov);
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
@@ -303,9 +355,11 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
       if (p.lse && valid) p.lse[(int64_t)h * p.T + j] = (m_ref + log2f(l)) * kLn2;
     }
   }
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -338,9 +392,11 @@ mis_status_t launch_d(const HostPlan& pl, const void* q, const void* k, const vo
   prm.o_stride = os;
   prm.T = pl.T;
   prm.group = pl.Hq / pl.Hkv;
+  prm.heads = (prm.group % 2 == 0) ? 2 : 1;
   prm.scale_log2 = pl.scale * 1.4426950408889634f;
   prm.status = reinterpret_cast<uint32_t*>(ws);
   prm.wait_ns = wait_limit_ns();
+  prm.stall = inject_stall_mask() & 1u;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return MIS_ERR_CUDA;
@@ -349,8 +405,8 @@ mis_status_t launch_d(const HostPlan& pl, const void* q, const void* k, const vo
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
       cudaSuccess)
     return MIS_ERR_CUDA;
-  dim3 grid((unsigned)pl.work.size(), (unsigned)pl.Hq);
-  kern<<<grid, 256, C::kSmem, st>>>(qm, km, vm, prm);
+  dim3 grid((unsigned)pl.work.size(), (unsigned)(pl.Hq / prm.heads));
+  kern<<<grid, kThreads, C::kSmem, st>>>(qm, km, vm, prm);
   return cudaGetLastError() == cudaSuccess ? MIS_OK : MIS_ERR_CUDA;
 }
 

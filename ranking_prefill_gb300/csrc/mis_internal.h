@@ -59,6 +59,8 @@ int num_sms();
 
 // Process-wide wait limit for the kernels' bounded waits.
 uint64_t wait_limit_ns();
+// Process-wide failure-injection mask (bit 0: attention, bit 1: scoring).
+uint32_t inject_stall_mask();
 
 // Kernel launchers (defined in the .cu files). Return MIS_ERR_CUDA on launch
 // failure. Pointers are already validated.

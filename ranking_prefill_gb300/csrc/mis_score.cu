@@ -83,6 +83,7 @@ struct ScoreParams {
   float* zlab;        // [m_pad][K] label logits
   uint32_t* status;
   uint64_t wait_ns;
+  uint32_t stall;     // failure injection: wait on a barrier nothing arrives on
 };
 
 // ------------------------------------------------------------------ gather
@@ -175,6 +176,7 @@ mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(kItemTile, kVocabTile, false);
       bool ok = true;
+      if (p.stall) ok = wait(bar(bDR), 0, W, 0x7ff);   // nothing arrives before the drain
       for (int ti = 0; ok && ti < nt; ++ti) {
         const int buf = ti & 1;
         if (ti >= 2 && !wait(bar(bAE + buf), ((ti >> 1) - 1) & 1, W, 0x200)) break;
@@ -218,6 +220,7 @@ mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
         uint32_t zr[32];
         tmem_ld32(tacc + c * 32, zr);
         tmem_ld_wait();
+        reg_fence32(zr);
         const int vbase = v0 + c * 32;
         float cm = -INFINITY;
 #pragma unroll
@@ -238,8 +241,9 @@ mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
       for (int l = 0; l < p.K; ++l) {
         const int lab = p.labels[l];
         if (lab >= v0 && lab < v0 + kVocabTile) {
-          const uint32_t z = tmem_ld1(tacc + (lab - v0));
+          uint32_t z = tmem_ld1(tacc + (lab - v0));
           tmem_ld_wait();
+          reg_fence1(z);
           if (item < p.M) p.zlab[(int64_t)item * p.K + l] = __uint_as_float(z);
         }
       }
@@ -255,37 +259,51 @@ mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
 // ----------------------------------------------------------------- combine
+// One warp per item: lanes stride over the vocab chunks, then merge their
+// (max, sum) pairs with shuffles.
 __global__ void __launch_bounds__(128)
 mis_score_combine_kernel(const ScoreParams p, float* __restrict__ out,
                          float* __restrict__ renorm) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int i = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
   if (i >= p.M) return;
   if (*(volatile uint32_t*)p.status & kDevTimeout) return;
-  const float* pp = p.part + (int64_t)i * p.n_chunks * 2;
+  const float2* pp = reinterpret_cast<const float2*>(p.part) + (int64_t)i * p.n_chunks;
   float m = -INFINITY, s = 0.f;
-  for (int c = 0; c < p.n_chunks; ++c) {
-    const float mc = pp[2 * c], sc = pp[2 * c + 1];
-    if (mc == -INFINITY) continue;
-    if (mc > m) { s = s * exp2f(m - mc) + sc; m = mc; }
-    else s += sc * exp2f(mc - m);
+  for (int c = lane; c < p.n_chunks; c += 32) {
+    const float2 e = pp[c];
+    if (e.x == -INFINITY) continue;
+    if (e.x > m) { s = s * exp2f(m - e.x) + e.y; m = e.x; }
+    else s += e.y * exp2f(e.x - m);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float mo = __shfl_xor_sync(0xffffffffu, m, off);
+    const float so = __shfl_xor_sync(0xffffffffu, s, off);
+    const float mm = fmaxf(m, mo);
+    if (mm != -INFINITY) s = s * exp2f(m - mm) + so * exp2f(mo - mm);
+    m = mm;
   }
   const float lse = (m + log2f(s)) * kLn2;
   const float* zl = p.zlab + (int64_t)i * p.K;
-  float zmax = -INFINITY;
-  for (int l = 0; l < p.K; ++l) {
-    out[(int64_t)i * p.K + l] = zl[l] - lse;
-    zmax = fmaxf(zmax, zl[l]);
-  }
+  if (lane < p.K) out[(int64_t)i * p.K + lane] = zl[lane] - lse;
   if (renorm) {
-    float den = 0.f;
-    for (int l = 0; l < p.K; ++l) den += expf(zl[l] - zmax);
-    for (int l = 0; l < p.K; ++l) renorm[(int64_t)i * p.K + l] = expf(zl[l] - zmax) / den;
+    const float z = lane < p.K ? zl[lane] : -INFINITY;
+    float zmax = z;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, off));
+    float e = lane < p.K ? expf(z - zmax) : 0.f;
+    float den = e;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    if (lane < p.K) renorm[(int64_t)i * p.K + lane] = e / den;
   }
 }
 
@@ -348,13 +366,14 @@ mis_status_t launch_score(const ScoreArgs& a, void* stream) {
   p.zlab = reinterpret_cast<float*>(ws + L.zlab);
   p.status = status;
   p.wait_ns = wait_limit_ns();
+  p.stall = (inject_stall_mask() >> 1) & 1u;
 
   if (cudaFuncSetAttribute(mis_score_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmem) != cudaSuccess)
     return MIS_ERR_CUDA;
   mis_score_partial_kernel<<<dim3(n_mtiles, p.n_chunks), 256, kSmem, st>>>(am, wm, p);
   if (cudaGetLastError() != cudaSuccess) return MIS_ERR_CUDA;
-  mis_score_combine_kernel<<<(a.M + 127) / 128, 128, 0, st>>>(p, a.out_logprobs, a.out_renorm);
+  mis_score_combine_kernel<<<(a.M + 3) / 4, 128, 0, st>>>(p, a.out_logprobs, a.out_renorm);
   return cudaGetLastError() == cudaSuccess ? MIS_OK : MIS_ERR_CUDA;
 }
 

@@ -32,7 +32,8 @@ EXPORTS = ["mis_status_string", "mis_abi_version", "mis_layout_size", "mis_build
            "mis_plan_workspace_size", "mis_plan_create", "mis_plan_get_stats",
            "mis_plan_tile_map", "mis_plan_destroy", "mis_attention_fwd_plan",
            "mis_attention_fwd", "mis_label_scores_workspace_size", "mis_label_scores",
-           "mis_get_device_status", "mis_set_wait_limit_ns", "mis_label_scores_noalloc"]
+           "mis_get_device_status", "mis_set_wait_limit_ns", "mis_label_scores_noalloc",
+           "mis_inject_stall"]
 
 
 class MisError(RuntimeError):
@@ -89,6 +90,7 @@ def load(path: str = LIB_PATH):
                                        i32p, C.c_int32, vp, vp, vp, sz, vp]),
         "mis_get_device_status": (C.c_int, [vp, vp]),
         "mis_set_wait_limit_ns": (C.c_uint64, [C.c_uint64]),
+        "mis_inject_stall": (C.c_uint32, [C.c_uint32]),
         "mis_label_scores_noalloc": (C.c_int, [vp, i64, C.c_int32, vp, C.c_int32, C.c_int32, vp,
                                                C.c_int32, i32p, C.c_int32, vp, vp, vp, vp]),
     }
@@ -324,6 +326,10 @@ def mis_get_device_status(workspace, stream=None) -> int:
 
 def mis_set_wait_limit_ns(ns: int) -> int:
     return int(load().mis_set_wait_limit_ns(int(ns)))
+
+
+def mis_inject_stall(mask: int) -> int:
+    return int(load().mis_inject_stall(int(mask)))
 
 
 def mis_status_string(st: int) -> str:
