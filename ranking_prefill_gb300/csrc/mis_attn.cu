@@ -74,18 +74,12 @@ struct AttnParams {
   int32_t T;
   int32_t group;        // Hq / Hkv
   int32_t heads;        // query heads per block: 2 (a GQA pair) or 1
+  int32_t n_head_groups;  // Hq / heads
   float scale_log2;     // softmax scale * log2(e)
   uint32_t* status;
   uint64_t wait_ns;
   uint32_t stall;       // failure injection: wait on a barrier nothing arrives on
 };
-
-// Visibility of key column c of a tile from a row, with a = row - c0 (last
-// visible column), pq = pend - c0 (columns below pq are the shared set Q),
-// lc = lo - c0 (first column of the row's own set).
-__device__ __forceinline__ bool visible(int c, int a, int pq, int lc) {
-  return c <= a && (c < pq || c >= lc);
-}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -114,9 +108,13 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const WorkItem wi = p.work[blockIdx.x];
+  // 1-D grid: consecutive blocks take the head groups of one query tile, and
+  // query tiles come in longest-first order, so blocks start in
+  // longest-processing-time order across all heads
+  const int n_groups = p.n_head_groups;
+  const WorkItem wi = p.work[blockIdx.x / n_groups];
   const int nh = p.heads;
-  const int h0 = blockIdx.y * nh;                      // first query head of the block
+  const int h0 = (blockIdx.x % n_groups) * nh;         // first query head of the block
   const int g = h0 / p.group;                          // shared kv head
   const ReqInfo R = p.req[wi.req];
   const int nk = wi.nk;
@@ -255,11 +253,12 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
+    uint32_t e_next = nk > 0 ? p.klist[wi.kofs] : 0u;
     for (int it = 0; it < nk; ++it) {
-      const uint32_t e = p.klist[wi.kofs + it];
+      const uint32_t e = e_next;
+      if (it + 1 < nk) e_next = p.klist[wi.kofs + it + 1];   // prefetch the next entry
       const int32_t c0 = (int32_t)(e & ~kNeedMask);
       const bool masked = (e & kNeedMask) != 0;
-      const int a = jj - c0, pq = R.pend - c0, lc = lo - c0;
       ok = wait(bar(bSF + t), it & 1, W, 0x600 + it);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -272,41 +271,53 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
       for (int c = 0; c < kBN / 32; ++c) reg_fence32(su + c * 32);
       if (masked) {
+        // visible columns of this row: [0, min(row, pend-1) - c0] of the shared
+        // set and [lo - c0, row - c0] of its own set, as 4 words of bits
+        const int a1 = jj - c0 + 1, q1 = min(a1, R.pend - c0), lc = lo - c0;
 #pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (!visible(c, a, pq, lc)) su[c] = 0xff800000u;           // -inf
+        for (int w = 0; w < kBN / 32; ++w) {
+          const uint32_t vis = bit_range(-32 * w, q1 - 32 * w) | bit_range(lc - 32 * w, a1 - 32 * w);
+#pragma unroll
+          for (int x = 0; x < 32; ++x)
+            if (!((vis >> x) & 1u)) su[w * 32 + x] = 0xff800000u;     // -inf
+        }
       }
-      // row max: eight independent chains
-      float mx8[8];
+      // row max: three-input max, four independent chains
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int x = 0; x < 8; ++x) mx8[x] = __uint_as_float(su[x]);
-#pragma unroll
-      for (int c = 8; c < kBN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(su[c]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int c = 0; c < kBN; c += 2)
+        mx4[(c >> 1) & 3] = max3(mx4[(c >> 1) & 3], __uint_as_float(su[c]), __uint_as_float(su[c + 1]));
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float m_new = fmaxf(m_ref, mx * sl2);
       const bool grow = m_new > m_ref + kRescaleThreshold;
       const bool any_grow = __any_sync(0xffffffffu, grow);
       const float alpha = grow ? ex2(m_ref - m_new) : 1.f;
       if (grow) { l *= alpha; m_ref = m_new; }
       const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // P = 2^(s*scale*log2e - m) as bf16 pairs over the first half of S_h
-      float rs8[8];
-#pragma unroll
-      for (int x = 0; x < 8; ++x) rs8[x] = 0.f;
+      // P = 2^(s*scale*log2e - m) as bf16 pairs over the first half of S_h;
+      // scale/shift and the row sum run on packed fp32 pairs
+      const uint64_t sl2x2 = f2_pack(__float_as_uint(sl2), __float_as_uint(sl2));
+      const uint64_t nmbx2 = f2_pack(__float_as_uint(-mb), __float_as_uint(-mb));
+      uint64_t rs4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int hf = 0; hf < kBN / 64; ++hf) {        // 64 columns -> 32 packed words
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float p0 = ex2(fmaf(__uint_as_float(su[hf * 64 + 2 * c]), sl2, -mb));
-          const float p1 = ex2(fmaf(__uint_as_float(su[hf * 64 + 2 * c + 1]), sl2, -mb));
-          rs8[c & 7] += p0 + p1;
+          const int k2 = hf * 64 + 2 * c;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(su[k2], su[k2 + 1]), sl2x2, nmbx2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          rs4[c & 3] = f2_add(rs4[c & 3], f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
           pk[c] = pack_bf16(p0, p1);
         }
         tmem_st32(tS + hf * 32, pk);
       }
-      l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      {
+        float a0, a1;
+        f2_unpack(f2_add(f2_add(rs4[0], rs4[1]), f2_add(rs4[2], rs4[3])), a0, a1);
+        l += a0 + a1;
+      }
       if (any_grow && it > 0) {
         // O_h holds the products up to tile it-1, all complete (see above);
         // it is rescaled after P so that O and S are never live together
@@ -393,6 +404,7 @@ mis_status_t launch_d(const HostPlan& pl, const void* q, const void* k, const vo
   prm.T = pl.T;
   prm.group = pl.Hq / pl.Hkv;
   prm.heads = (prm.group % 2 == 0) ? 2 : 1;
+  prm.n_head_groups = pl.Hq / prm.heads;
   prm.scale_log2 = pl.scale * 1.4426950408889634f;
   prm.status = reinterpret_cast<uint32_t*>(ws);
   prm.wait_ns = wait_limit_ns();
@@ -405,7 +417,9 @@ mis_status_t launch_d(const HostPlan& pl, const void* q, const void* k, const vo
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
       cudaSuccess)
     return MIS_ERR_CUDA;
-  dim3 grid((unsigned)pl.work.size(), (unsigned)(pl.Hq / prm.heads));
+  const int64_t blocks = (int64_t)pl.work.size() * prm.n_head_groups;
+  if (blocks > 0x7fffffff) return MIS_ERR_UNSUPPORTED;
+  dim3 grid((unsigned)blocks);
   kern<<<grid, kThreads, C::kSmem, st>>>(qm, km, vm, prm);
   return cudaGetLastError() == cudaSuccess ? MIS_OK : MIS_ERR_CUDA;
 }
