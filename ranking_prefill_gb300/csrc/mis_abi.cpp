@@ -8,6 +8,8 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <utility>
+#include <vector>
 
 #include "mis_internal.h"
 
@@ -48,11 +50,46 @@ int num_sms() {
   return n;
 }
 
+namespace {
+
+// A few recently encoded tensor maps (the LM head, a layer's Q/K/V buffers
+// are reused call after call); encoding is pure host work, so a hit only
+// saves time and a miss re-encodes.
+struct TmapKey {
+  const void* base;
+  int rank;
+  uint64_t dims[3], strides[2];
+  uint32_t box[3];
+  bool operator==(const TmapKey& o) const {
+    return base == o.base && rank == o.rank && std::memcmp(dims, o.dims, sizeof(dims)) == 0 &&
+           std::memcmp(strides, o.strides, sizeof(strides)) == 0 &&
+           std::memcmp(box, o.box, sizeof(box)) == 0;
+  }
+};
+constexpr int kTmapCache = 16;
+std::mutex g_tmap_mu;
+TmapKey g_tmap_key[kTmapCache];
+CUtensorMap g_tmap_val[kTmapCache];
+int g_tmap_n = 0, g_tmap_next = 0;
+
+}  // namespace
+
 // bf16 tiled tensor map with 128-byte swizzle; dims/box innermost first.
 CUtensorMap make_tmap_bf16(const void* base, int rank, const uint64_t* dims,
                            const uint64_t* strides_bytes, const uint32_t* box, bool* ok) {
   CUtensorMap m;
   std::memset(&m, 0, sizeof(m));
+  TmapKey key;
+  std::memset(&key, 0, sizeof(key));
+  key.base = base;
+  key.rank = rank;
+  for (int i = 0; i < rank && i < 3; ++i) { key.dims[i] = dims[i]; key.box[i] = box[i]; }
+  for (int i = 0; i + 1 < rank && i < 2; ++i) key.strides[i] = strides_bytes[i];
+  {
+    std::lock_guard<std::mutex> lock(g_tmap_mu);
+    for (int i = 0; i < g_tmap_n; ++i)
+      if (g_tmap_key[i] == key) return g_tmap_val[i];
+  }
   auto fn = encode_fn();
   if (!fn) { *ok = false; return m; }
   cuuint64_t gd[5];
@@ -63,8 +100,33 @@ CUtensorMap make_tmap_bf16(const void* base, int rank, const uint64_t* dims,
   CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
                   gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) *ok = false;
+  if (r != CUDA_SUCCESS) {
+    *ok = false;
+    return m;
+  }
+  std::lock_guard<std::mutex> lock(g_tmap_mu);
+  g_tmap_key[g_tmap_next] = key;
+  g_tmap_val[g_tmap_next] = m;
+  g_tmap_next = (g_tmap_next + 1) % kTmapCache;
+  if (g_tmap_n < kTmapCache) ++g_tmap_n;
   return m;
+}
+
+bool kernel_attr_once(const void* kernel, int smem_bytes) {
+  // cudaFuncSetAttribute is per device; remember which (kernel, device) pairs
+  // are done
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  for (auto& d : done)
+    if (d.first == kernel && d.second == dev) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
+      cudaSuccess)
+    return false;
+  done.emplace_back(kernel, dev);
+  return true;
 }
 
 }  // namespace mis

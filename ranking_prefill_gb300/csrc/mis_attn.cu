@@ -107,6 +107,8 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   volatile uint32_t* skip_flag = tmem_slot + 2;
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
+  griddep_wait();                 // inputs of earlier stream work are visible
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // 1-D grid: consecutive blocks take the head groups of one query tile, and
   // query tiles come in longest-first order, so blocks start in
@@ -125,7 +127,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
     mbar_init(bar(bQ), 1);
     for (int s = 0; s < KS; ++s) { mbar_init(bar(bKF + s), 1); mbar_init(bar(bKE + s), 1); }
     for (int s = 0; s < VS; ++s) { mbar_init(bar(bVF + s), 1); mbar_init(bar(bVE + s), 1); }
-    for (int s = 0; s < 2; ++s) { mbar_init(bar(bSF + s), 1); mbar_init(bar(bPF + s), 128); }
+    for (int s = 0; s < 2; ++s) { mbar_init(bar(bSF + s), 1); mbar_init(bar(bPF + s), 4); }
     mbar_init(bar(bOF), 1);
     mbar_init(bar(bDR), 1);
     fence_mbar_init();
@@ -334,7 +336,8 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(bPF + t));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(bPF + t));         // one arrival per warp
     }
     if (ok) {
       ok = wait(bar(bOF), 0, W, 0x700);
@@ -414,14 +417,13 @@ mis_status_t launch_d(const HostPlan& pl, const void* q, const void* k, const vo
   if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return MIS_ERR_CUDA;
   if (pl.work.empty()) return MIS_OK;
   auto kern = mis_attn_fwd_kernel<D>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
-      cudaSuccess)
-    return MIS_ERR_CUDA;
+  if (!kernel_attr_once(reinterpret_cast<const void*>(kern), C::kSmem)) return MIS_ERR_CUDA;
   const int64_t blocks = (int64_t)pl.work.size() * prm.n_head_groups;
   if (blocks > 0x7fffffff) return MIS_ERR_UNSUPPORTED;
   dim3 grid((unsigned)blocks);
-  kern<<<grid, kThreads, C::kSmem, st>>>(qm, km, vm, prm);
-  return cudaGetLastError() == cudaSuccess ? MIS_OK : MIS_ERR_CUDA;
+  return launch_pdl(kern, grid, dim3(kThreads), C::kSmem, st, qm, km, vm, prm) == cudaSuccess
+             ? MIS_OK
+             : MIS_ERR_CUDA;
 }
 
 }  // namespace

@@ -4,7 +4,10 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <vector>
+
+#include <cuda_runtime.h>
 
 #include "../../include/mis.h"
 
@@ -56,6 +59,28 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p);
 
 // Per-device properties the launchers need (cached).
 int num_sms();
+
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel in the stream drains; every kernel of this library calls
+// griddepcontrol.wait before it touches global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device.
+bool kernel_attr_once(const void* kernel, int smem_bytes);
 
 // Process-wide wait limit for the kernels' bounded waits.
 uint64_t wait_limit_ns();

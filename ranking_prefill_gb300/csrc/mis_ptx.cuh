@@ -95,6 +95,18 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
     if (globaltimer() - t0 > 20000000ull) break;
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// Wait until every grid this launch depends on has completed and its writes
+// are visible; a no-op when the kernel was launched without the attribute.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the next kernel in the stream start launching (it still waits for this
+// grid's completion in its own griddep_wait()).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

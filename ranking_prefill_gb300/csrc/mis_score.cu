@@ -91,6 +91,8 @@ __global__ void __launch_bounds__(128)
 mis_gather_rows_kernel(const __nv_bfloat16* __restrict__ hidden, int64_t stride, int32_t T,
                        const int32_t* __restrict__ rows, int32_t M, int32_t d,
                        __nv_bfloat16* __restrict__ out, uint32_t* status) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int i = blockIdx.x;
   int32_t r = -1;
   if (i < M) {
@@ -114,6 +116,8 @@ mis_gather_rows_kernel(const __nv_bfloat16* __restrict__ hidden, int64_t stride,
 __global__ void __launch_bounds__(256, 1)
 mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
                          const __grid_constant__ CUtensorMap wmap, const ScoreParams p) {
+  griddep_wait();
+  griddep_launch_dependents();
   constexpr int bF = 0, bE = kStages, bAF = 2 * kStages, bAE = bAF + 2, bDR = bAE + 2,
                 nBar = bDR + 1;
   extern __shared__ uint8_t smem_raw[];
@@ -271,6 +275,8 @@ mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
 __global__ void __launch_bounds__(128)
 mis_score_combine_kernel(const ScoreParams p, float* __restrict__ out,
                          float* __restrict__ renorm) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int i = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (i >= p.M) return;
@@ -338,10 +344,10 @@ mis_status_t launch_score(const ScoreArgs& a, void* stream) {
   if (a.M == 0) return MIS_OK;
 
   __nv_bfloat16* gathered = reinterpret_cast<__nv_bfloat16*>(ws + L.gathered);
-  mis_gather_rows_kernel<<<L.m_pad, 128, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(a.hidden), a.hidden_stride, a.T, a.delim, a.M, a.d,
-      gathered, status);
-  if (cudaGetLastError() != cudaSuccess) return MIS_ERR_CUDA;
+  if (launch_pdl(mis_gather_rows_kernel, dim3(L.m_pad), dim3(128), 0, st,
+                 static_cast<const __nv_bfloat16*>(a.hidden), a.hidden_stride, a.T, a.delim, a.M,
+                 a.d, gathered, status) != cudaSuccess)
+    return MIS_ERR_CUDA;
 
   bool ok = true;
   const uint64_t adims[2] = {(uint64_t)a.d, (uint64_t)L.m_pad};
@@ -368,13 +374,15 @@ mis_status_t launch_score(const ScoreArgs& a, void* stream) {
   p.wait_ns = wait_limit_ns();
   p.stall = (inject_stall_mask() >> 1) & 1u;
 
-  if (cudaFuncSetAttribute(mis_score_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmem) != cudaSuccess)
+  if (!kernel_attr_once(reinterpret_cast<const void*>(mis_score_partial_kernel), kSmem))
     return MIS_ERR_CUDA;
-  mis_score_partial_kernel<<<dim3(n_mtiles, p.n_chunks), 256, kSmem, st>>>(am, wm, p);
-  if (cudaGetLastError() != cudaSuccess) return MIS_ERR_CUDA;
-  mis_score_combine_kernel<<<(a.M + 3) / 4, 128, 0, st>>>(p, a.out_logprobs, a.out_renorm);
-  return cudaGetLastError() == cudaSuccess ? MIS_OK : MIS_ERR_CUDA;
+  if (launch_pdl(mis_score_partial_kernel, dim3(n_mtiles, p.n_chunks), dim3(256), kSmem, st, am,
+                 wm, p) != cudaSuccess)
+    return MIS_ERR_CUDA;
+  return launch_pdl(mis_score_combine_kernel, dim3((a.M + 3) / 4), dim3(128), 0, st, p,
+                    a.out_logprobs, a.out_renorm) == cudaSuccess
+             ? MIS_OK
+             : MIS_ERR_CUDA;
 }
 
 }  // namespace mis
