@@ -11,20 +11,25 @@
 // of the former: attention work O(Lq^2 + N Lq Lbar) instead of the causal
 // O((Lq + N Lbar)^2)).
 //
-// One block = one query tile and a pair of query heads that share a kv head
-// (GQA), or one head when the group size is odd. The pair shares every K/V
-// tile the block loads. Warp roles (384 threads):
-//   warp 0      : TMA producer (both Q tiles once, then K and V tiles through
-//                 separate rings: K is released as soon as both S products
-//                 are issued, V after both PV products)
+// Persistent kernel: one block per SM walks the planner's units (a query
+// tile with its key-tile list, for a pair of query heads that share a kv
+// head, or one head when the GQA group size is odd) in longest-first order,
+// snaking over the blocks. Pipelines, barriers and tensor memory carry over
+// from unit to unit: the next unit's Q and first K/V tiles load while the
+// current one finishes, and its first S product runs during the epilogue.
+//
+// Warp roles (384 threads):
+//   warp 0      : TMA producer (both Q tiles of a unit, then K and V tiles
+//                 through separate rings: K is released as soon as both S
+//                 products are issued, V after both PV products)
 //   warp 1      : TMEM allocator and the single thread issuing tcgen05.mma:
 //                   S_h = Q_h K^T  (SS: both operands in shared memory)
 //                   O_h += P_h V   (TS: P_h from tensor memory, V MN-major)
 //                 in the order S_0(j), PV_1(j-1), S_1(j), PV_0(j), so each
 //                 head's softmax overlaps the other head's products
-//   warps 4..7  : softmax of head 0, warps 8..11: softmax of head 1. One TMEM
-//                 lane (= one query row) per thread: the row max and sum stay
-//                 in the thread, no shuffles.
+//   warps 4..7  : softmax and epilogue of head 0, warps 8..11: of head 1. One
+//                 TMEM lane (= one query row) per thread: the row max and sum
+//                 stay in the thread, no shuffles.
 // Tensor memory (512 columns): S_0 | S_1 | O_0 | O_1. P_h (bf16 pairs) is
 // written over the first half of S_h once S_h has been read. Because S_h(j)
 // is committed after PV_h(j-1) was issued, "S_h(j) ready" also means O_h and
@@ -35,6 +40,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "mis_internal.h"
@@ -66,20 +72,30 @@ constexpr float kLn2 = 0.69314718055994530942f;
 struct AttnParams {
   const ReqInfo* req;
   const int32_t* seg_start;
-  const WorkItem* work;
+  const WorkItem* units;  // query tiles, longest first
   const uint32_t* klist;
+  int32_t n_units;        // query tiles
   __nv_bfloat16* o;
   float* lse;
   int64_t o_stride;
   int32_t T;
-  int32_t group;        // Hq / Hkv
-  int32_t heads;        // query heads per block: 2 (a GQA pair) or 1
+  int32_t group;          // Hq / Hkv
+  int32_t heads;          // query heads per unit: 2 (a GQA pair) or 1
   int32_t n_head_groups;  // Hq / heads
-  float scale_log2;     // softmax scale * log2(e)
+  float scale_log2;       // softmax scale * log2(e)
   uint32_t* status;
   uint64_t wait_ns;
-  uint32_t stall;       // failure injection: wait on a barrier nothing arrives on
+  uint32_t stall;         // failure injection: wait on a barrier nothing arrives on
 };
+
+// Unit handled by this block in pass kk over the longest-first unit list:
+// passes alternate direction (snake order), so every block gets a long and a
+// short unit from each pair of passes; -1 past the end.
+__device__ __forceinline__ int unit_at(int kk, int total) {
+  const int G = gridDim.x, c = blockIdx.x;
+  const int u = kk * G + ((kk & 1) ? (G - 1 - c) : c);
+  return u < total ? u : -1;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -93,8 +109,12 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   auto colS = [](int t) { return (uint32_t)(t * 128); };
   auto colO = [](int t) { return (uint32_t)(256 + t * D); };
   // barrier slots
-  constexpr int bQ = 0, bKF = 1, bKE = bKF + KS, bVF = bKE + KS, bVE = bVF + VS,
-                bSF = bVE + VS, bPF = bSF + 2, bOF = bPF + 2, bDR = bOF + 1, nBar = bDR + 1;
+  constexpr int bQF = 0, bQE = 1, bKF = 2, bKE = bKF + KS, bVF = bKE + KS, bVE = bVF + VS,
+                bSF = bVE + VS, bPF = bSF + 2, bOF = bPF + 2, bOE = bOF + 1, bDR = bOE + 2,
+                nBar = bDR + 1;
+
+  griddep_wait();                 // inputs of earlier stream work are visible
+  griddep_launch_dependents();
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -107,27 +127,22 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   volatile uint32_t* skip_flag = tmem_slot + 2;
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
-  griddep_wait();                 // inputs of earlier stream work are visible
-  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // 1-D grid: consecutive blocks take the head groups of one query tile, and
-  // query tiles come in longest-first order, so blocks start in
-  // longest-processing-time order across all heads
-  const int n_groups = p.n_head_groups;
-  const WorkItem wi = p.work[blockIdx.x / n_groups];
-  const int nh = p.heads;
-  const int h0 = (blockIdx.x % n_groups) * nh;         // first query head of the block
-  const int g = h0 / p.group;                          // shared kv head
-  const ReqInfo R = p.req[wi.req];
-  const int nk = wi.nk;
+  const int nh = p.heads, n_hg = p.n_head_groups;
+  const int total = p.n_units * n_hg;                  // unit u: p.units[u / n_hg], head group u % n_hg
 
   if (threadIdx.x == 0) {
     *skip_flag = (*(volatile uint32_t*)p.status & kDevTimeout) ? 1u : 0u;
     *abort_flag = 0;
-    mbar_init(bar(bQ), 1);
+    mbar_init(bar(bQF), 1);
+    mbar_init(bar(bQE), 1);
     for (int s = 0; s < KS; ++s) { mbar_init(bar(bKF + s), 1); mbar_init(bar(bKE + s), 1); }
     for (int s = 0; s < VS; ++s) { mbar_init(bar(bVF + s), 1); mbar_init(bar(bVE + s), 1); }
-    for (int s = 0; s < 2; ++s) { mbar_init(bar(bSF + s), 1); mbar_init(bar(bPF + s), 4); }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(bSF + s), 1);
+      mbar_init(bar(bPF + s), 4);                      // one arrival per softmax warp
+      mbar_init(bar(bOE + s), 4);
+    }
     mbar_init(bar(bOF), 1);
     mbar_init(bar(bDR), 1);
     fence_mbar_init();
@@ -144,33 +159,46 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Waiter W{abort_flag, p.status, p.wait_ns};
-  if (warp < 4) {
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&qmap); tma_prefetch_desc(&kmap); tma_prefetch_desc(&vmap);
-      mbar_arrive_expect_tx(bar(bQ), nh * C::kTile);
-      for (int t = 0; t < nh; ++t)
-        for (int b = 0; b < NB; ++b)
-          tma_load_3d(smem_u32(sQ + t * C::kTile + b * C::kBox), &qmap, bar(bQ), b * 64, h0 + t,
-                      wi.q0);
-      int k_issued = 0, v_issued = 0;
-      for (int it = 0; it < nk; ++it) {
-        const int32_t c0 = (int32_t)(p.klist[wi.kofs + it] & ~kNeedMask);
-        const int sk = it % KS, sv = it % VS;
-        if (it >= KS && !wait(bar(bKE + sk), ((it / KS) - 1) & 1, W, 0x100 + it)) break;
-        mbar_arrive_expect_tx(bar(bKF + sk), C::kTile);
-        for (int b = 0; b < NB; ++b)
-          tma_load_3d(smem_u32(sK + sk * C::kTile + b * C::kBox), &kmap, bar(bKF + sk), b * 64, g, c0);
-        k_issued = it + 1;
-        if (it >= VS && !wait(bar(bVE + sv), ((it / VS) - 1) & 1, W, 0x180 + it)) break;
-        mbar_arrive_expect_tx(bar(bVF + sv), C::kTile);
-        for (int b = 0; b < NB; ++b)
-          tma_load_3d(smem_u32(sV + sv * C::kTile + b * C::kBox), &vmap, bar(bVF + sv), b * 64, g, c0);
-        v_issued = it + 1;
+      int gk = 0, lu = 0, q_issued = 0, k_issued = 0, v_issued = 0;
+      bool ok = true;
+      for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {
+        const int u = unit_at(kk, total);
+        if (u < 0) continue;
+        const WorkItem un = p.units[u / n_hg];
+        const int h0 = (u % n_hg) * nh, g = h0 / p.group;
+        // Q of this unit once the previous unit's S products are done with it
+        if (lu > 0 && !(ok = wait(bar(bQE), (lu - 1) & 1, W, 0x80))) break;
+        mbar_arrive_expect_tx(bar(bQF), nh * C::kTile);
+        for (int t = 0; t < nh; ++t)
+          for (int b = 0; b < NB; ++b)
+            tma_load_3d(smem_u32(sQ + t * C::kTile + b * C::kBox), &qmap, bar(bQF), b * 64, h0 + t,
+                        un.q0);
+        q_issued = lu + 1;
+        for (int it = 0; it < un.nk; ++it) {
+          const int gi = gk + it;
+          const int32_t c0 = (int32_t)(p.klist[un.kofs + it] & ~kNeedMask);
+          const int sk = gi % KS, sv = gi % VS;
+          if (gi >= KS && !(ok = wait(bar(bKE + sk), ((gi / KS) - 1) & 1, W, 0x100))) break;
+          mbar_arrive_expect_tx(bar(bKF + sk), C::kTile);
+          for (int b = 0; b < NB; ++b)
+            tma_load_3d(smem_u32(sK + sk * C::kTile + b * C::kBox), &kmap, bar(bKF + sk), b * 64, g, c0);
+          k_issued = gi + 1;
+          if (gi >= VS && !(ok = wait(bar(bVE + sv), ((gi / VS) - 1) & 1, W, 0x180))) break;
+          mbar_arrive_expect_tx(bar(bVF + sv), C::kTile);
+          for (int b = 0; b < NB; ++b)
+            tma_load_3d(smem_u32(sV + sv * C::kTile + b * C::kBox), &vmap, bar(bVF + sv), b * 64, g, c0);
+          v_issued = gi + 1;
+        }
+        gk += un.nk;
+        ++lu;
       }
       // drain: every copy this thread started has landed before the block exits
-      wait_drain(bar(bQ), 0);
+      if (q_issued > 0) wait_drain(bar(bQF), (q_issued - 1) & 1);
       for (int i = (k_issued > KS ? k_issued - KS : 0); i < k_issued; ++i)
         wait_drain(bar(bKF + i % KS), (i / KS) & 1);
       for (int i = (v_issued > VS ? v_issued - VS : 0); i < v_issued; ++i)
@@ -183,7 +211,6 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
       constexpr uint32_t idO = idesc_bf16(128, D, true);
       bool ok = true;
       if (p.stall) ok = wait(bar(bDR), 0, W, 0x7ff);   // nothing arrives before the drain
-      if (ok) ok = wait(bar(bQ), 0, W, 0x200);
       auto issue_s = [&](int t, int sk) {
         const uint32_t aQ = smem_u32(sQ + t * C::kTile);
         const uint32_t aK = smem_u32(sK + sk * C::kTile);
@@ -205,146 +232,177 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
           mma_ts(tmem + colO(t), tmem + colS(t) + ks * 8, db, idO, (acc || ks != 0) ? 1u : 0u);
         }
       };
-      for (int it = 0; ok && it < nk; ++it) {
-        const int sk = it % KS, sv = it % VS;
-        if (!(ok = wait(bar(bKF + sk), (it / KS) & 1, W, 0x300 + it))) break;
-        tc_fence_after();
-        issue_s(0, sk);
-        if (nh == 2) {
-          if (it > 0) {
-            if (!(ok = wait(bar(bPF + 1), (it - 1) & 1, W, 0x400 + it))) break;
-            tc_fence_after();
-            issue_pv(1, (it - 1) % VS, it - 1 > 0);
-            mma_commit(bar(bVE + (it - 1) % VS));
-          }
-          issue_s(1, sk);
-        }
-        mma_commit(bar(bKE + sk));
-        if (!(ok = wait(bar(bVF + sv), (it / VS) & 1, W, 0x480 + it))) break;
-        if (!(ok = wait(bar(bPF + 0), it & 1, W, 0x500 + it))) break;
-        tc_fence_after();
-        issue_pv(0, sv, it > 0);
-        if (nh == 1) mma_commit(bar(bVE + sv));
-      }
-      if (ok && nh == 2 && nk > 0) {
-        if (wait(bar(bPF + 1), (nk - 1) & 1, W, 0x580)) {
+      int gk = 0, lu = 0;
+      for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {
+        const int u = unit_at(kk, total);
+        if (u < 0) continue;
+        const int nk = p.units[u / n_hg].nk;
+        if (!(ok = wait(bar(bQF), lu & 1, W, 0x200))) break;
+        // the first PV of head t in this unit overwrites O_t: the epilogue of
+        // the previous unit must have read it out of tensor memory
+        auto first_pv = [&](int t) -> bool {
+          if (lu == 0) return true;
+          if (!wait(bar(bOE + t), (lu - 1) & 1, W, 0x280 + t)) return false;
           tc_fence_after();
-          issue_pv(1, (nk - 1) % VS, nk - 1 > 0);
-          mma_commit(bar(bVE + (nk - 1) % VS));
+          return true;
+        };
+        for (int it = 0; ok && it < nk; ++it) {
+          const int gi = gk + it, sk = gi % KS, sv = gi % VS;
+          if (!(ok = wait(bar(bKF + sk), (gi / KS) & 1, W, 0x300))) break;
+          tc_fence_after();
+          issue_s(0, sk);
+          if (nh == 2) {
+            if (it > 0) {
+              if (!(ok = wait(bar(bPF + 1), (gi - 1) & 1, W, 0x400))) break;
+              tc_fence_after();
+              if (it == 1 && !(ok = first_pv(1))) break;
+              issue_pv(1, (gi - 1) % VS, it - 1 > 0);
+              mma_commit(bar(bVE + (gi - 1) % VS));
+            }
+            issue_s(1, sk);
+          }
+          mma_commit(bar(bKE + sk));
+          if (it == nk - 1) mma_commit(bar(bQE));        // Q of this unit no longer read
+          if (!(ok = wait(bar(bVF + sv), (gi / VS) & 1, W, 0x480))) break;
+          if (!(ok = wait(bar(bPF + 0), gi & 1, W, 0x500))) break;
+          tc_fence_after();
+          if (it == 0 && !(ok = first_pv(0))) break;
+          issue_pv(0, sv, it > 0);
+          if (nh == 1) mma_commit(bar(bVE + sv));
         }
+        if (ok && nh == 2) {
+          const int gl = gk + nk - 1;
+          if ((ok = wait(bar(bPF + 1), gl & 1, W, 0x580))) {
+            tc_fence_after();
+            if (nk == 1) ok = first_pv(1);
+            if (ok) {
+              issue_pv(1, gl % VS, nk - 1 > 0);
+              mma_commit(bar(bVE + gl % VS));
+            }
+          }
+        }
+        if (ok) mma_commit(bar(bOF));                    // every PV of the unit done
+        gk += nk;
+        ++lu;
       }
-      mma_commit(bar(bOF));
       // drain: all tensor-core work of this thread completes before dealloc
       mma_commit(bar(bDR));
       wait_drain(bar(bDR), 0);
     }
-  }
-  } else {
-  if ((warp - 4) / 4 < nh) {
-    // ------------------------------------------------------------- softmax
+  } else if (warp >= 4 && (warp - 4) / 4 < nh) {
+    // ------------------------------------------------- softmax and epilogue
     const int t = (warp - 4) / 4;                       // head of the pair
-    const int h = h0 + t;
     const int sw = warp & 3;
     const int r = sw * 32 + lane;
-    const int j = wi.q0 + r;
-    const bool valid = j < R.e0;
-    const int jj = valid ? j : -1;                      // invalid rows see nothing
-    const int lo = valid ? p.seg_start[j] : 0x7fffffff;
     const uint32_t tl = tmem + ((uint32_t)(sw * 32) << 16);
     const uint32_t tS = tl + colS(t), tO = tl + colO(t);
     const float sl2 = p.scale_log2;
-    float m_ref = -INFINITY, l = 0.f;
+    const uint64_t sl2x2 = f2_pack(__float_as_uint(sl2), __float_as_uint(sl2));
+    int gk = 0, lu = 0;
     bool ok = true;
-    uint32_t e_next = nk > 0 ? p.klist[wi.kofs] : 0u;
-    for (int it = 0; it < nk; ++it) {
-      const uint32_t e = e_next;
-      if (it + 1 < nk) e_next = p.klist[wi.kofs + it + 1];   // prefetch the next entry
-      const int32_t c0 = (int32_t)(e & ~kNeedMask);
-      const bool masked = (e & kNeedMask) != 0;
-      ok = wait(bar(bSF + t), it & 1, W, 0x600 + it);
+    for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {
+      const int u = unit_at(kk, total);
+      if (u < 0) continue;
+      const WorkItem un = p.units[u / n_hg];
+      const int hg = u % n_hg, h = hg * nh + t;
+      const ReqInfo R = p.req[un.req];
+      const int j = un.q0 + r;
+      const bool valid = j < R.e0;
+      const int jj = valid ? j : -1;                    // invalid rows see nothing
+      const int lo = valid ? p.seg_start[j] : 0x7fffffff;
+      const int nk = un.nk;
+      float m_ref = -INFINITY, l = 0.f;
+      uint32_t e_next = p.klist[un.kofs];
+      for (int it = 0; it < nk; ++it) {
+        const int gi = gk + it;
+        const uint32_t e = e_next;
+        if (it + 1 < nk) e_next = p.klist[un.kofs + it + 1];   // prefetch the next entry
+        const int32_t c0 = (int32_t)(e & ~kNeedMask);
+        const bool masked = (e & kNeedMask) != 0;
+        ok = wait(bar(bSF + t), gi & 1, W, 0x600);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        // the whole S row in registers: one load round trip per tile
+        uint32_t su[kBN];
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) tmem_ld32(tS + c * 32, su + c * 32);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) reg_fence32(su + c * 32);
+        if (masked) {
+          // visible columns of this row: [0, min(row, pend-1) - c0] of the shared
+          // set and [lo - c0, row - c0] of its own set, as 4 words of bits
+          const int a1 = jj - c0 + 1, q1 = min(a1, R.pend - c0), lc = lo - c0;
+#pragma unroll
+          for (int w = 0; w < kBN / 32; ++w) {
+            const uint32_t vis = bit_range(-32 * w, q1 - 32 * w) | bit_range(lc - 32 * w, a1 - 32 * w);
+#pragma unroll
+            for (int x = 0; x < 32; ++x)
+              if (!((vis >> x) & 1u)) su[w * 32 + x] = 0xff800000u;     // -inf
+          }
+        }
+        // row max: three-input max, four independent chains
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < kBN; c += 2)
+          mx4[(c >> 1) & 3] = max3(mx4[(c >> 1) & 3], __uint_as_float(su[c]), __uint_as_float(su[c + 1]));
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        const float m_new = fmaxf(m_ref, mx * sl2);
+        const bool grow = m_new > m_ref + kRescaleThreshold;
+        const bool any_grow = __any_sync(0xffffffffu, grow);
+        const float alpha = grow ? ex2(m_ref - m_new) : 1.f;
+        if (grow) { l *= alpha; m_ref = m_new; }
+        const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
+        // P = 2^(s*scale*log2e - m) as bf16 pairs over the first half of S_h;
+        // scale/shift and the row sum run on packed fp32 pairs
+        const uint64_t nmbx2 = f2_pack(__float_as_uint(-mb), __float_as_uint(-mb));
+        uint64_t rs4[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int hf = 0; hf < kBN / 64; ++hf) {        // 64 columns -> 32 packed words
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int k2 = hf * 64 + 2 * c;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(su[k2], su[k2 + 1]), sl2x2, nmbx2), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            rs4[c & 3] = f2_add(rs4[c & 3], f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
+            pk[c] = pack_bf16(p0, p1);
+          }
+          tmem_st32(tS + hf * 32, pk);
+        }
+        {
+          float a0, a1;
+          f2_unpack(f2_add(f2_add(rs4[0], rs4[1]), f2_add(rs4[2], rs4[3])), a0, a1);
+          l += a0 + a1;
+        }
+        if (any_grow && it > 0) {
+          // O_h holds the products up to tile it-1, all complete (see above);
+          // it is rescaled after P so that O and S are never live together
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + c * 32, ov);
+            tmem_ld_wait();
+            reg_fence32(ov);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * alpha);
+            tmem_st32(tO + c * 32, ov);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(bPF + t));       // one arrival per warp
+      }
+      if (!ok) break;
+      gk += nk;
+      ok = wait(bar(bOF), lu & 1, W, 0x700);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // the whole S row in registers: one load round trip per tile
-      uint32_t su[kBN];
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) tmem_ld32(tS + c * 32, su + c * 32);
-      tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) reg_fence32(su + c * 32);
-      if (masked) {
-        // visible columns of this row: [0, min(row, pend-1) - c0] of the shared
-        // set and [lo - c0, row - c0] of its own set, as 4 words of bits
-        const int a1 = jj - c0 + 1, q1 = min(a1, R.pend - c0), lc = lo - c0;
-#pragma unroll
-        for (int w = 0; w < kBN / 32; ++w) {
-          const uint32_t vis = bit_range(-32 * w, q1 - 32 * w) | bit_range(lc - 32 * w, a1 - 32 * w);
-#pragma unroll
-          for (int x = 0; x < 32; ++x)
-            if (!((vis >> x) & 1u)) su[w * 32 + x] = 0xff800000u;     // -inf
-        }
-      }
-      // row max: three-input max, four independent chains
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c = 0; c < kBN; c += 2)
-        mx4[(c >> 1) & 3] = max3(mx4[(c >> 1) & 3], __uint_as_float(su[c]), __uint_as_float(su[c + 1]));
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      const float m_new = fmaxf(m_ref, mx * sl2);
-      const bool grow = m_new > m_ref + kRescaleThreshold;
-      const bool any_grow = __any_sync(0xffffffffu, grow);
-      const float alpha = grow ? ex2(m_ref - m_new) : 1.f;
-      if (grow) { l *= alpha; m_ref = m_new; }
-      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // P = 2^(s*scale*log2e - m) as bf16 pairs over the first half of S_h;
-      // scale/shift and the row sum run on packed fp32 pairs
-      const uint64_t sl2x2 = f2_pack(__float_as_uint(sl2), __float_as_uint(sl2));
-      const uint64_t nmbx2 = f2_pack(__float_as_uint(-mb), __float_as_uint(-mb));
-      uint64_t rs4[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-      for (int hf = 0; hf < kBN / 64; ++hf) {        // 64 columns -> 32 packed words
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int k2 = hf * 64 + 2 * c;
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(su[k2], su[k2 + 1]), sl2x2, nmbx2), x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          rs4[c & 3] = f2_add(rs4[c & 3], f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
-          pk[c] = pack_bf16(p0, p1);
-        }
-        tmem_st32(tS + hf * 32, pk);
-      }
-      {
-        float a0, a1;
-        f2_unpack(f2_add(f2_add(rs4[0], rs4[1]), f2_add(rs4[2], rs4[3])), a0, a1);
-        l += a0 + a1;
-      }
-      if (any_grow && it > 0) {
-        // O_h holds the products up to tile it-1, all complete (see above);
-        // it is rescaled after P so that O and S are never live together
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(tO + c * 32, ov);
-          tmem_ld_wait();
-          reg_fence32(ov);
-#pragma unroll
-          for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * alpha);
-          tmem_st32(tO + c * 32, ov);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(bPF + t));         // one arrival per warp
-    }
-    if (ok) {
-      ok = wait(bar(bOF), 0, W, 0x700);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
-      tc_fence_after();
+      // normalise and store bf16 O
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = p.o + (int64_t)(valid ? j : 0) * p.o_stride + (int64_t)h * D;
 #pragma unroll
@@ -353,6 +411,11 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
         tmem_ld32(tO + c * 32, ov);
         tmem_ld_wait();
         reg_fence32(ov);
+        if (c == D / 32 - 1) {                          // O_t fully read: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(bOE + t));
+        }
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
@@ -367,8 +430,8 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
         }
       }
       if (p.lse && valid) p.lse[(int64_t)h * p.T + j] = (m_ref + log2f(l)) * kLn2;
+      ++lu;
     }
-  }
   }
   tc_fence_before();
   __syncthreads();
@@ -399,15 +462,16 @@ mis_status_t launch_d(const HostPlan& pl, const void* q, const void* k, const vo
   AttnParams prm;
   prm.req = reinterpret_cast<const ReqInfo*>(ws + pl.off_req);
   prm.seg_start = reinterpret_cast<const int32_t*>(ws + pl.off_seg);
-  prm.work = reinterpret_cast<const WorkItem*>(ws + pl.off_work);
+  prm.units = reinterpret_cast<const WorkItem*>(ws + pl.off_work);
   prm.klist = reinterpret_cast<const uint32_t*>(ws + pl.off_klist);
+  prm.n_units = (int32_t)pl.work.size();
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
   prm.o_stride = os;
   prm.T = pl.T;
   prm.group = pl.Hq / pl.Hkv;
   prm.heads = (prm.group % 2 == 0) ? 2 : 1;
-  prm.n_head_groups = pl.Hq / prm.heads;
+  prm.n_head_groups = pl.n_head_groups;
   prm.scale_log2 = pl.scale * 1.4426950408889634f;
   prm.status = reinterpret_cast<uint32_t*>(ws);
   prm.wait_ns = wait_limit_ns();
@@ -418,9 +482,9 @@ mis_status_t launch_d(const HostPlan& pl, const void* q, const void* k, const vo
   if (pl.work.empty()) return MIS_OK;
   auto kern = mis_attn_fwd_kernel<D>;
   if (!kernel_attr_once(reinterpret_cast<const void*>(kern), C::kSmem)) return MIS_ERR_CUDA;
-  const int64_t blocks = (int64_t)pl.work.size() * prm.n_head_groups;
-  if (blocks > 0x7fffffff) return MIS_ERR_UNSUPPORTED;
-  dim3 grid((unsigned)blocks);
+  const int64_t total = (int64_t)pl.work.size() * pl.n_head_groups;
+  if (total > 0x7fffffff) return MIS_ERR_UNSUPPORTED;
+  dim3 grid((unsigned)std::min<int64_t>(total, num_sms()));
   return launch_pdl(kern, grid, dim3(kThreads), C::kSmem, st, qm, km, vm, prm) == cudaSuccess
              ? MIS_OK
              : MIS_ERR_CUDA;

@@ -51,6 +51,7 @@ struct HostPlan {
   mis_plan_stats stats{};
   // byte offsets inside the device workspace
   size_t off_req = 0, off_seg = 0, off_work = 0, off_klist = 0, total = 0;
+  int32_t n_head_groups = 1;       // blocks' head groups per query tile (pairs or single heads)
   void* workspace = nullptr;       // device base, set by mis_plan_create
 };
 

@@ -126,6 +126,8 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
   p->work.reserve(tmp.size());
   for (const Tmp& w : tmp) p->work.push_back(WorkItem{w.req, w.q0, w.kofs, w.nk});
 
+  p->n_head_groups = ((p->Hq / p->Hkv) % 2 == 0) ? p->Hq / 2 : p->Hq;
+
   p->stats.n_qtiles = (int64_t)p->work.size();
   p->stats.n_tiles = p->stats.n_full + p->stats.n_partial;
   p->stats.n_causal_tiles = causal_tiles;
