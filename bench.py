@@ -66,16 +66,16 @@ def kernel_source_sha(name: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def ncu_traffic(kernel_file: str):
-    """DRAM bytes per launch from the committed ncu summary, if it still
-    describes the current kernel source; else None."""
+def ncu_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it describes
+    the current kernel source on this workload; else None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(kernel_file)
-    if not e or e.get("source_sha") != kernel_source_sha(kernel_file):
+    if not e or e.get("source_sha") != kernel_source_sha(kernel_file) or e.get("workload") != workload:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -270,15 +270,15 @@ def run_ours(args, rank, world, dist):
         if bound_hbm:
             roof = {"kernel": "mis_label_scores (gather + tcgen05 LM head with fused LSE + combine)",
                     "bound": "hbm", "achieved": round(score_gbs, 1), "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "traffic": ncu_traffic("mis_score.cu"),
+                    "unit": "GB/s", "traffic": ncu_traffic("mis_score.cu", w.name),
                     "algorithmic_bytes_per_launch": score_bytes}
         else:
             roof = {"kernel": "mis_label_scores", "bound": "tensor", "achieved": round(score_tflops, 1),
-                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "traffic": ncu_traffic("mis_score.cu"),
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "traffic": ncu_traffic("mis_score.cu", w.name),
                     "algorithmic_flops_per_launch": score_flops}
     else:
         roof = {"kernel": "mis_attention_fwd", "bound": "tensor", "achieved": round(attn_tflops, 1),
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "traffic": ncu_traffic("mis_attn.cu"),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "traffic": ncu_traffic("mis_attn.cu", w.name),
                 "algorithmic_flops_per_launch": attn_flops}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["peak_source"] = peak_src
@@ -458,45 +458,43 @@ def run_comparators(w, shapes, vals, labels, dev, stream, q, k, v, hidden, w_lm,
 # ---------------------------------------------------------------- CPU oracle
 
 def _oracle_sample(w, shapes, vals, labels, budget_s, seed=0):
-    """Time the oracle on a seeded sample of rows and items; returns an
-    estimate of the full workload's oracle time and the sample description."""
+    """Time the oracle on a seeded sample of rows and items sized from a small
+    timed pilot, so the whole run stays near `budget_s`; returns an estimate
+    of the full workload's oracle time and the sample description."""
     import oracle as O
     import torch
     lay = O.build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
     f64 = lambda t: t.to(torch.float64).numpy()
     q, k, v = f64(vals["q"]), f64(vals["k"]), f64(vals["v"])
-    hidden = f64(vals["hidden"])
-    W = vals["w_lm"]
+    hidden, W = f64(vals["hidden"]), f64(vals["w_lm"])
     rng = np.random.default_rng(seed)
-    # rows: a fraction sized to the budget (cost ~ rows x request length)
-    frac_r = 1.0
-    work = float(sum(np.diff(lay.cu_seqlens) ** 2)) * w.hq * w.head_dim
-    # roughly 2 GFLOP/s/core effective for the masked numpy path; stay inside ~1/2 budget
-    est = 4 * work / (2e9 * max(1, os.cpu_count() or 1))
-    if est > budget_s / 2:
-        frac_r = max(1e-3, (budget_s / 2) / est)
-    n_rows = max(1, int(round(lay.T * frac_r)))
-    rows = np.sort(rng.choice(lay.T, size=n_rows, replace=False)) if n_rows < lay.T else None
-    t0 = time.perf_counter()
-    O.attention(q, k, v, lay, rows=rows)
-    t_attn = time.perf_counter() - t0
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    # attention: cost per row from a 32-row pilot, then as many rows as fit
+    pilot = np.sort(rng.choice(lay.T, size=min(32, lay.T), replace=False))
+    per_row = timed(lambda: O.attention(q, k, v, lay, rows=pilot)) / len(pilot)
+    n_rows = int(min(lay.T, max(len(pilot), (budget_s / 2) / max(per_row, 1e-9))))
+    rows = None if n_rows >= lay.T else np.sort(rng.choice(lay.T, size=n_rows, replace=False))
+    t_attn = timed(lambda: O.attention(q, k, v, lay, rows=rows))
     frac_r = 1.0 if rows is None else n_rows / lay.T
-    # items
-    n_items = lay.M
-    frac_i = 1.0
-    if lay.M * w.d_model * w.vocab * 2 / (5e9 * max(1, os.cpu_count() or 1)) > budget_s / 2:
-        n_items = max(1, int(lay.M * (budget_s / 2) / (lay.M * w.d_model * w.vocab * 2 / (5e9 * (os.cpu_count() or 1)))))
-        n_items = min(n_items, lay.M)
-        frac_i = n_items / lay.M
-    items = np.sort(rng.choice(lay.M, size=n_items, replace=False)) if n_items < lay.M else None
-    t0 = time.perf_counter()
-    O.label_scores(hidden, f64(W), lay.delim_positions, labels, items=items)
-    t_score = time.perf_counter() - t0
+    # scoring: cost per item from a 4-item pilot
+    pilot_i = np.sort(rng.choice(lay.M, size=min(4, lay.M), replace=False))
+    per_item = timed(lambda: O.label_scores(hidden, W, lay.delim_positions, labels, items=pilot_i)) / len(pilot_i)
+    n_items = int(min(lay.M, max(len(pilot_i), (budget_s / 2) / max(per_item, 1e-9))))
+    items = None if n_items >= lay.M else np.sort(rng.choice(lay.M, size=n_items, replace=False))
+    t_score = timed(lambda: O.label_scores(hidden, W, lay.delim_positions, labels, items=items))
+    frac_i = 1.0 if items is None else n_items / lay.M
     t_full = t_attn / frac_r + t_score / frac_i
-    sample = (f"oracle on {'all' if rows is None else n_rows} of {lay.T} rows x {w.hq} heads and "
-              f"{'all' if items is None else n_items} of {lay.M} items; full-workload time "
-              f"extrapolated by rows and items" if (rows is not None or items is not None)
-              else f"oracle on the whole workload ({lay.T} rows x {w.hq} heads, {lay.M} items)")
+    if rows is None and items is None:
+        sample = f"oracle on the whole workload ({lay.T} rows x {w.hq} heads, {lay.M} items)"
+    else:
+        sample = (f"oracle on {'all' if rows is None else n_rows} of {lay.T} rows x {w.hq} heads and "
+                  f"{'all' if items is None else n_items} of {lay.M} items; full-workload time "
+                  f"extrapolated by rows and items")
     return t_full, lay.M, sample, t_attn + t_score
 
 

@@ -120,9 +120,19 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
     }
   }
   if (p->klist.size() > (size_t)std::numeric_limits<int32_t>::max()) return MIS_ERR_SHAPE;
-  // heaviest query tiles first (longest-processing-time order), stable
-  std::stable_sort(tmp.begin(), tmp.end(),
-                   [](const Tmp& a, const Tmp& b) { return a.cost > b.cost; });
+  // Order: request by request, requests with the most expensive query tile
+  // first, and inside a request the query tiles longest first. Blocks that run
+  // at the same time then work on the same request and share its K/V tiles
+  // through L2 (a request-blind longest-first order scatters them and every
+  // query tile re-reads its request's K/V from HBM), while the long units
+  // still start first.
+  std::vector<int64_t> req_max(B, 0);
+  for (const Tmp& w : tmp) req_max[w.req] = std::max(req_max[w.req], w.cost);
+  std::stable_sort(tmp.begin(), tmp.end(), [&](const Tmp& a, const Tmp& b) {
+    if (req_max[a.req] != req_max[b.req]) return req_max[a.req] > req_max[b.req];
+    if (a.req != b.req) return a.req < b.req;
+    return a.cost > b.cost;
+  });
   p->work.reserve(tmp.size());
   for (const Tmp& w : tmp) p->work.push_back(WorkItem{w.req, w.q0, w.kofs, w.nk});
 
