@@ -184,27 +184,26 @@ def run_ours(args, rank, world, dist):
     lay0 = lib.mis_build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
     plan0 = lib.Plan(lay0.cu_seqlens, lay0.prefix_len, lay0.item_ptr, lay0.item_offsets,
                      w.hq, w.hkv, w.head_dim)
-    ws_plan = torch.zeros(plan0.workspace_size(), dtype=torch.uint8, device=dev)
+    # plan workspace, followed by the batch's readout rows (uploaded together)
+    wsz = plan0.workspace_size()
+    ws_plan = torch.zeros(wsz + 4 * M, dtype=torch.uint8, device=dev)
+    delim_dev = ws_plan[wsz:wsz + 4 * M].view(torch.int32)
     ws_score = torch.zeros(lib.mis_label_scores_workspace_size(M, w.d_model, w.vocab, K),
                            dtype=torch.uint8, device=dev)
-    delim_host = torch.empty(M, dtype=torch.int32).pin_memory()
-    delim_dev = torch.empty(M, dtype=torch.int32, device=dev)
     flush = L2Flush(dev)
     plan0.create(ws_plan, sp)
     stats = plan0.stats()
     plan0.destroy()
+    planner = lib.Planner()
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
     def step(times=None):
         # a1: layout (host)
         lay = lib.mis_build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens,
                                    with_positions=False)
-        delim_host.numpy()[:] = lay.delim_positions
-        delim_dev.copy_(delim_host, non_blocking=True)
-        # a2: plan (host) + upload into the workspace
-        plan = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets,
-                        w.hq, w.hkv, w.head_dim)
-        plan.create(ws_plan, sp)
+        # a2: plan (host); one asynchronous upload of the plan and the readout rows
+        plan = planner.plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets,
+                            w.hq, w.hkv, w.head_dim, ws_plan, stream=sp, extra=lay.delim_positions)
         # a3: MIS attention
         if times is not None:
             times["a0"].record(stream)
@@ -330,11 +329,12 @@ def run_e2e(args, w, shapes, vals, labels, dev, stream, dist, world):
     o = torch.empty_like(dbuf["q"])
     out_dev = torch.empty(M, K, dtype=torch.float32, device=dev)
     out_host = torch.empty(M, K, dtype=torch.float32).pin_memory()
-    delim_host = torch.empty(M, dtype=torch.int32).pin_memory()
-    delim_dev = torch.empty(M, dtype=torch.int32, device=dev)
+    planner = lib.Planner()
     plan0 = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets,
                      w.hq, w.hkv, w.head_dim)
-    ws_plan = torch.zeros(plan0.workspace_size(), dtype=torch.uint8, device=dev)
+    wsz = plan0.workspace_size()
+    ws_plan = torch.zeros(wsz + 4 * M, dtype=torch.uint8, device=dev)
+    delim_dev = ws_plan[wsz:wsz + 4 * M].view(torch.int32)
     ws_score = torch.zeros(lib.mis_label_scores_workspace_size(M, w.d_model, w.vocab, K),
                            dtype=torch.uint8, device=dev)
     h2d = sum(t.numel() * t.element_size() for t in host.values()) + M * 4
@@ -345,11 +345,8 @@ def run_e2e(args, w, shapes, vals, labels, dev, stream, dist, world):
             dbuf[n].copy_(host[n], non_blocking=True)
         l = lib.mis_build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens,
                                  with_positions=False)
-        delim_host.numpy()[:] = l.delim_positions
-        delim_dev.copy_(delim_host, non_blocking=True)
-        plan = lib.Plan(l.cu_seqlens, l.prefix_len, l.item_ptr, l.item_offsets,
-                        w.hq, w.hkv, w.head_dim)
-        plan.create(ws_plan, sp)
+        plan = planner.plan(l.cu_seqlens, l.prefix_len, l.item_ptr, l.item_offsets,
+                            w.hq, w.hkv, w.head_dim, ws_plan, stream=sp, extra=l.delim_positions)
         lib.mis_attention_fwd_plan(plan, dbuf["q"], dbuf["k"], dbuf["v"], o, None, sp)
         lib.mis_label_scores(dbuf["hidden"], w_lm, delim_dev, labels, out_dev, None, ws_score, stream=sp)
         out_host.copy_(out_dev, non_blocking=True)

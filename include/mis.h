@@ -160,6 +160,25 @@ mis_status_t mis_plan_get_stats(mis_plan_t plan, mis_plan_stats* out);
 mis_status_t mis_plan_tile_map(mis_plan_t plan, int32_t* host_out, size_t cap, size_t* n_out);
 mis_status_t mis_plan_destroy(mis_plan_t plan);
 
+/* Reusable planner for a stream of batches. mis_plan_create() uploads the
+ * plan from pageable memory, which CUDA turns into a synchronisation with
+ * the stream; a planner instead owns two pinned host staging buffers (grown
+ * on demand) and an event per buffer, so mis_planner_plan() only waits for
+ * the upload issued two calls earlier (long finished in a steady loop) and
+ * the host can plan the next batch while the device still works. Same
+ * validation, workspace rules and result as mis_plan_create(); the returned
+ * plan is freed with mis_plan_destroy() and must not outlive its workspace.
+ * A planner is not thread-safe; destroy waits for its uploads. */
+typedef struct mis_planner_s* mis_planner_t;
+mis_status_t mis_planner_create(mis_planner_t* out);
+/* extra_host / extra_bytes: an optional side payload (e.g. the batch's
+ * readout rows) copied in the same transfer to workspace +
+ * mis_plan_workspace_size(desc); ws_bytes must cover it. NULL / 0 for none. */
+mis_status_t mis_planner_plan(mis_planner_t planner, const mis_attn_desc* desc, void* workspace,
+                              size_t ws_bytes, const void* extra_host, size_t extra_bytes,
+                              void* stream, mis_plan_t* out);
+mis_status_t mis_planner_destroy(mis_planner_t planner);
+
 /* ------------------------------------------------------------------------
  * MIS attention forward ("From Generation to Scoring", eq. 4 and Section
  * 4.2; "Turbocharging ...", section "FlashInfer changes").

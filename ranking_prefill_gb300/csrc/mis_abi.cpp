@@ -212,6 +212,109 @@ mis_status_t mis_plan_create(const mis_attn_desc* desc, void* workspace, size_t 
   }
 }
 
+}  // extern "C"
+
+struct mis_planner_s {
+  void* staging[2] = {nullptr, nullptr};
+  size_t cap[2] = {0, 0};
+  cudaEvent_t done[2] = {nullptr, nullptr};
+  bool used[2] = {false, false};
+  int next = 0;
+};
+
+extern "C" {
+
+mis_status_t mis_planner_create(mis_planner_t* out) {
+  if (!out) return MIS_ERR_INVALID_ARG;
+  *out = nullptr;
+  mis_planner_s* pl = nullptr;
+  try {
+    pl = new mis_planner_s();
+  } catch (...) {
+    return MIS_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < 2; ++i)
+    if (cudaEventCreateWithFlags(&pl->done[i], cudaEventDisableTiming) != cudaSuccess) {
+      mis_planner_destroy(pl);
+      return MIS_ERR_CUDA;
+    }
+  *out = pl;
+  return MIS_OK;
+}
+
+mis_status_t mis_planner_destroy(mis_planner_t pl) {
+  if (!pl) return MIS_OK;
+  for (int i = 0; i < 2; ++i) {
+    if (pl->done[i]) {
+      if (pl->used[i]) cudaEventSynchronize(pl->done[i]);
+      cudaEventDestroy(pl->done[i]);
+    }
+    if (pl->staging[i]) cudaFreeHost(pl->staging[i]);
+  }
+  delete pl;
+  return MIS_OK;
+}
+
+mis_status_t mis_planner_plan(mis_planner_t pl, const mis_attn_desc* desc, void* workspace,
+                              size_t ws_bytes, const void* extra_host, size_t extra_bytes,
+                              void* stream, mis_plan_t* out) {
+  if (!pl || !out || (extra_bytes && !extra_host)) return MIS_ERR_INVALID_ARG;
+  *out = nullptr;
+  mis_plan_s* h = nullptr;
+  try {
+    h = new mis_plan_s();
+    mis_status_t st = build_plan(desc, &h->p);
+    if (st != MIS_OK) { delete h; return st; }
+    HostPlan& p = h->p;
+    if (!workspace || !aligned256(workspace) || ws_bytes < p.total + extra_bytes) {
+      delete h;
+      return MIS_ERR_WORKSPACE;
+    }
+    p.workspace = workspace;
+    const int b = pl->next;
+    // one image from offset 0: zeroed status words, the plan, the side payload
+    const size_t n = p.total + extra_bytes;
+    // the buffer's previous upload (two calls ago) must have been read
+    if (pl->used[b] && cudaEventSynchronize(pl->done[b]) != cudaSuccess) { delete h; return MIS_ERR_CUDA; }
+    if (pl->cap[b] < n) {
+      if (pl->staging[b]) cudaFreeHost(pl->staging[b]);
+      pl->staging[b] = nullptr;
+      pl->cap[b] = 0;
+      const size_t want = n + n / 2 + 4096;
+      if (cudaHostAlloc(&pl->staging[b], want, cudaHostAllocDefault) != cudaSuccess) {
+        pl->staging[b] = nullptr;
+        delete h;
+        return MIS_ERR_CUDA;
+      }
+      pl->cap[b] = want;
+    }
+    uint8_t* img = static_cast<uint8_t*>(pl->staging[b]);
+    std::memset(img, 0, p.total);
+    auto put = [&](size_t off, const void* src, size_t len) {
+      if (len) std::memcpy(img + off, src, len);
+    };
+    put(p.off_req, p.req.data(), p.req.size() * sizeof(ReqInfo));
+    put(p.off_seg, p.seg_start.data(), p.seg_start.size() * sizeof(int32_t));
+    put(p.off_work, p.work.data(), p.work.size() * sizeof(WorkItem));
+    put(p.off_klist, p.klist.data(), p.klist.size() * sizeof(uint32_t));
+    put(p.total, extra_host, extra_bytes);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(workspace, img, n, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaEventRecord(pl->done[b], s) != cudaSuccess) {
+      delete h;
+      return MIS_ERR_CUDA;
+    }
+    p.status_clear = true;
+    pl->used[b] = true;
+    pl->next = b ^ 1;
+    *out = h;
+    return MIS_OK;
+  } catch (...) {
+    delete h;
+    return MIS_ERR_INVALID_ARG;
+  }
+}
+
 mis_status_t mis_plan_get_stats(mis_plan_t plan, mis_plan_stats* out) {
   if (!plan || !out) return MIS_ERR_INVALID_ARG;
   *out = plan->p.stats;
@@ -237,7 +340,7 @@ mis_status_t mis_attention_fwd_plan(mis_plan_t plan, const void* q, const void* 
                                     void* o, float* lse, int64_t qs, int64_t ks, int64_t vs,
                                     int64_t os, void* stream) {
   if (!plan) return MIS_ERR_INVALID_ARG;
-  const HostPlan& p = plan->p;
+  HostPlan& p = plan->p;
   if (!p.workspace) return MIS_ERR_WORKSPACE;
   if (!q || !k || !v || !o) return MIS_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return MIS_ERR_INVALID_ARG;

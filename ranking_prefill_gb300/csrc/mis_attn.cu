@@ -443,7 +443,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
 }
 
 template <int D>
-mis_status_t launch_d(const HostPlan& pl, const void* q, const void* k, const void* v, void* o,
+mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v, void* o,
                       float* lse, int64_t qs, int64_t ks, int64_t vs, int64_t os, void* stream) {
   using C = AttnCfg<D>;
   bool ok = true;
@@ -478,7 +478,11 @@ mis_status_t launch_d(const HostPlan& pl, const void* q, const void* k, const vo
   prm.stall = inject_stall_mask() & 1u;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return MIS_ERR_CUDA;
+  if (pl.status_clear) {
+    pl.status_clear = false;               // zeroed by the plan upload just before
+  } else if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) {
+    return MIS_ERR_CUDA;
+  }
   if (pl.work.empty()) return MIS_OK;
   auto kern = mis_attn_fwd_kernel<D>;
   if (!kernel_attr_once(reinterpret_cast<const void*>(kern), C::kSmem)) return MIS_ERR_CUDA;
@@ -492,7 +496,7 @@ mis_status_t launch_d(const HostPlan& pl, const void* q, const void* k, const vo
 
 }  // namespace
 
-mis_status_t launch_attention(const HostPlan& p, const void* q, const void* k, const void* v,
+mis_status_t launch_attention(HostPlan& p, const void* q, const void* k, const void* v,
                               void* o, float* lse, int64_t qs, int64_t ks, int64_t vs, int64_t os,
                               void* stream) {
   if (p.D == 128) return launch_d<128>(p, q, k, v, o, lse, qs, ks, vs, os, stream);

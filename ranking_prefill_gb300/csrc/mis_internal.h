@@ -53,6 +53,8 @@ struct HostPlan {
   size_t off_req = 0, off_seg = 0, off_work = 0, off_klist = 0, total = 0;
   int32_t n_head_groups = 1;       // blocks' head groups per query tile (pairs or single heads)
   void* workspace = nullptr;       // device base, set by mis_plan_create
+  bool status_clear = false;       // the upload zeroed the status words; the
+                                   // first launch need not clear them again
 };
 
 // Validates the descriptor and fills everything but `workspace`.
@@ -90,7 +92,7 @@ uint32_t inject_stall_mask();
 
 // Kernel launchers (defined in the .cu files). Return MIS_ERR_CUDA on launch
 // failure. Pointers are already validated.
-mis_status_t launch_attention(const HostPlan& p, const void* q, const void* k, const void* v,
+mis_status_t launch_attention(HostPlan& p, const void* q, const void* k, const void* v,
                               void* o, float* lse, int64_t qs, int64_t ks, int64_t vs, int64_t os,
                               void* stream);
 

@@ -33,7 +33,7 @@ EXPORTS = ["mis_status_string", "mis_abi_version", "mis_layout_size", "mis_build
            "mis_plan_tile_map", "mis_plan_destroy", "mis_attention_fwd_plan",
            "mis_attention_fwd", "mis_label_scores_workspace_size", "mis_label_scores",
            "mis_get_device_status", "mis_set_wait_limit_ns", "mis_label_scores_noalloc",
-           "mis_inject_stall"]
+           "mis_inject_stall", "mis_planner_create", "mis_planner_plan", "mis_planner_destroy"]
 
 
 class MisError(RuntimeError):
@@ -91,6 +91,10 @@ def load(path: str = LIB_PATH):
         "mis_get_device_status": (C.c_int, [vp, vp]),
         "mis_set_wait_limit_ns": (C.c_uint64, [C.c_uint64]),
         "mis_inject_stall": (C.c_uint32, [C.c_uint32]),
+        "mis_planner_create": (C.c_int, [C.POINTER(vp)]),
+        "mis_planner_plan": (C.c_int, [vp, C.POINTER(mis_attn_desc), vp, sz, vp, sz, vp,
+                                       C.POINTER(vp)]),
+        "mis_planner_destroy": (C.c_int, [vp]),
         "mis_label_scores_noalloc": (C.c_int, [vp, i64, C.c_int32, vp, C.c_int32, C.c_int32, vp,
                                                C.c_int32, i32p, C.c_int32, vp, vp, vp, vp]),
     }
@@ -250,6 +254,42 @@ class Plan:
     def destroy(self):
         if self._h is not None:
             self._L.mis_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+class Planner:
+    """mis_planner_*: plans uploaded through pinned staging, no stream sync."""
+
+    def __init__(self):
+        self._L = load()
+        h = C.c_void_p()
+        _check(self._L.mis_planner_create(C.byref(h)), "mis_planner_create")
+        self._h = h
+
+    def plan(self, cu_seqlens, prefix_len, item_ptr, item_offsets, Hq, Hkv, D, workspace,
+             scale: float = 0.0, stream=None, extra: Optional[np.ndarray] = None) -> Plan:
+        """`extra` (a contiguous host array, e.g. the readout rows) rides in the
+        same upload and lands at workspace byte offset plan.workspace_size()."""
+        p = Plan(cu_seqlens, prefix_len, item_ptr, item_offsets, Hq, Hkv, D, scale)
+        h = C.c_void_p()
+        nbytes = workspace.numel() * workspace.element_size()
+        ex = None if extra is None else np.ascontiguousarray(extra)
+        _check(self._L.mis_planner_plan(self._h, C.byref(p.desc), _dptr(workspace), nbytes,
+                                        None if ex is None else ex.ctypes.data,
+                                        0 if ex is None else ex.nbytes,
+                                        _stream(stream), C.byref(h)), "mis_planner_plan")
+        p._h, p.workspace = h, workspace
+        return p
+
+    def destroy(self):
+        if self._h is not None:
+            self._L.mis_planner_destroy(self._h)
             self._h = None
 
     def __del__(self):

@@ -111,3 +111,35 @@ def test_large_workloads_sampled_rows(name):
     lay = oracle_layout(s)
     rows = _sample_rows(lay, 384, w.seed)
     check_attention(s, w.hq, w.hkv, w.head_dim, w.seed, rows=rows)
+
+
+def test_planner_plans_match_oracle_across_buffer_reuse():
+    # three batches through one planner: the third reuses the first staging buffer
+    planner = lib.Planner()
+    dev = torch.device("cuda")
+    cases = [synth.custom_shapes([300], [5], [10, 0, 64, 129, 7]),
+             synth.custom_shapes([17, 900], [2, 3], [5, 6, 40, 1, 250]),
+             synth.custom_shapes([128], [8], [16] * 8)]
+    outs = []
+    for n, s in enumerate(cases):
+        lay = lib.mis_build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+        v = synth.draw_values(50 + n, lay.T, 4, 2, 128, want=("q", "k", "v"))
+        q, k, vv = v["q"].to(dev), v["k"].to(dev), v["v"].to(dev)
+        o = torch.empty_like(q)
+        probe = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, 4, 2, 128)
+        wsz = probe.workspace_size()
+        ws = torch.full((wsz + 4 * lay.M + 64,), 0xAB, dtype=torch.uint8, device=dev)
+        plan = planner.plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, 4, 2, 128,
+                            ws, extra=lay.delim_positions)
+        lib.mis_attention_fwd_plan(plan, q, k, vv, o, None)
+        lib.mis_attention_fwd_plan(plan, q, k, vv, o, None)     # a second launch of the same plan
+        outs.append((s, v, o, ws, plan, wsz, lay))
+    torch.cuda.synchronize()
+    for s, v, o, ws, plan, wsz, lay in outs:
+        assert lib.mis_get_device_status(ws) == lib.MIS_OK
+        # the side payload landed right after the plan
+        side = ws[wsz:wsz + 4 * lay.M].view(torch.int32).cpu().numpy()
+        assert np.array_equal(side, lay.delim_positions)
+        ro, _ = O.attention(f64(v["q"]), f64(v["k"]), f64(v["v"]), oracle_layout(s))
+        assert np.abs(f64(o) - ro).max() <= ATTN_TOL
+    planner.destroy()
