@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define MIS_ABI_VERSION 1
+#define MIS_ABI_VERSION 2
 
 typedef enum {
   MIS_OK = 0,
@@ -131,6 +131,9 @@ typedef struct {
   int64_t n_causal_tiles;  /* blocks a causal mask of the same cu_seqlens keeps */
   int64_t visible_pairs;   /* unmasked (row, key) pairs, per head              */
   int64_t workspace_bytes; /* device workspace the plan occupies               */
+  int64_t schedule;        /* MIS_SCHEDULE_PAIR or MIS_SCHEDULE_SPLIT          */
+  int64_t n_units;         /* work units of the attention kernel: query tiles  */
+                           /* x (Hq / 2) for pairs, x Hq for split             */
 } mis_plan_stats;
 
 /* Bytes of device workspace mis_plan_create() needs for this descriptor (0
@@ -256,6 +259,25 @@ uint64_t mis_set_wait_limit_ns(uint64_t ns);
  * context left usable. 0 (the default) turns it off. Process-wide; returns
  * the previous mask. */
 uint32_t mis_inject_stall(uint32_t mask);
+
+/* Attention schedule of plans created after the call (process-wide; returns
+ * the previous mode, or -1 for an unknown mode, which changes nothing).
+ *   MIS_SCHEDULE_AUTO  — the planner picks (default);
+ *   MIS_SCHEDULE_PAIR  — a unit is one query tile for two query heads that
+ *                        share a kv head; each of the block's two softmax
+ *                        streams computes one head over every key tile;
+ *   MIS_SCHEDULE_SPLIT — a unit is one query tile for one head; the streams
+ *                        take alternate key tiles and merge their partial
+ *                        (max, sum, O) in the epilogue: twice the units at
+ *                        half the length, which fills the last wave of SMs
+ *                        better, at twice the K/V tile loads per FLOP.
+ * AUTO compares the two by the largest per-SM sum of unit costs under the
+ * kernel's static unit order. PAIR needs an even Hq / Hkv; odd groups always
+ * run SPLIT. The result is the same up to float rounding either way. */
+#define MIS_SCHEDULE_AUTO 0
+#define MIS_SCHEDULE_PAIR 1
+#define MIS_SCHEDULE_SPLIT 2
+int32_t mis_set_schedule(int32_t mode);
 
 /* ------------------------------------------------------------------------
  * Allocation-free label scoring. The pages have no counterpart of this call;

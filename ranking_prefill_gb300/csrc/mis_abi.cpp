@@ -19,6 +19,7 @@ namespace {
 
 std::atomic<uint64_t> g_wait_limit_ns{200ull * 1000 * 1000};
 std::atomic<uint32_t> g_inject_stall{0};
+std::atomic<int32_t> g_schedule{MIS_SCHEDULE_AUTO};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
@@ -41,6 +42,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
 uint32_t inject_stall_mask() { return g_inject_stall.load(); }
+int32_t schedule_override() { return g_schedule.load(); }
 
 int num_sms() {
   int dev = 0, n = 0;
@@ -158,6 +160,12 @@ int mis_abi_version(void) { return MIS_ABI_VERSION; }
 uint64_t mis_set_wait_limit_ns(uint64_t ns) { return g_wait_limit_ns.exchange(ns); }
 
 uint32_t mis_inject_stall(uint32_t mask) { return g_inject_stall.exchange(mask); }
+
+int32_t mis_set_schedule(int32_t mode) {
+  if (mode != MIS_SCHEDULE_AUTO && mode != MIS_SCHEDULE_PAIR && mode != MIS_SCHEDULE_SPLIT)
+    return -1;
+  return g_schedule.exchange(mode);
+}
 
 size_t mis_plan_workspace_size(const mis_attn_desc* desc) {
   try {

@@ -11,32 +11,41 @@
 // of the former: attention work O(Lq^2 + N Lq Lbar) instead of the causal
 // O((Lq + N Lbar)^2)).
 //
-// Persistent kernel: one block per SM walks the planner's units (a query
-// tile with its key-tile list, for a pair of query heads that share a kv
-// head, or one head when the GQA group size is odd) in longest-first order,
-// snaking over the blocks. Pipelines, barriers and tensor memory carry over
-// from unit to unit: the next unit's Q and first K/V tiles load while the
-// current one finishes, and its first S product runs during the epilogue.
+// Persistent kernel: one block per SM walks the planner's units in
+// longest-first order, snaking over the blocks. A unit is a query tile with
+// its key-tile list and either
+//   * a pair of query heads that share a kv head ("pair" schedule): stream t
+//     of the block computes head t over every key tile, or
+//   * one query head ("split" schedule): stream t takes the key tiles
+//     t, t+2, t+4, ... of that head, and the two partial results (running
+//     maximum, row sum, unnormalised O) are merged in the epilogue.
+// The split schedule doubles the number of units and halves their length,
+// which the planner picks when the pair units would leave the last wave of
+// blocks half empty, and always for odd GQA group sizes. Pipelines, barriers
+// and tensor memory carry over from unit to unit: the next unit's Q and first
+// K/V tiles load while the current one finishes, and its first S product
+// runs during the epilogue.
 //
 // Warp roles (384 threads):
-//   warp 0      : TMA producer (both Q tiles of a unit, then K and V tiles
-//                 through separate rings: K is released as soon as both S
-//                 products are issued, V after both PV products)
+//   warp 0      : TMA producer (the unit's Q tiles, then K and V tiles
+//                 through separate rings: K is released once its S products
+//                 are issued, V after its PV products)
 //   warp 1      : TMEM allocator and the single thread issuing tcgen05.mma:
-//                   S_h = Q_h K^T  (SS: both operands in shared memory)
-//                   O_h += P_h V   (TS: P_h from tensor memory, V MN-major)
-//                 in the order S_0(j), PV_1(j-1), S_1(j), PV_0(j), so each
-//                 head's softmax overlaps the other head's products
-//   warps 4..7  : softmax and epilogue of head 0, warps 8..11: of head 1. One
-//                 TMEM lane (= one query row) per thread: the row max and sum
-//                 stay in the thread, no shuffles.
-// Tensor memory (512 columns): S_0 | S_1 | O_0 | O_1. P_h (bf16 pairs) is
-// written over the first half of S_h once S_h has been read. Because S_h(j)
-// is committed after PV_h(j-1) was issued, "S_h(j) ready" also means O_h and
-// the previous P_h are free, so the softmax never waits on a PV.
+//                   S_t = Q K^T  (SS: both operands in shared memory)
+//                   O_t += P_t V (TS: P_t from tensor memory, V MN-major)
+//                 in the order S_0(s), PV_1(s-1), S_1(s), PV_0(s) for step s,
+//                 so each stream's softmax overlaps the other's products
+//   warps 4..7  : softmax and epilogue of stream 0, warps 8..11: of stream 1.
+//                 One TMEM lane (= one query row) per thread: the row max and
+//                 sum stay in the thread, no shuffles.
+// Tensor memory (512 columns): S_0 | S_1 | O_0 | O_1. P_t (bf16 pairs) is
+// written over the first half of S_t once S_t has been read. Because S_t(s)
+// is committed after PV_t(s-1) was issued, "S_t(s) ready" also means O_t and
+// the previous P_t are free, so the softmax never waits on a PV.
 // The running maximum is only moved (and O rescaled in TMEM) when it grows by
 // more than 2^8; the final division by the row sum makes the result exact for
-// any reference maximum.
+// any reference maximum, and the same holds for the merge of the split
+// schedule's two partial results.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -80,8 +89,7 @@ struct AttnParams {
   int64_t o_stride;
   int32_t T;
   int32_t group;          // Hq / Hkv
-  int32_t heads;          // query heads per unit: 2 (a GQA pair) or 1
-  int32_t n_head_groups;  // Hq / heads
+  int32_t n_head_groups;  // units per query tile: Hq / 2 (pair) or Hq (split)
   float scale_log2;       // softmax scale * log2(e)
   uint32_t* status;
   uint64_t wait_ns;
@@ -97,7 +105,7 @@ __device__ __forceinline__ int unit_at(int kk, int total) {
   return u < total ? u : -1;
 }
 
-template <int D>
+template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap kmap,
@@ -111,7 +119,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   // barrier slots
   constexpr int bQF = 0, bQE = 1, bKF = 2, bKE = bKF + KS, bVF = bKE + KS, bVE = bVF + VS,
                 bSF = bVE + VS, bPF = bSF + 2, bOF = bPF + 2, bOE = bOF + 1, bDR = bOE + 2,
-                nBar = bDR + 1;
+                bXC = bDR + 1, nBar = bXC + 1;
 
   griddep_wait();                 // inputs of earlier stream work are visible
   griddep_launch_dependents();
@@ -128,7 +136,9 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nh = p.heads, n_hg = p.n_head_groups;
+  constexpr bool split = kSplit;
+  constexpr int nh = split ? 1 : 2;                    // Q tiles (heads) per unit
+  const int n_hg = p.n_head_groups;
   const int total = p.n_units * n_hg;                  // unit u: p.units[u / n_hg], head group u % n_hg
 
   if (threadIdx.x == 0) {
@@ -141,10 +151,11 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(bSF + s), 1);
       mbar_init(bar(bPF + s), 4);                      // one arrival per softmax warp
-      mbar_init(bar(bOE + s), 4);
+      mbar_init(bar(bOE + s), split ? 8 : 4);          // split: both streams read O_0 and O_1
     }
     mbar_init(bar(bOF), 1);
     mbar_init(bar(bDR), 1);
+    mbar_init(bar(bXC), 256);                          // split: (max, sum) exchange, every thread
     fence_mbar_init();
     fence_proxy_async();
   }
@@ -211,8 +222,9 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
       constexpr uint32_t idO = idesc_bf16(128, D, true);
       bool ok = true;
       if (p.stall) ok = wait(bar(bDR), 0, W, 0x7ff);   // nothing arrives before the drain
-      auto issue_s = [&](int t, int sk) {
-        const uint32_t aQ = smem_u32(sQ + t * C::kTile);
+      // S_t = Q_q K^T into the S columns of stream t (q: the Q slot)
+      auto issue_s = [&](int t, int q, int sk) {
+        const uint32_t aQ = smem_u32(sQ + q * C::kTile);
         const uint32_t aK = smem_u32(sK + sk * C::kTile);
 #pragma unroll
         for (int b = 0; b < NB; ++b)
@@ -227,60 +239,79 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks) {
           // V is MN-major (head dim contiguous): 8-key groups 1024 B apart,
-          // 64-column boxes kBox apart. P_h sits in the first columns of S_h.
+          // 64-column boxes kBox apart. P_t sits in the first columns of S_t.
           const uint64_t db = sdesc_sw128(aV + ks * 16 * 128, C::kBox, 1024);
           mma_ts(tmem + colO(t), tmem + colS(t) + ks * 8, db, idO, (acc || ks != 0) ? 1u : 0u);
         }
       };
-      int gk = 0, lu = 0;
+      // c0, c1: S products issued so far for each stream (the phase of SF_t / PF_t)
+      int gk = 0, lu = 0, c0 = 0, c1 = 0;
       for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {
         const int u = unit_at(kk, total);
         if (u < 0) continue;
         const int nk = p.units[u / n_hg].nk;
         if (!(ok = wait(bar(bQF), lu & 1, W, 0x200))) break;
-        // the first PV of head t in this unit overwrites O_t: the epilogue of
-        // the previous unit must have read it out of tensor memory
+        // the first PV of stream t in this unit overwrites O_t: the epilogue of
+        // the previous unit must have read it out of tensor memory. In the
+        // split schedule one barrier covers both accumulators, and stream 0's
+        // first PV always comes first.
         auto first_pv = [&](int t) -> bool {
-          if (lu == 0) return true;
+          if (lu == 0 || (split && t == 1)) return true;
           if (!wait(bar(bOE + t), (lu - 1) & 1, W, 0x280 + t)) return false;
           tc_fence_after();
           return true;
         };
-        for (int it = 0; ok && it < nk; ++it) {
-          const int gi = gk + it, sk = gi % KS, sv = gi % VS;
-          if (!(ok = wait(bar(bKF + sk), (gi / KS) & 1, W, 0x300))) break;
+        // unit-local key tile of stream t at step s
+        const int ns = split ? (nk + 1) / 2 : nk;
+        bool pend1 = false;            // stream 1 owes the PV of the previous step
+        int pend1_g = 0;               // ... on this key tile (global index)
+        bool pend1_acc = false, pend1_first = false;
+        auto flush_pv1 = [&]() -> bool {
+          const int pend1_v = pend1_g % VS;
+          // split: stream 1's V tile is not stream 0's, wait for it here (in
+          // the pair schedule PV_0 of the same tile already waited)
+          if (split && !wait(bar(bVF + pend1_v), (pend1_g / VS) & 1, W, 0x3c0)) return false;
+          if (!wait(bar(bPF + 1), (c1 - 1) & 1, W, 0x400)) return false;
           tc_fence_after();
-          issue_s(0, sk);
-          if (nh == 2) {
-            if (it > 0) {
-              if (!(ok = wait(bar(bPF + 1), (gi - 1) & 1, W, 0x400))) break;
+          if (pend1_first && !first_pv(1)) return false;
+          issue_pv(1, pend1_v, pend1_acc);
+          mma_commit(bar(bVE + pend1_v));
+          pend1 = false;
+          return true;
+        };
+        for (int st = 0; ok && st < ns; ++st) {
+          const int g0 = gk + (split ? 2 * st : st);
+          const int sk0 = g0 % KS, sv0 = g0 % VS;
+          if (!(ok = wait(bar(bKF + sk0), (g0 / KS) & 1, W, 0x300))) break;
+          tc_fence_after();
+          issue_s(0, 0, sk0);
+          if (split) mma_commit(bar(bKE + sk0));
+          if (pend1 && !(ok = flush_pv1())) break;
+          const int i1 = split ? 2 * st + 1 : st;
+          if (i1 < nk) {
+            const int g1 = gk + i1, sk1 = g1 % KS;
+            if (split) {
+              if (!(ok = wait(bar(bKF + sk1), (g1 / KS) & 1, W, 0x380))) break;
               tc_fence_after();
-              if (it == 1 && !(ok = first_pv(1))) break;
-              issue_pv(1, (gi - 1) % VS, it - 1 > 0);
-              mma_commit(bar(bVE + (gi - 1) % VS));
             }
-            issue_s(1, sk);
+            issue_s(1, split ? 0 : 1, sk1);
+            mma_commit(bar(bKE + sk1));
+            ++c1;
+            pend1 = true;
+            pend1_g = g1;
+            pend1_acc = st > 0;
+            pend1_first = st == 0;
           }
-          mma_commit(bar(bKE + sk));
-          if (it == nk - 1) mma_commit(bar(bQE));        // Q of this unit no longer read
-          if (!(ok = wait(bar(bVF + sv), (gi / VS) & 1, W, 0x480))) break;
-          if (!(ok = wait(bar(bPF + 0), gi & 1, W, 0x500))) break;
+          if (st == ns - 1) mma_commit(bar(bQE));        // Q of this unit no longer read
+          if (!(ok = wait(bar(bVF + sv0), (g0 / VS) & 1, W, 0x480))) break;
+          if (!(ok = wait(bar(bPF + 0), c0 & 1, W, 0x500))) break;
           tc_fence_after();
-          if (it == 0 && !(ok = first_pv(0))) break;
-          issue_pv(0, sv, it > 0);
-          if (nh == 1) mma_commit(bar(bVE + sv));
+          if (st == 0 && !(ok = first_pv(0))) break;
+          issue_pv(0, sv0, st > 0);
+          ++c0;
+          if (split) mma_commit(bar(bVE + sv0));
         }
-        if (ok && nh == 2) {
-          const int gl = gk + nk - 1;
-          if ((ok = wait(bar(bPF + 1), gl & 1, W, 0x580))) {
-            tc_fence_after();
-            if (nk == 1) ok = first_pv(1);
-            if (ok) {
-              issue_pv(1, gl % VS, nk - 1 > 0);
-              mma_commit(bar(bVE + gl % VS));
-            }
-          }
-        }
+        if (ok && pend1) ok = flush_pv1();
         if (ok) mma_commit(bar(bOF));                    // every PV of the unit done
         gk += nk;
         ++lu;
@@ -289,34 +320,40 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
       mma_commit(bar(bDR));
       wait_drain(bar(bDR), 0);
     }
-  } else if (warp >= 4 && (warp - 4) / 4 < nh) {
+  } else if (warp >= 4) {
     // ------------------------------------------------- softmax and epilogue
-    const int t = (warp - 4) / 4;                       // head of the pair
+    const int t = (warp - 4) / 4;                       // stream
     const int sw = warp & 3;
     const int r = sw * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(sw * 32) << 16);
     const uint32_t tS = tl + colS(t), tO = tl + colO(t);
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = f2_pack(__float_as_uint(sl2), __float_as_uint(sl2));
-    int gk = 0, lu = 0;
+    // split schedule: each stream's (max, sum) for the other, in the unused
+    // second Q slot
+    float2* xch = reinterpret_cast<float2*>(sQ + C::kTile);
+    int lu = 0, cs = 0;                                 // cs: S tiles of this stream so far
     bool ok = true;
     for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {
       const int u = unit_at(kk, total);
       if (u < 0) continue;
       const WorkItem un = p.units[u / n_hg];
-      const int hg = u % n_hg, h = hg * nh + t;
+      const int h = split ? u % n_hg : (u % n_hg) * 2 + t;
       const ReqInfo R = p.req[un.req];
       const int j = un.q0 + r;
       const bool valid = j < R.e0;
       const int jj = valid ? j : -1;                    // invalid rows see nothing
       const int lo = valid ? p.seg_start[j] : 0x7fffffff;
       const int nk = un.nk;
+      // key tiles of this stream: all (pair) or t, t+2, ... (split)
+      const int kstep = split ? 2 : 1, kfirst = split ? t : 0;
+      const int nkt = split ? (nk - t + 1) / 2 : nk;
       float m_ref = -INFINITY, l = 0.f;
-      uint32_t e_next = p.klist[un.kofs];
-      for (int it = 0; it < nk; ++it) {
-        const int gi = gk + it;
+      uint32_t e_next = nkt > 0 ? p.klist[un.kofs + kfirst] : 0u;
+      for (int it = 0; it < nkt; ++it) {
+        const int gi = cs + it;
         const uint32_t e = e_next;
-        if (it + 1 < nk) e_next = p.klist[un.kofs + it + 1];   // prefetch the next entry
+        if (it + 1 < nkt) e_next = p.klist[un.kofs + kfirst + (it + 1) * kstep];   // prefetch
         const int32_t c0 = (int32_t)(e & ~kNeedMask);
         const bool masked = (e & kNeedMask) != 0;
         ok = wait(bar(bSF + t), gi & 1, W, 0x600);
@@ -397,39 +434,91 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
         if (lane == 0) mbar_arrive(bar(bPF + t));       // one arrival per warp
       }
       if (!ok) break;
-      gk += nk;
+      cs += nkt;
       ok = wait(bar(bOF), lu & 1, W, 0x700);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // normalise and store bf16 O
-      const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = p.o + (int64_t)(valid ? j : 0) * p.o_stride + (int64_t)h * D;
+      auto store32 = [&](int c, const uint32_t* v) {     // 32 fp32 values as bf16
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(tO + c * 32, ov);
-        tmem_ld_wait();
-        reg_fence32(ov);
-        if (c == D / 32 - 1) {                          // O_t fully read: hand it back
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(bOE + t));
+        for (int q = 0; q < 4; ++q) {
+          uint4 w;
+          w.x = pack_bf16(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+          w.y = pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+          w.z = pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+          w.w = pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+          dst[q] = w;
         }
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+      };
+      if (!split) {
+        // normalise and store bf16 O
+        const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(ov[8 * q + 0]) * inv, __uint_as_float(ov[8 * q + 1]) * inv);
-            w.y = pack_bf16(__uint_as_float(ov[8 * q + 2]) * inv, __uint_as_float(ov[8 * q + 3]) * inv);
-            w.z = pack_bf16(__uint_as_float(ov[8 * q + 4]) * inv, __uint_as_float(ov[8 * q + 5]) * inv);
-            w.w = pack_bf16(__uint_as_float(ov[8 * q + 6]) * inv, __uint_as_float(ov[8 * q + 7]) * inv);
-            dst[q] = w;
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tO + c * 32, ov);
+          tmem_ld_wait();
+          reg_fence32(ov);
+          if (c == D / 32 - 1) {                        // O_t fully read: hand it back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bOE + t));
+          }
+          if (valid) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * inv);
+            store32(c, ov);
           }
         }
+        if (p.lse && valid) p.lse[(int64_t)h * p.T + j] = (m_ref + log2f(l)) * kLn2;
+      } else {
+        // merge the two streams' partial results of this row:
+        //   m = max(m_0, m_1), a_s = 2^(m_s - m), L = a_0 l_0 + a_1 l_1,
+        //   O = (a_0 O_0 + a_1 O_1) / L.
+        // Stream t writes the head-dim half [t D/2, (t+1) D/2).
+        xch[t * kBM + r] = make_float2(m_ref, l);
+        mbar_arrive(bar(bXC));
+        ok = wait(bar(bXC), lu & 1, W, 0x780);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const float2 other = xch[(1 - t) * kBM + r];
+        const float m = fmaxf(m_ref, other.x);
+        const float a_me = (m == -INFINITY) ? 0.f : ex2(m_ref - m);
+        const float a_ot = (m == -INFINITY) ? 0.f : ex2(other.x - m);
+        const float L = l * a_me + other.y * a_ot;
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const float w0 = (t == 0 ? a_me : a_ot) * inv, w1 = (t == 0 ? a_ot : a_me) * inv;
+        const bool has1 = nk > 1;                       // stream 1 wrote O_1 in this unit
+        const uint32_t tO0 = tl + colO(0), tO1 = tl + colO(1);
+#pragma unroll
+        for (int c2 = 0; c2 < D / 64; ++c2) {
+          const int c = t * (D / 64) + c2;
+          // O_1 is read even when stream 1 had no tile (then it holds an older
+          // unit's values, or nothing ever written) and dropped by a select
+          uint32_t o0[32], o1[32];
+          tmem_ld32(tO0 + c * 32, o0);
+          tmem_ld32(tO1 + c * 32, o1);
+          tmem_ld_wait();
+          reg_fence32(o0);
+          reg_fence32(o1);
+          if (c2 == D / 64 - 1) {                       // both halves read: hand O back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bOE + 0));
+          }
+          if (valid) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+              const float a = __uint_as_float(o0[x]) * w0;
+              o0[x] = __float_as_uint(has1 ? fmaf(__uint_as_float(o1[x]), w1, a) : a);
+            }
+            store32(c, o0);
+          }
+        }
+        if (p.lse && valid && t == 0) p.lse[(int64_t)h * p.T + j] = (m + log2f(L)) * kLn2;
       }
-      if (p.lse && valid) p.lse[(int64_t)h * p.T + j] = (m_ref + log2f(l)) * kLn2;
       ++lu;
     }
   }
@@ -470,7 +559,6 @@ mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
   prm.o_stride = os;
   prm.T = pl.T;
   prm.group = pl.Hq / pl.Hkv;
-  prm.heads = (prm.group % 2 == 0) ? 2 : 1;
   prm.n_head_groups = pl.n_head_groups;
   prm.scale_log2 = pl.scale * 1.4426950408889634f;
   prm.status = reinterpret_cast<uint32_t*>(ws);
@@ -484,7 +572,7 @@ mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
     return MIS_ERR_CUDA;
   }
   if (pl.work.empty()) return MIS_OK;
-  auto kern = mis_attn_fwd_kernel<D>;
+  auto kern = pl.split ? mis_attn_fwd_kernel<D, true> : mis_attn_fwd_kernel<D, false>;
   if (!kernel_attr_once(reinterpret_cast<const void*>(kern), C::kSmem)) return MIS_ERR_CUDA;
   const int64_t total = (int64_t)pl.work.size() * pl.n_head_groups;
   if (total > 0x7fffffff) return MIS_ERR_UNSUPPORTED;

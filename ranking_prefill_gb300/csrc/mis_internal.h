@@ -51,7 +51,9 @@ struct HostPlan {
   mis_plan_stats stats{};
   // byte offsets inside the device workspace
   size_t off_req = 0, off_seg = 0, off_work = 0, off_klist = 0, total = 0;
-  int32_t n_head_groups = 1;       // blocks' head groups per query tile (pairs or single heads)
+  bool split = false;              // split schedule (one head per unit, key tiles alternate
+                                   // between the block's two softmax streams)
+  int32_t n_head_groups = 1;       // units per query tile: Hq / 2 (pair) or Hq (split)
   void* workspace = nullptr;       // device base, set by mis_plan_create
   bool status_clear = false;       // the upload zeroed the status words; the
                                    // first launch need not clear them again
@@ -89,6 +91,8 @@ bool kernel_attr_once(const void* kernel, int smem_bytes);
 uint64_t wait_limit_ns();
 // Process-wide failure-injection mask (bit 0: attention, bit 1: scoring).
 uint32_t inject_stall_mask();
+// Process-wide attention schedule override (MIS_SCHEDULE_*).
+int32_t schedule_override();
 
 // Kernel launchers (defined in the .cu files). Return MIS_ERR_CUDA on launch
 // failure. Pointers are already validated.

@@ -25,6 +25,32 @@ namespace {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Cost of a unit in softmax-step units (one step: two 128x128 S tiles, one
+// per stream, with their PV products); a masked tile costs 5/4 of a full one.
+// kUnitCost covers a unit's Q load, epilogue and pipeline turn-around. Fitted
+// on GB300 to kernel times of both schedules on four packed batches (one
+// request of 3.5K rows, one of 18.5K, 16 requests with 201K rows in all, 256
+// requests with 174K) as time = fixed + step * makespan: a unit costs 1.5
+// steps, and the split schedule's doubled K/V tile loads show up in that
+// per-unit cost rather than in a per-step factor.
+constexpr double kUnitCost = 1.5;
+
+// Largest per-block total of unit costs when `units` (in list order, each
+// repeated `reps` times for its heads) are dealt to min(total, n_blocks)
+// persistent blocks in the kernel's snake order.
+double snake_makespan(const std::vector<double>& cost, int reps, int n_blocks) {
+  const int64_t total = (int64_t)cost.size() * reps;
+  if (total == 0) return 0.0;
+  const int64_t G = std::min<int64_t>(total, n_blocks);
+  std::vector<double> load((size_t)G, 0.0);
+  for (int64_t kk = 0; kk * G < total; ++kk)
+    for (int64_t c = 0; c < G; ++c) {
+      const int64_t u = kk * G + ((kk & 1) ? (G - 1 - c) : c);
+      if (u < total) load[(size_t)c] += cost[(size_t)(u / reps)];
+    }
+  return *std::max_element(load.begin(), load.end());
+}
+
 }  // namespace
 
 mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
@@ -77,7 +103,7 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
   }
 
   // ---- tiles ----
-  struct Tmp { int32_t req, q0, kofs, nk; int64_t cost; int64_t order; };
+  struct Tmp { int32_t req, q0, kofs, nk; int64_t cost, cost_even, cost_odd; int64_t order; };
   std::vector<Tmp> tmp;
   int64_t visible = 0, causal_tiles = 0;
   for (int b = 0; b < B; ++b) {
@@ -98,7 +124,7 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
       // interval 1: keys of Q up to the last row; interval 2: [lo_min, r1)
       const int32_t qa = 0, qb = (std::min(R.pend, r1) - R.s0 + kBN - 1) / kBN;  // [qa, qb)
       const int32_t ba = (lo_min - R.s0) / kBN, bb = (r1 - 1 - R.s0) / kBN + 1;  // [ba, bb)
-      Tmp w{b, r0, (int32_t)p->klist.size(), 0, 0, (int64_t)tmp.size()};
+      Tmp w{b, r0, (int32_t)p->klist.size(), 0, 0, 0, 0, (int64_t)tmp.size()};
       auto emit = [&](int32_t u) {
         const int32_t c0 = R.s0 + u * kBN;
         const int32_t c1 = std::min(c0 + kBN, R.e0);
@@ -111,8 +137,10 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
         p->klist.push_back((uint32_t)c0 | (need_mask ? kNeedMask : 0u));
         p->tile_map.insert(p->tile_map.end(), {b, t, u, full ? 1 : 2});
         if (full) ++p->stats.n_full; else ++p->stats.n_partial;
+        const int c = need_mask ? 5 : 4;   // masked tiles spend extra ALU in the softmax
+        (w.nk % 2 ? w.cost_odd : w.cost_even) += c;
         ++w.nk;
-        w.cost += need_mask ? 5 : 4;   // masked tiles spend extra ALU in the softmax
+        w.cost += c;
       };
       for (int32_t u = qa; u < qb; ++u) emit(u);
       for (int32_t u = std::max(ba, qb); u < bb; ++u) emit(u);
@@ -136,7 +164,29 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
   p->work.reserve(tmp.size());
   for (const Tmp& w : tmp) p->work.push_back(WorkItem{w.req, w.q0, w.kofs, w.nk});
 
-  p->n_head_groups = ((p->Hq / p->Hkv) % 2 == 0) ? p->Hq / 2 : p->Hq;
+  // ---- schedule: head pairs, or one head with the key tiles split between
+  // the two softmax streams. Pairs need an even GQA group; otherwise the one
+  // with the smaller snake makespan over the device's SMs.
+  const bool even_group = (p->Hq / p->Hkv) % 2 == 0;
+  bool split = !even_group;
+  const int32_t forced = schedule_override();
+  if (even_group && forced == MIS_SCHEDULE_SPLIT) {
+    split = true;
+  } else if (even_group && forced == MIS_SCHEDULE_AUTO && !tmp.empty()) {
+    std::vector<double> c_pair, c_split;
+    c_pair.reserve(tmp.size());
+    c_split.reserve(tmp.size());
+    for (const Tmp& w : tmp) {
+      c_pair.push_back(w.cost / 4.0 + kUnitCost);
+      c_split.push_back(std::max(w.cost_even, w.cost_odd) / 4.0 + kUnitCost);
+    }
+    const int sms = num_sms();
+    split = snake_makespan(c_split, p->Hq, sms) < snake_makespan(c_pair, p->Hq / 2, sms);
+  }
+  p->split = split;
+  p->n_head_groups = split ? p->Hq : p->Hq / 2;
+  p->stats.schedule = split ? MIS_SCHEDULE_SPLIT : MIS_SCHEDULE_PAIR;
+  p->stats.n_units = (int64_t)p->work.size() * p->n_head_groups;
 
   p->stats.n_qtiles = (int64_t)p->work.size();
   p->stats.n_tiles = p->stats.n_full + p->stats.n_partial;

@@ -33,7 +33,8 @@ EXPORTS = ["mis_status_string", "mis_abi_version", "mis_layout_size", "mis_build
            "mis_plan_tile_map", "mis_plan_destroy", "mis_attention_fwd_plan",
            "mis_attention_fwd", "mis_label_scores_workspace_size", "mis_label_scores",
            "mis_get_device_status", "mis_set_wait_limit_ns", "mis_label_scores_noalloc",
-           "mis_inject_stall", "mis_planner_create", "mis_planner_plan", "mis_planner_destroy"]
+           "mis_inject_stall", "mis_planner_create", "mis_planner_plan", "mis_planner_destroy",
+           "mis_set_schedule"]
 
 
 class MisError(RuntimeError):
@@ -51,7 +52,8 @@ class mis_attn_desc(C.Structure):
 
 class mis_plan_stats(C.Structure):
     _fields_ = [(n, C.c_int64) for n in ("n_qtiles", "n_tiles", "n_full", "n_partial",
-                                           "n_causal_tiles", "visible_pairs", "workspace_bytes")]
+                                           "n_causal_tiles", "visible_pairs", "workspace_bytes",
+                                           "schedule", "n_units")]
 
     def as_dict(self):
         return {n: int(getattr(self, n)) for n, _ in self._fields_}
@@ -91,6 +93,7 @@ def load(path: str = LIB_PATH):
         "mis_get_device_status": (C.c_int, [vp, vp]),
         "mis_set_wait_limit_ns": (C.c_uint64, [C.c_uint64]),
         "mis_inject_stall": (C.c_uint32, [C.c_uint32]),
+        "mis_set_schedule": (C.c_int32, [C.c_int32]),
         "mis_planner_create": (C.c_int, [C.POINTER(vp)]),
         "mis_planner_plan": (C.c_int, [vp, C.POINTER(mis_attn_desc), vp, sz, vp, sz, vp,
                                        C.POINTER(vp)]),
@@ -370,6 +373,17 @@ def mis_set_wait_limit_ns(ns: int) -> int:
 
 def mis_inject_stall(mask: int) -> int:
     return int(load().mis_inject_stall(int(mask)))
+
+
+SCHEDULE_AUTO, SCHEDULE_PAIR, SCHEDULE_SPLIT = 0, 1, 2
+
+
+def mis_set_schedule(mode: int) -> int:
+    """Attention schedule of plans created afterwards (process-wide); returns the previous mode."""
+    prev = int(load().mis_set_schedule(int(mode)))
+    if prev < 0:
+        raise MisError(MIS_ERR_INVALID_ARG, "mis_set_schedule")
+    return prev
 
 
 def mis_status_string(st: int) -> str:

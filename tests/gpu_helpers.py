@@ -11,6 +11,20 @@ LSE_TOL = 2e-3       # max-abs on the natural-log normaliser (fp32 exp2/log2 pat
 SCORE_TOL = 1e-2     # max-abs on label log-probs
 
 
+class forced_schedule:
+    """Plans created inside the block use the given attention schedule."""
+
+    def __init__(self, mode: int):
+        self.mode = mode
+
+    def __enter__(self):
+        self.prev = lib.mis_set_schedule(self.mode)
+        return self
+
+    def __exit__(self, *exc):
+        lib.mis_set_schedule(self.prev)
+
+
 def f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu", torch.float64).numpy()
 

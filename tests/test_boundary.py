@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(L):
     assert declared == set(lib.EXPORTS), declared ^ set(lib.EXPORTS)
     for name in declared:
         assert hasattr(L, name)
-    assert L.mis_abi_version() == 1
+    assert L.mis_abi_version() == 2
     for st in range(8):
         assert lib.mis_status_string(st) != "unknown status"
 
@@ -79,6 +79,33 @@ def test_tile_map_and_pairs_bit_exact(L):
         assert st["n_partial"] == int((ref[:, 3] == O.PARTIAL).sum())
         if lay.T <= 6000:
             assert st["visible_pairs"] == O.pair_count(lay)
+
+
+def test_schedule_override_and_units(L):
+    s = synth.draw_shapes(synth.WORKLOADS["qwen3-0.6b-layer"])
+    lay = lib.mis_build_layout(s.prefix_tokens, s.n_items, s.item_lens, with_positions=False)
+    args = (lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets)
+    prev = lib.mis_set_schedule(lib.SCHEDULE_AUTO)
+    ref_map = lib.Plan.host_only(*args, 16, 8, 128).tile_map()
+    try:
+        for mode, hq, hkv, want, per_tile in [(lib.SCHEDULE_PAIR, 16, 8, lib.SCHEDULE_PAIR, 8),
+                                              (lib.SCHEDULE_SPLIT, 16, 8, lib.SCHEDULE_SPLIT, 16),
+                                              (lib.SCHEDULE_PAIR, 12, 4, lib.SCHEDULE_SPLIT, 12),
+                                              (lib.SCHEDULE_AUTO, 6, 6, lib.SCHEDULE_SPLIT, 6)]:
+            lib.mis_set_schedule(mode)
+            st = lib.Plan.host_only(*args, hq, hkv, 128).stats()
+            assert st["schedule"] == want                 # odd GQA groups always split
+            assert st["n_units"] == st["n_qtiles"] * per_tile
+            # the schedule changes the execution order only, never the tile map
+            assert np.array_equal(lib.Plan.host_only(*args, hq, hkv, 128).tile_map(), ref_map)
+        lib.mis_set_schedule(lib.SCHEDULE_AUTO)
+        st = lib.Plan.host_only(*args, 16, 8, 128).stats()
+        assert st["schedule"] in (lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT)
+        with pytest.raises(lib.MisError):
+            lib.mis_set_schedule(7)
+        assert lib.mis_set_schedule(lib.SCHEDULE_AUTO) == lib.SCHEDULE_AUTO   # 7 changed nothing
+    finally:
+        lib.mis_set_schedule(prev)
 
 
 def test_causal_plan_is_plain_causal(L):

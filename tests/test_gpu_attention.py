@@ -12,9 +12,22 @@ import torch
 
 import oracle as O
 from ranking_prefill_gb300 import lib, synth
-from gpu_helpers import ATTN_TOL, check_attention, f64, oracle_layout, run_attention
+from gpu_helpers import ATTN_TOL, check_attention, f64, forced_schedule, oracle_layout, run_attention
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=[lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT], ids=["pair", "split"])
+def schedule(request):
+    """Run the test under both attention schedules (odd GQA groups are always split)."""
+    with forced_schedule(request.param):
+        yield request.param
+
+
+def _expect_schedule(st, mode, hq, hkv):
+    want = mode if (hq // hkv) % 2 == 0 else lib.SCHEDULE_SPLIT
+    assert st["schedule"] == want
+    assert st["n_units"] == st["n_qtiles"] * (hq // 2 if want == lib.SCHEDULE_PAIR else hq)
 
 
 def _sample_rows(lay, n, seed):
@@ -28,14 +41,15 @@ def _sample_rows(lay, n, seed):
     return sorted(rows)
 
 
-def test_tiny_workload_full():
+def test_tiny_workload_full(schedule):
     w = synth.WORKLOADS["tiny"]
     err, st = check_attention(synth.draw_shapes(w), w.hq, w.hkv, w.head_dim, w.seed)
     assert st["n_full"] + st["n_partial"] == 6
+    _expect_schedule(st, schedule, w.hq, w.hkv)
 
 
 @pytest.mark.parametrize("seed", range(6))
-def test_random_small_layouts(seed):
+def test_random_small_layouts(seed, schedule):
     rng = np.random.default_rng(100 + seed)
     B = int(rng.integers(1, 5))
     p = rng.integers(0, 400, B)
@@ -44,17 +58,18 @@ def test_random_small_layouts(seed):
     # requests without items must be plain prefixes; keep them valid
     hq, hkv = [(4, 2), (8, 2), (2, 2), (8, 8), (16, 4), (4, 1)][seed]
     D = 64 if seed % 2 else 128
-    check_attention(synth.custom_shapes(p, n, lens), hq, hkv, D, 1000 + seed)
+    err, st = check_attention(synth.custom_shapes(p, n, lens), hq, hkv, D, 1000 + seed)
+    _expect_schedule(st, schedule, hq, hkv)
 
 
 @pytest.mark.parametrize("D", [64, 128])
-def test_plain_causal_ragged(D):
+def test_plain_causal_ragged(D, schedule):
     lens = [1, 127, 128, 129, 300, 513]
     s = synth.custom_shapes([L - 1 for L in lens], [0] * len(lens), [])
     check_attention(s, 4, 2, D, 7, causal=True)
 
 
-def test_single_item_and_empty_items():
+def test_single_item_and_empty_items(schedule):
     s = synth.custom_shapes([200, 0, 5], [1, 3, 4], [150, 0, 0, 0, 1, 0, 300, 2])
     check_attention(s, 4, 2, 128, 8)
 
@@ -98,14 +113,28 @@ def test_item_permutation_invariance_on_gpu():
     assert diff <= ATTN_TOL
 
 
-def test_qwen3_layer_full():
+def test_qwen3_layer_full(schedule):
     w = synth.WORKLOADS["qwen3-0.6b-layer"]
     err, st = check_attention(synth.draw_shapes(w), w.hq, w.hkv, w.head_dim, w.seed)
     assert st["visible_pairs"] == 3120825
+    _expect_schedule(st, schedule, w.hq, w.hkv)
+
+
+def test_schedules_agree_on_a_long_unit_mix():
+    # the two schedules reduce the same terms in different orders: their
+    # outputs differ by rounding only (much less than the oracle tolerance)
+    s = synth.custom_shapes([700, 40, 1500], [9, 1, 30], [3 + 3 * i for i in range(40)])
+    outs = []
+    for mode in (lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT):
+        with forced_schedule(mode):
+            lay, v, o, lse, st, _ = run_attention(s, 8, 2, 128, 21)
+            outs.append((o.float(), lse.clone()))
+    assert (outs[0][0] - outs[1][0]).abs().max().item() <= 8e-3
+    assert (outs[0][1] - outs[1][1]).abs().max().item() <= 1e-4
 
 
 @pytest.mark.parametrize("name", ["8b-large", "decision-256", "varlen-16"])
-def test_large_workloads_sampled_rows(name):
+def test_large_workloads_sampled_rows(name, schedule):
     w = synth.WORKLOADS[name]
     s = synth.draw_shapes(w)
     lay = oracle_layout(s)
