@@ -121,7 +121,6 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
                 bSF = bVE + VS, bPF = bSF + 2, bOF = bPF + 2, bOE = bOF + 1, bDR = bOE + 2,
                 bXC = bDR + 1, nBar = bXC + 1;
 
-  griddep_wait();                 // inputs of earlier stream work are visible
   griddep_launch_dependents();
 
   extern __shared__ uint8_t smem_raw[];
@@ -141,8 +140,9 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   const int n_hg = p.n_head_groups;
   const int total = p.n_units * n_hg;                  // unit u: p.units[u / n_hg], head group u % n_hg
 
+  // prologue (shared memory and tensor memory only) overlaps the previous
+  // kernel in the stream; global memory is read after griddepcontrol.wait
   if (threadIdx.x == 0) {
-    *skip_flag = (*(volatile uint32_t*)p.status & kDevTimeout) ? 1u : 0u;
     *abort_flag = 0;
     mbar_init(bar(bQF), 1);
     mbar_init(bar(bQE), 1);
@@ -159,22 +159,28 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
     fence_mbar_init();
     fence_proxy_async();
   }
-  __syncthreads();
-  if (*skip_flag) return;                 // another block already gave up
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&qmap); tma_prefetch_desc(&kmap); tma_prefetch_desc(&vmap);
+  }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
+  griddep_wait();                         // inputs of earlier stream work are visible
+  if (threadIdx.x == 0) *skip_flag = (*(volatile uint32_t*)p.status & kDevTimeout) ? 1u : 0u;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (*skip_flag) {                       // another block already gave up
+    if (warp == 1) tmem_dealloc(tmem, 512);
+    return;
+  }
   const Waiter W{abort_flag, p.status, p.wait_ns};
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&qmap); tma_prefetch_desc(&kmap); tma_prefetch_desc(&vmap);
       int gk = 0, lu = 0, q_issued = 0, k_issued = 0, v_issued = 0;
       bool ok = true;
       for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {

@@ -59,7 +59,7 @@ constexpr float kLn2 = 0.69314718055994530942f;
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct ScoreLayout {       // byte offsets inside the scoring workspace
-  size_t gathered, part, zlab, total;
+  size_t gathered, part, zlab, bad, total;
   int32_t m_pad, n_vtiles, max_chunks;
 };
 
@@ -72,6 +72,7 @@ ScoreLayout score_layout(int32_t M, int32_t d, int32_t V, int32_t K) {
   L.gathered = off; off = align_up(off + (size_t)L.m_pad * d * 2, 1024);
   L.part = off;     off = align_up(off + (size_t)L.m_pad * L.max_chunks * 2 * sizeof(float), 256);
   L.zlab = off;     off = align_up(off + (size_t)L.m_pad * std::max(K, 1) * sizeof(float), 256);
+  L.bad = off;      off = align_up(off + (size_t)L.m_pad * sizeof(int32_t), 256);
   L.total = off;
   return L;
 }
@@ -81,27 +82,34 @@ struct ScoreParams {
   int32_t labels[16];
   float* part;        // [m_pad][n_chunks][2] = (max in log2 units, sum of 2^(z*log2e - max))
   float* zlab;        // [m_pad][K] label logits
+  const int32_t* bad; // [m_pad] 1 where the readout row was out of range
   uint32_t* status;
   uint64_t wait_ns;
   uint32_t stall;     // failure injection: wait on a barrier nothing arrives on
 };
 
 // ------------------------------------------------------------------ gather
+// Also starts the call's device status: block 0 clears the status words (no
+// other block of this launch writes them; an out-of-range row is recorded in
+// bad[] and raised by the combine kernel, which runs after every block here).
 __global__ void __launch_bounds__(128)
 mis_gather_rows_kernel(const __nv_bfloat16* __restrict__ hidden, int64_t stride, int32_t T,
                        const int32_t* __restrict__ rows, int32_t M, int32_t d,
-                       __nv_bfloat16* __restrict__ out, uint32_t* status) {
+                       __nv_bfloat16* __restrict__ out, int32_t* __restrict__ bad,
+                       uint32_t* status) {
   griddep_wait();
   griddep_launch_dependents();
   const int i = blockIdx.x;
+  if (i == 0 && threadIdx.x == 0) {
+    status[0] = 0u;
+    status[1] = 0u;
+  }
   int32_t r = -1;
   if (i < M) {
     r = rows[i];
-    if (r < 0 || r >= T) {
-      if (threadIdx.x == 0) raise_status(status, kDevIndex, (uint32_t)i);
-      r = -1;
-    }
+    if (r < 0 || r >= T) r = -1;
   }
+  if (threadIdx.x == 0) bad[i] = (i < M && r < 0) ? 1 : 0;
   const int n16 = d / 8;                              // 16-byte chunks per row
   uint4* dst = reinterpret_cast<uint4*>(out + (int64_t)i * d);
   if (r < 0) {
@@ -116,7 +124,6 @@ mis_gather_rows_kernel(const __nv_bfloat16* __restrict__ hidden, int64_t stride,
 __global__ void __launch_bounds__(256, 1)
 mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
                          const __grid_constant__ CUtensorMap wmap, const ScoreParams p) {
-  griddep_wait();
   griddep_launch_dependents();
   constexpr int bF = 0, bE = kStages, bAF = 2 * kStages, bAE = bAF + 2, bDR = bAE + 2,
                 nBar = bDR + 1;
@@ -136,8 +143,9 @@ mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
   const int nt = v_last - v_first;
   const int nkb = p.n_kb;
 
+  // prologue (shared memory and tensor memory only) overlaps the previous
+  // kernel in the stream; global memory is read after griddepcontrol.wait
   if (threadIdx.x == 0) {
-    *skip_flag = (*(volatile uint32_t*)p.status & kDevTimeout) ? 1u : 0u;
     *abort_flag = 0;
     for (int s = 0; s < kStages; ++s) { mbar_init(bar(bF + s), 1); mbar_init(bar(bE + s), 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(bar(bAF + s), 1); mbar_init(bar(bAE + s), 128); }
@@ -145,22 +153,27 @@ mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
     fence_mbar_init();
     fence_proxy_async();
   }
-  __syncthreads();
-  if (*skip_flag || nt <= 0) return;
-  if (warp == 1) {
+  if (warp == 0 && lane == 0) { tma_prefetch_desc(&amap); tma_prefetch_desc(&wmap); }
+  if (warp == 1 && nt > 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
+  griddep_wait();
+  if (threadIdx.x == 0) *skip_flag = (*(volatile uint32_t*)p.status & kDevTimeout) ? 1u : 0u;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (nt <= 0) return;
   const uint32_t tmem = *tmem_slot;
+  if (*skip_flag) {                       // another block already gave up
+    if (warp == 1) tmem_dealloc(tmem, 512);
+    return;
+  }
   const Waiter W{abort_flag, p.status, p.wait_ns};
   const int total_steps = nt * nkb;
 
   if (warp == 0) {
     if (lane == 0) {
-      tma_prefetch_desc(&amap); tma_prefetch_desc(&wmap);
       int issued = 0;
       for (int step = 0; step < total_steps; ++step) {
         const int st = step % kStages;
@@ -280,6 +293,7 @@ mis_score_combine_kernel(const ScoreParams p, float* __restrict__ out,
   const int i = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (i >= p.M) return;
+  if (lane == 0 && p.bad[i]) raise_status(p.status, kDevIndex, (uint32_t)i);
   if (*(volatile uint32_t*)p.status & kDevTimeout) return;
   const float2* pp = reinterpret_cast<const float2*>(p.part) + (int64_t)i * p.n_chunks;
   float m = -INFINITY, s = 0.f;
@@ -340,13 +354,14 @@ mis_status_t launch_score(const ScoreArgs& a, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
-  if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return MIS_ERR_CUDA;
-  if (a.M == 0) return MIS_OK;
+  if (a.M == 0)   // no kernel runs: clear the status words here
+    return cudaMemsetAsync(ws, 0, 8, st) == cudaSuccess ? MIS_OK : MIS_ERR_CUDA;
 
   __nv_bfloat16* gathered = reinterpret_cast<__nv_bfloat16*>(ws + L.gathered);
+  int32_t* bad = reinterpret_cast<int32_t*>(ws + L.bad);
   if (launch_pdl(mis_gather_rows_kernel, dim3(L.m_pad), dim3(128), 0, st,
                  static_cast<const __nv_bfloat16*>(a.hidden), a.hidden_stride, a.T, a.delim, a.M,
-                 a.d, gathered, status) != cudaSuccess)
+                 a.d, gathered, bad, status) != cudaSuccess)
     return MIS_ERR_CUDA;
 
   bool ok = true;
@@ -370,6 +385,7 @@ mis_status_t launch_score(const ScoreArgs& a, void* stream) {
   for (int l = 0; l < 16; ++l) p.labels[l] = l < a.K ? a.labels[l] : -1;
   p.part = reinterpret_cast<float*>(ws + L.part);
   p.zlab = reinterpret_cast<float*>(ws + L.zlab);
+  p.bad = bad;
   p.status = status;
   p.wait_ns = wait_limit_ns();
   p.stall = (inject_stall_mask() >> 1) & 1u;

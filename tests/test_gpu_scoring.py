@@ -79,6 +79,24 @@ def test_index_out_of_range_reports_status():
     assert np.abs(f64(out)[[0, 2]] - lp[[0, 2]]).max() <= SCORE_TOL
 
 
+def test_next_call_clears_the_status():
+    # the status words belong to the last call on the workspace: an index
+    # error is reported once, and a clean call afterwards reads MIS_OK
+    g = torch.Generator().manual_seed(5)
+    hidden = torch.randn(40, 128, generator=g).to(torch.bfloat16).cuda()
+    w = (torch.randn(700, 128, generator=g) * 0.05).to(torch.bfloat16).cuda()
+    out = torch.empty(3, 2, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(lib.mis_label_scores_workspace_size(3, 128, 700, 2), dtype=torch.uint8,
+                     device="cuda")
+    for rows, want in [([1, 40, 2], lib.MIS_ERR_DEVICE_INDEX), ([1, 39, 2], lib.MIS_OK),
+                       ([-1, 5, 6], lib.MIS_ERR_DEVICE_INDEX), ([0, 5, 6], lib.MIS_OK)]:
+        lib.mis_label_scores(hidden, w, torch.tensor(rows, dtype=torch.int32).cuda(), [3, 4], out,
+                             None, ws)
+        assert lib.mis_get_device_status(ws) == want
+    lp, _, _ = O.label_scores(f64(hidden), f64(w), [0, 5, 6], [3, 4])
+    assert np.abs(f64(out) - lp).max() <= SCORE_TOL
+
+
 def test_zero_items():
     out, ren, ws = run_scores(torch.zeros(4, 64, dtype=torch.bfloat16).cuda(),
                               torch.zeros(10, 64, dtype=torch.bfloat16).cuda(),
