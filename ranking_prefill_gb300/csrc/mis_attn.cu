@@ -68,9 +68,10 @@ template <int D>
 struct AttnCfg {
   static constexpr int kBox = kBN * 64 * 2;            // one 64-column box, 128 rows: 16 KB
   static constexpr int kTile = kBN * D * 2;            // a Q, K or V tile
-  static constexpr int kKStages = (D == 128) ? 3 : 4;
+  static constexpr int kKStages = (D == 128) ? 2 : 4;
   static constexpr int kVStages = (D == 128) ? 2 : 4;
-  static constexpr int kData = (2 + kKStages + kVStages) * kTile;
+  static constexpr int kOWarp = 32 * 128;              // O staging per softmax warp: 32 rows x 64 bf16
+  static constexpr int kData = (2 + kKStages + kVStages) * kTile + 8 * kOWarp;
   static constexpr int kSmem = kData + 512 + 1024;     // barriers + alignment slack
 };
 
@@ -109,7 +110,8 @@ template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap kmap,
-                    const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
+                    const __grid_constant__ CUtensorMap vmap,
+                    const __grid_constant__ CUtensorMap omap, const AttnParams p) {
   using C = AttnCfg<D>;
   constexpr int KS = C::kKStages, VS = C::kVStages;
   constexpr int NB = D / 64;                          // 64-column boxes per row
@@ -128,6 +130,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   uint8_t* sQ = smem;                                  // 2 tiles
   uint8_t* sK = smem + 2 * C::kTile;                   // KS tiles
   uint8_t* sV = sK + KS * C::kTile;                    // VS tiles
+  uint8_t* sO = sV + VS * C::kTile;                    // 8 x kOWarp: O staging of the softmax warps
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kData);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + nBar);
   volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -161,6 +164,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&qmap); tma_prefetch_desc(&kmap); tma_prefetch_desc(&vmap);
+    tma_prefetch_desc(&omap);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -446,37 +450,58 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
       if (!ok) break;
       tc_fence_after();
       __nv_bfloat16* orow = p.o + (int64_t)(valid ? j : 0) * p.o_stride + (int64_t)h * D;
-      auto store32 = [&](int c, const uint32_t* v) {     // 32 fp32 values as bf16
-        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+      // O leaves through a 32-row x 64-column staging buffer per warp and a
+      // TMA tensor store (asynchronous, whole rows); a warp whose 32 rows run
+      // past the request's end stores its valid rows directly instead, since
+      // the rows after them belong to the next request
+      const int row0 = un.q0 + sw * 32;
+      const bool wfull = row0 + 32 <= R.e0;
+      const uint32_t sOw = smem_u32(sO + (warp - 4) * C::kOWarp);
+      auto store64 = [&](const uint32_t* pk, int col0) {   // 64 bf16 of this row at column col0
+        if (wfull) {
+          if (lane == 0) bulk_wait_read0();               // the previous store read the buffer
+          __syncwarp();
+          const uint32_t ra = sOw + lane * 128;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 w;
-          w.x = pack_bf16(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-          w.y = pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-          w.z = pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-          w.w = pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-          dst[q] = w;
+          for (int c = 0; c < 8; ++c)                     // 128-byte swizzle: chunk c ^ (row & 7)
+            st_shared_v4(ra + ((c ^ (lane & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                         pk[4 * c + 3]);
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&omap, sOw, col0, h, row0);
+            bulk_commit();
+          }
+        } else if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + col0);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       };
       if (!split) {
-        // normalise and store bf16 O
+        // normalise O_t and store it as bf16, 64 columns at a time
         const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(tO + c * 32, ov);
-          tmem_ld_wait();
-          reg_fence32(ov);
-          if (c == D / 32 - 1) {                        // O_t fully read: hand it back
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(bOE + t));
-          }
-          if (valid) {
+        for (int hh = 0; hh < D / 64; ++hh) {
+          uint32_t pk[32];
 #pragma unroll
-            for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * inv);
-            store32(c, ov);
+          for (int c = 0; c < 2; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + hh * 64 + c * 32, ov);
+            tmem_ld_wait();
+            reg_fence32(ov);
+            if (hh == D / 64 - 1 && c == 1) {           // O_t fully read: hand it back
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar(bOE + t));
+            }
+#pragma unroll
+            for (int x = 0; x < 16; ++x)
+              pk[c * 16 + x] = pack_bf16(__uint_as_float(ov[2 * x]) * inv,
+                                         __uint_as_float(ov[2 * x + 1]) * inv);
           }
+          store64(pk, hh * 64);
         }
         if (p.lse && valid) p.lse[(int64_t)h * p.T + j] = (m_ref + log2f(l)) * kLn2;
       } else {
@@ -498,9 +523,11 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
         const float w0 = (t == 0 ? a_me : a_ot) * inv, w1 = (t == 0 ? a_ot : a_me) * inv;
         const bool has1 = nk > 1;                       // stream 1 wrote O_1 in this unit
         const uint32_t tO0 = tl + colO(0), tO1 = tl + colO(1);
+        constexpr int NH = D / 64;                      // 32-column chunks per half
+        uint32_t pk[16 * NH];
 #pragma unroll
-        for (int c2 = 0; c2 < D / 64; ++c2) {
-          const int c = t * (D / 64) + c2;
+        for (int c2 = 0; c2 < NH; ++c2) {
+          const int c = t * NH + c2;
           // O_1 is read even when stream 1 had no tile (then it holds an older
           // unit's values, or nothing ever written) and dropped by a select
           uint32_t o0[32], o1[32];
@@ -509,24 +536,35 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
           tmem_ld_wait();
           reg_fence32(o0);
           reg_fence32(o1);
-          if (c2 == D / 64 - 1) {                       // both halves read: hand O back
+          if (c2 == NH - 1) {                           // both halves read: hand O back
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(bOE + 0));
           }
-          if (valid) {
 #pragma unroll
-            for (int x = 0; x < 32; ++x) {
-              const float a = __uint_as_float(o0[x]) * w0;
-              o0[x] = __float_as_uint(has1 ? fmaf(__uint_as_float(o1[x]), w1, a) : a);
+          for (int x = 0; x < 16; ++x) {
+            float v2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float a = __uint_as_float(o0[2 * x + e]) * w0;
+              v2[e] = has1 ? fmaf(__uint_as_float(o1[2 * x + e]), w1, a) : a;
             }
-            store32(c, o0);
+            pk[c2 * 16 + x] = pack_bf16(v2[0], v2[1]);
           }
+        }
+        if constexpr (D == 128) {
+          store64(pk, t * 64);
+        } else if (valid) {                             // 32 columns: direct stores
+          uint4* dst = reinterpret_cast<uint4*>(orow + t * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
         if (p.lse && valid && t == 0) p.lse[(int64_t)h * p.T + j] = (m + log2f(L)) * kLn2;
       }
       ++lu;
     }
+    if (lane == 0) bulk_wait0();          // O stores complete before the block exits
   }
   tc_fence_before();
   __syncthreads();
@@ -551,6 +589,9 @@ mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
   CUtensorMap qm = make_tmap_bf16(q, 3, qd, qstr, box, &ok);
   CUtensorMap km = make_tmap_bf16(k, 3, kd, kstr, box, &ok);
   CUtensorMap vm = make_tmap_bf16(v, 3, kd, vstr, box, &ok);
+  const uint32_t obox[3] = {64, 1, 32};
+  const uint64_t ostr[2] = {(uint64_t)D * 2, (uint64_t)os * 2};
+  CUtensorMap om = make_tmap_bf16(o, 3, qd, ostr, obox, &ok);
   if (!ok) return MIS_ERR_CUDA;
 
   uint8_t* ws = static_cast<uint8_t*>(pl.workspace);
@@ -583,7 +624,7 @@ mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
   const int64_t total = (int64_t)pl.work.size() * pl.n_head_groups;
   if (total > 0x7fffffff) return MIS_ERR_UNSUPPORTED;
   dim3 grid((unsigned)std::min<int64_t>(total, num_sms()));
-  return launch_pdl(kern, grid, dim3(kThreads), C::kSmem, st, qm, km, vm, prm) == cudaSuccess
+  return launch_pdl(kern, grid, dim3(kThreads), C::kSmem, st, qm, km, vm, om, prm) == cudaSuccess
              ? MIS_OK
              : MIS_ERR_CUDA;
 }
