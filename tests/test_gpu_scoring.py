@@ -124,3 +124,48 @@ def test_large_workloads_sampled_items(name):
     items = sorted(set(rng.choice(lay.M, size=min(96, lay.M), replace=False).tolist()) | {0, lay.M - 1})
     for labels in s.label_sets:
         _check(v["hidden"], v["w_lm"], lay.delim_positions, labels.tolist(), items=items)
+
+
+def test_one_workspace_for_calls_of_different_shapes_and_after_a_timeout():
+    # A workspace sized for the largest call serves calls of other shapes, and
+    # a call whose waits ran out leaves nothing behind that later calls on the
+    # same workspace would read: they report MIS_OK and stay exact.
+    g = torch.Generator().manual_seed(11)
+    T = 700
+    hidden = torch.randn(T, 256, generator=g).to(torch.bfloat16)
+    w_big = (torch.randn(20000, 256, generator=g) * 0.05).to(torch.bfloat16)
+    cases = [(np.random.default_rng(1).choice(T, 300, replace=False), w_big[:5000], [7, 4999, 7]),
+             (np.random.default_rng(2).choice(T, 40, replace=False), w_big, [19999]),
+             (np.random.default_rng(3).choice(T, 260, replace=False), w_big[:9001], list(range(16)))]
+    need = max(lib.mis_label_scores_workspace_size(len(r), 256, int(wl.shape[0]), len(lb))
+               for r, wl, lb in cases)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    dev_h = hidden.cuda()
+
+    def call(rows, wl, labels):
+        out = torch.full((len(rows), len(labels)), 7.0, dtype=torch.float32, device="cuda")
+        ren = torch.full_like(out, 7.0)
+        lib.mis_label_scores(dev_h, wl.cuda(), torch.as_tensor(rows, dtype=torch.int32).cuda(),
+                             labels, out, ren, ws)
+        torch.cuda.synchronize()
+        return out, ren
+
+    def check(rows, wl, labels):
+        out, ren = call(rows, wl, labels)
+        assert lib.mis_get_device_status(ws) == lib.MIS_OK
+        lp, rn, _ = O.label_scores(f64(hidden), f64(wl), rows, labels)
+        assert np.abs(f64(out) - lp).max() <= SCORE_TOL
+        assert np.abs(f64(ren) - rn).max() <= SCORE_TOL
+
+    for c in cases:
+        check(*c)
+    old = lib.mis_set_wait_limit_ns(2_000_000)
+    lib.mis_inject_stall(2)
+    try:
+        call(*cases[0])
+        assert lib.mis_get_device_status(ws) == lib.MIS_ERR_DEVICE_TIMEOUT
+    finally:
+        lib.mis_inject_stall(0)
+        lib.mis_set_wait_limit_ns(old)
+    for c in reversed(cases):
+        check(*c)
