@@ -46,8 +46,9 @@ class MisError(RuntimeError):
 class mis_attn_desc(C.Structure):
     _fields_ = [("B", C.c_int32), ("T", C.c_int32), ("Hq", C.c_int32), ("Hkv", C.c_int32),
                 ("D", C.c_int32), ("scale", C.c_float),
-                ("cu_seqlens", C.POINTER(C.c_int32)), ("prefix_len", C.POINTER(C.c_int32)),
-                ("item_ptr", C.POINTER(C.c_int32)), ("item_offsets", C.POINTER(C.c_int32))]
+                # const int32_t* fields, passed as plain addresses
+                ("cu_seqlens", C.c_void_p), ("prefix_len", C.c_void_p),
+                ("item_ptr", C.c_void_p), ("item_offsets", C.c_void_p)]
 
 
 class mis_plan_stats(C.Structure):
@@ -71,7 +72,7 @@ def load(path: str = LIB_PATH):
         raise RuntimeError(f"MIS CUDA library not built: {path} is missing "
                            "(run ranking_prefill_gb300/build.py)")
     L = C.CDLL(path)
-    i32p = C.POINTER(C.c_int32)
+    i32p = C.c_void_p        # int32 arrays go across as plain addresses (cheap to marshal)
     vp, sz, i64 = C.c_void_p, C.c_size_t, C.c_int64
     sig = {
         "mis_status_string": (C.c_char_p, [C.c_int]),
@@ -121,8 +122,9 @@ def _i32(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
 
 
-def _ptr_i32(a: np.ndarray):
-    return a.ctypes.data_as(C.POINTER(C.c_int32))
+def _ptr_i32(a: np.ndarray) -> int:
+    """Address of a contiguous int32 array (the array must outlive the call)."""
+    return a.ctypes.data
 
 
 def _dptr(t) -> Optional[int]:
