@@ -140,9 +140,34 @@ def make_workload(name: str):
     from ranking_prefill_gb300 import lib, synth
     w = synth.WORKLOADS[name]
     shapes = synth.draw_shapes(w)
-    T, M = lib.mis_layout_size(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
+    size = lib.mis_setwise_layout_size if w.layout == "setwise" else lib.mis_layout_size
+    T, M = size(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
     vals = synth.draw_values(w.seed, T, w.hq, w.hkv, w.head_dim, w.d_model, w.vocab)
     return w, shapes, vals, T, M
+
+
+class HostLayout:
+    """The attention descriptor arrays and readout rows of one batch: MIS
+    requests (items isolated, read at their trailing DELIMs) or setwise
+    prompts (plain causal, read at their markers)."""
+
+    def __init__(self, w, shapes, with_positions=False):
+        from ranking_prefill_gb300 import lib
+        if w.layout == "setwise":
+            l = lib.mis_build_setwise_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens,
+                                             with_positions=with_positions)
+            self.item_ptr = self.item_offsets = None
+            self.readout = l.marker_positions
+        else:
+            l = lib.mis_build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens,
+                                     with_positions=with_positions)
+            self.item_ptr, self.item_offsets = l.item_ptr, l.item_offsets
+            self.readout = l.delim_positions
+        self.cu_seqlens, self.prefix_len = l.cu_seqlens, l.prefix_len
+        self.T, self.M = l.T, len(self.readout)
+
+    def plan_args(self):
+        return self.cu_seqlens, self.prefix_len, self.item_ptr, self.item_offsets
 
 
 def max_over_ranks(value: float, dist, device=None) -> float:
@@ -181,9 +206,8 @@ def run_ours(args, rank, world, dist):
     hidden, w_lm = vals["hidden"].to(dev), vals["w_lm"].to(dev)
     o = torch.empty_like(q)
     out = torch.empty(M, K, dtype=torch.float32, device=dev)
-    lay0 = lib.mis_build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
-    plan0 = lib.Plan(lay0.cu_seqlens, lay0.prefix_len, lay0.item_ptr, lay0.item_offsets,
-                     w.hq, w.hkv, w.head_dim)
+    lay0 = HostLayout(w, shapes)
+    plan0 = lib.Plan(*lay0.plan_args(), w.hq, w.hkv, w.head_dim)
     # plan workspace, followed by the batch's readout rows (uploaded together)
     wsz = plan0.workspace_size()
     ws_plan = torch.zeros(wsz + 4 * M, dtype=torch.uint8, device=dev)
@@ -199,11 +223,10 @@ def run_ours(args, rank, world, dist):
 
     def step(times=None):
         # a1: layout (host)
-        lay = lib.mis_build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens,
-                                   with_positions=False)
+        lay = HostLayout(w, shapes)
         # a2: plan (host); one asynchronous upload of the plan and the readout rows
-        plan = planner.plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets,
-                            w.hq, w.hkv, w.head_dim, ws_plan, stream=sp, extra=lay.delim_positions)
+        plan = planner.plan(*lay.plan_args(), w.hq, w.hkv, w.head_dim, ws_plan, stream=sp,
+                            extra=lay.readout)
         # a3: MIS attention
         if times is not None:
             times["a0"].record(stream)
@@ -345,14 +368,13 @@ def run_e2e(args, w, shapes, vals, labels, dev, stream, dist, world):
     used = [None, None]          # step that last read each buffer set is done
     w_lm = vals["w_lm"].to(dev)
     T = host["q"].shape[0]
-    lay = lib.mis_build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
+    lay = HostLayout(w, shapes)
     M, K = lay.M, len(labels)
     o = torch.empty_like(sets[0]["q"])
     out_dev = torch.empty(M, K, dtype=torch.float32, device=dev)
     out_host = torch.empty(M, K, dtype=torch.float32).pin_memory()
     planner = lib.Planner()
-    plan0 = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets,
-                     w.hq, w.hkv, w.head_dim)
+    plan0 = lib.Plan(*lay.plan_args(), w.hq, w.hkv, w.head_dim)
     wsz = plan0.workspace_size()
     # one plan workspace (plan + readout rows) per buffer set: the plan of step
     # i+1 is uploaded while step i may still read its own
@@ -366,8 +388,7 @@ def run_e2e(args, w, shapes, vals, labels, dev, stream, dist, world):
     def step(i):
         s = i % 2
         dbuf = sets[s]
-        l = lib.mis_build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens,
-                                 with_positions=False)
+        l = HostLayout(w, shapes)
         # inputs, then the plan (with the readout rows), on the copy stream:
         # the copy engine serves them in that order, so this step's small plan
         # upload never queues behind the next step's inputs
@@ -375,9 +396,8 @@ def run_e2e(args, w, shapes, vals, labels, dev, stream, dist, world):
             if used[s] is not None:
                 copy_stream.wait_event(used[s])
             dev_all[s].copy_(host_all, non_blocking=True)
-            plan = planner.plan(l.cu_seqlens, l.prefix_len, l.item_ptr, l.item_offsets,
-                                w.hq, w.hkv, w.head_dim, ws_plans[s], stream=copy_stream.cuda_stream,
-                                extra=l.delim_positions)
+            plan = planner.plan(*l.plan_args(), w.hq, w.hkv, w.head_dim, ws_plans[s],
+                                stream=copy_stream.cuda_stream, extra=l.readout)
             copied[s].record(copy_stream)
         stream.wait_event(copied[s])
         lib.mis_attention_fwd_plan(plan, dbuf["q"], dbuf["k"], dbuf["v"], o, None, sp)
@@ -435,6 +455,9 @@ def run_comparators(w, shapes, vals, labels, dev, stream, q, k, v, hidden, w_lm,
     from ranking_prefill_gb300 import lib
     sp = stream.cuda_stream
     flush = L2Flush(dev)
+    if w.layout == "setwise":
+        return {"mis_same_candidates": _mis_same_candidates(w, shapes, labels, dev, stream, w_lm,
+                                                            t_attn, t_score, M, flush)}
     lay = lib.mis_build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
     res = {}
     with torch.cuda.stream(stream):
@@ -492,6 +515,39 @@ def run_comparators(w, shapes, vals, labels, dev, stream, q, k, v, hidden, w_lm,
     return res
 
 
+def _mis_same_candidates(w, shapes, labels, dev, stream, w_lm, t_attn, t_score, M, flush):
+    """The same requests as MIS (items isolated, read at their DELIMs) through
+    the same kernels, against the setwise run (one causal sequence per
+    request, read at its markers). Inputs N(0, 1) drawn on the device."""
+    import torch
+    from ranking_prefill_gb300 import lib
+    sp = stream.cuda_stream
+    lay = lib.mis_build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens,
+                               with_positions=False)
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    rnd = lambda *shape: torch.randn(*shape, generator=g, device=dev).to(torch.bfloat16)
+    q, k, v = rnd(lay.T, w.hq, w.head_dim), rnd(lay.T, w.hkv, w.head_dim), rnd(lay.T, w.hkv, w.head_dim)
+    hidden = rnd(lay.T, w.d_model)
+    plan = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, w.hq, w.hkv,
+                    w.head_dim)
+    ws = torch.zeros(plan.workspace_size(), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    delim = torch.as_tensor(lay.delim_positions, device=dev)
+    out = torch.empty(lay.M, len(labels), dtype=torch.float32, device=dev)
+    wss = torch.zeros(lib.mis_label_scores_workspace_size(lay.M, w.d_model, w.vocab, len(labels)),
+                      dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        plan.create(ws, sp)
+        ta = _median_time(lambda: lib.mis_attention_fwd_plan(plan, q, k, v, o, None, sp), stream, flush)
+        ts = _median_time(lambda: lib.mis_label_scores(hidden, w_lm, delim, labels, out, None, wss,
+                                                       stream=sp), stream, flush)
+    return {"items_per_s": round(lay.M / (ta + ts), 1), "attention_ms": round(ta * 1e3, 4),
+            "scoring_ms": round(ts * 1e3, 4), "tokens": lay.T,
+            "setwise_vs_mis_kernel_time": round((t_attn + t_score) / (ta + ts), 3),
+            "note": "same candidate lengths packed as MIS requests; MIS isolates items, setwise "
+                    "markers see every candidate"}
+
+
 # ---------------------------------------------------------------- CPU oracle
 
 def _oracle_sample(w, shapes, vals, labels, budget_s, seed=0):
@@ -500,7 +556,13 @@ def _oracle_sample(w, shapes, vals, labels, budget_s, seed=0):
     of the full workload's oracle time and the sample description."""
     import oracle as O
     import torch
-    lay = O.build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
+    if w.layout == "setwise":
+        sl = O.setwise_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
+        lay, readout = sl.causal, sl.marker_positions
+    else:
+        lay = O.build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
+        readout = lay.delim_positions
+    n_read = len(readout)
     f64 = lambda t: t.to(torch.float64).numpy()
     q, k, v = f64(vals["q"]), f64(vals["k"]), f64(vals["v"])
     hidden, W = f64(vals["hidden"]), f64(vals["w_lm"])
@@ -519,20 +581,20 @@ def _oracle_sample(w, shapes, vals, labels, budget_s, seed=0):
     t_attn = timed(lambda: O.attention(q, k, v, lay, rows=rows))
     frac_r = 1.0 if rows is None else n_rows / lay.T
     # scoring: cost per item from a 4-item pilot
-    pilot_i = np.sort(rng.choice(lay.M, size=min(4, lay.M), replace=False))
-    per_item = timed(lambda: O.label_scores(hidden, W, lay.delim_positions, labels, items=pilot_i)) / len(pilot_i)
-    n_items = int(min(lay.M, max(len(pilot_i), (budget_s / 2) / max(per_item, 1e-9))))
-    items = None if n_items >= lay.M else np.sort(rng.choice(lay.M, size=n_items, replace=False))
-    t_score = timed(lambda: O.label_scores(hidden, W, lay.delim_positions, labels, items=items))
-    frac_i = 1.0 if items is None else n_items / lay.M
+    pilot_i = np.sort(rng.choice(n_read, size=min(4, n_read), replace=False))
+    per_item = timed(lambda: O.label_scores(hidden, W, readout, labels, items=pilot_i)) / len(pilot_i)
+    n_items = int(min(n_read, max(len(pilot_i), (budget_s / 2) / max(per_item, 1e-9))))
+    items = None if n_items >= n_read else np.sort(rng.choice(n_read, size=n_items, replace=False))
+    t_score = timed(lambda: O.label_scores(hidden, W, readout, labels, items=items))
+    frac_i = 1.0 if items is None else n_items / n_read
     t_full = t_attn / frac_r + t_score / frac_i
     if rows is None and items is None:
-        sample = f"oracle on the whole workload ({lay.T} rows x {w.hq} heads, {lay.M} items)"
+        sample = f"oracle on the whole workload ({lay.T} rows x {w.hq} heads, {n_read} items)"
     else:
         sample = (f"oracle on {'all' if rows is None else n_rows} of {lay.T} rows x {w.hq} heads and "
-                  f"{'all' if items is None else n_items} of {lay.M} items; full-workload time "
+                  f"{'all' if items is None else n_items} of {n_read} items; full-workload time "
                   f"extrapolated by rows and items")
-    return t_full, lay.M, sample, t_attn + t_score
+    return t_full, n_read, sample, t_attn + t_score
 
 
 def cpu_baseline(w, shapes, vals, labels, budget_s):

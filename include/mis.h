@@ -96,6 +96,31 @@ mis_status_t mis_build_layout(int32_t B, const int32_t* prefix_tokens, const int
                               int32_t* position_ids, int64_t position_cap);
 
 /* ------------------------------------------------------------------------
+ * Setwise (multi-marker) layout: the anchor-based setwise prompt of "Scaling
+ * JEV-like Decision Models with SGLang", section "Benchmark: Fused-Choice vs.
+ * Setwise Scoring". Request b is ONE plain causal sequence: its
+ * query_tokens[b] query tokens, the tokens of its n_cands[b] candidates
+ * (cand_lens, request after request), then one marker per candidate; the
+ * marker rows are the readout rows, in candidate order, and each sees every
+ * candidate (no item isolation). Attention runs with a plain causal plan
+ * (prefix_len[b] = request length, item_ptr = NULL) and scoring with
+ * mis_label_scores at marker_positions.
+ *   cu_seqlens       — host [B+1] out
+ *   prefix_len       — host [B] out (= request length)
+ *   marker_positions — host [M] out, M = sum of n_cands (may be NULL when M = 0)
+ *   position_ids     — host [T] out (0..len-1 per request) or NULL
+ * A request with no query token and no candidate is MIS_ERR_SHAPE.
+ * ------------------------------------------------------------------------ */
+mis_status_t mis_setwise_layout_size(int32_t B, const int32_t* query_tokens,
+                                     const int32_t* n_cands, const int32_t* cand_lens,
+                                     int64_t* T_out, int64_t* M_out);
+mis_status_t mis_build_setwise_layout(int32_t B, const int32_t* query_tokens,
+                                      const int32_t* n_cands, const int32_t* cand_lens,
+                                      int32_t* cu_seqlens, int32_t* prefix_len,
+                                      int32_t* marker_positions, int32_t* position_ids,
+                                      int64_t position_cap);
+
+/* ------------------------------------------------------------------------
  * Attention descriptor (all arrays host memory, read during planning only).
  *   B, T         — requests and packed rows; cu_seqlens[B] must equal T
  *   Hq, Hkv      — query / key-value heads; Hq % Hkv == 0; query head h

@@ -29,6 +29,10 @@ What it computes, and where each step comes from:
 * ``tile_map`` — which (q-tile, k-tile) blocks of the mask are empty, full or
   partial, counted element by element from ``mask_rows``.
 * ``cost_ratio`` — eq. (5), the prefill-token reduction factor R(N).
+* ``setwise_layout`` — the anchor-based setwise prompt of "Scaling JEV-like
+  Decision Models with SGLang" (section "Benchmark: Fused-Choice vs. Setwise
+  Scoring"): query, every candidate, then one marker per candidate, as one
+  plain causal sequence, scored at each marker.
 
 Readings taken where the pages are silent or garbled (each is also listed in
 the design notes):
@@ -125,6 +129,60 @@ def build_layout(prefix_tokens: Sequence[int], n_items: Sequence[int],
     i32 = lambda a: np.asarray(a, dtype=np.int32)
     return Layout(i32(cu), i32(plen), i32(iptr), i32(offs), i32(ends), i32(delims),
                   i32(pos), i32(req_of), i32(item_of))
+
+
+@dataclass
+class SetwiseLayout:
+    """A batch of setwise prompts: one plain causal sequence per request."""
+
+    causal: Layout               # the attention layout (no item sets)
+    cand_offsets: np.ndarray     # [M] absolute first row of each candidate's tokens
+    marker_positions: np.ndarray # [M] absolute marker row of each candidate (readout rows)
+
+    @property
+    def M(self) -> int:
+        return len(self.marker_positions)
+
+
+def setwise_layout(query_tokens: Sequence[int], n_cands: Sequence[int],
+                   cand_lens: Sequence[int]) -> SetwiseLayout:
+    """Setwise (anchor-based) prompts, token by token.
+
+    Per request: its query tokens (context, question, instruction), then the
+    tokens of every candidate in order, then one marker per candidate. The
+    prompt "ends with one marker per candidate", the markers "correspond to A,
+    B, and C in order", and "all markers follow the complete candidate list, so
+    each readout can attend to every candidate" ("Scaling JEV-like Decision
+    Models with SGLang", "Benchmark: Fused-Choice vs. Setwise Scoring"); MIS is
+    off, so attention is plain causal over the whole request. Marker i of a
+    request is the readout row of its candidate i.
+    """
+    query_tokens = [int(x) for x in query_tokens]
+    n_cands = [int(x) for x in n_cands]
+    cand_lens = [int(x) for x in cand_lens]
+    if len(query_tokens) != len(n_cands) or sum(n_cands) != len(cand_lens):
+        raise ValueError("inconsistent request description")
+    lengths, offs, marks = [], [], []
+    t, c = 0, 0
+    for q, n in zip(query_tokens, n_cands):
+        if q < 0 or n < 0:
+            raise ValueError("negative length")
+        start = t
+        t += q                                    # query
+        for _ in range(n):                        # candidate texts
+            if cand_lens[c] < 0:
+                raise ValueError("negative candidate length")
+            offs.append(t)
+            t += cand_lens[c]
+            c += 1
+        for _ in range(n):                        # one marker per candidate
+            marks.append(t)
+            t += 1
+        if t == start:
+            raise ValueError("empty request")
+        lengths.append(t - start)
+    i32 = lambda a: np.asarray(a, dtype=np.int32)
+    return SetwiseLayout(causal_layout(lengths), i32(offs), i32(marks))
 
 
 def causal_layout(lengths: Sequence[int]) -> Layout:

@@ -268,3 +268,59 @@ extern "C" mis_status_t mis_build_layout(int32_t B, const int32_t* prefix_tokens
   }
   return MIS_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Setwise layout (C ABI): per request its query tokens, every candidate's
+// tokens, then one marker per candidate, as one plain causal sequence; the
+// marker rows are the readout rows, in candidate order ("Scaling JEV-like
+// Decision Models with SGLang", "Benchmark: Fused-Choice vs. Setwise Scoring").
+// ---------------------------------------------------------------------------
+extern "C" mis_status_t mis_setwise_layout_size(int32_t B, const int32_t* query_tokens,
+                                                const int32_t* n_cands, const int32_t* cand_lens,
+                                                int64_t* T_out, int64_t* M_out) {
+  if (B < 1 || !query_tokens || !n_cands) return MIS_ERR_INVALID_ARG;
+  int64_t T = 0, M = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    if (query_tokens[b] < 0 || n_cands[b] < 0) return MIS_ERR_INVALID_ARG;
+    if (query_tokens[b] == 0 && n_cands[b] == 0) return MIS_ERR_SHAPE;   // empty request
+    T += (int64_t)query_tokens[b] + n_cands[b];                           // query + markers
+    M += n_cands[b];
+  }
+  if (M > 0 && !cand_lens) return MIS_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < M; ++i) {
+    if (cand_lens[i] < 0) return MIS_ERR_INVALID_ARG;
+    T += cand_lens[i];
+  }
+  if (T >= ((int64_t)1 << 31) - mis::kBN) return MIS_ERR_SHAPE;
+  if (T_out) *T_out = T;
+  if (M_out) *M_out = M;
+  return MIS_OK;
+}
+
+extern "C" mis_status_t mis_build_setwise_layout(int32_t B, const int32_t* query_tokens,
+                                                 const int32_t* n_cands, const int32_t* cand_lens,
+                                                 int32_t* cu_seqlens, int32_t* prefix_len,
+                                                 int32_t* marker_positions, int32_t* position_ids,
+                                                 int64_t position_cap) {
+  int64_t T = 0, M = 0;
+  mis_status_t st = mis_setwise_layout_size(B, query_tokens, n_cands, cand_lens, &T, &M);
+  if (st != MIS_OK) return st;
+  if (!cu_seqlens || !prefix_len) return MIS_ERR_INVALID_ARG;
+  if (M > 0 && !marker_positions) return MIS_ERR_INVALID_ARG;
+  if (position_ids && position_cap < T) return MIS_ERR_SHAPE;
+  int32_t row = 0, c = 0, m = 0;
+  cu_seqlens[0] = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    int32_t len = query_tokens[b];
+    for (int32_t i = 0; i < n_cands[b]; ++i) len += cand_lens[c + i];
+    c += n_cands[b];
+    for (int32_t i = 0; i < n_cands[b]; ++i) marker_positions[m++] = row + len + i;
+    len += n_cands[b];
+    if (position_ids)
+      for (int32_t t = 0; t < len; ++t) position_ids[row + t] = t;
+    prefix_len[b] = len;                 // every row in the shared set: plain causal
+    row += len;
+    cu_seqlens[b + 1] = row;
+  }
+  return MIS_OK;
+}

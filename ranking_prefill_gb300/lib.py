@@ -34,7 +34,7 @@ EXPORTS = ["mis_status_string", "mis_abi_version", "mis_layout_size", "mis_build
            "mis_attention_fwd", "mis_label_scores_workspace_size", "mis_label_scores",
            "mis_get_device_status", "mis_set_wait_limit_ns", "mis_label_scores_noalloc",
            "mis_inject_stall", "mis_planner_create", "mis_planner_plan", "mis_planner_destroy",
-           "mis_set_schedule"]
+           "mis_set_schedule", "mis_setwise_layout_size", "mis_build_setwise_layout"]
 
 
 class MisError(RuntimeError):
@@ -95,6 +95,10 @@ def load(path: str = LIB_PATH):
         "mis_set_wait_limit_ns": (C.c_uint64, [C.c_uint64]),
         "mis_inject_stall": (C.c_uint32, [C.c_uint32]),
         "mis_set_schedule": (C.c_int32, [C.c_int32]),
+        "mis_setwise_layout_size": (C.c_int, [C.c_int32, i32p, i32p, i32p, C.POINTER(i64),
+                                              C.POINTER(i64)]),
+        "mis_build_setwise_layout": (C.c_int, [C.c_int32, i32p, i32p, i32p, i32p, i32p, i32p,
+                                               i32p, i64]),
         "mis_planner_create": (C.c_int, [C.POINTER(vp)]),
         "mis_planner_plan": (C.c_int, [vp, C.POINTER(mis_attn_desc), vp, sz, vp, sz, vp,
                                        C.POINTER(vp)]),
@@ -189,6 +193,52 @@ def mis_build_layout(prefix_tokens, n_items, item_lens, with_positions: bool = T
                               _ptr_i32(pos) if with_positions else None, T if with_positions else 0),
            "mis_build_layout")
     return Layout(cu, pl, ip, io[:M], dp[:M], pos if with_positions else np.zeros(0, np.int32))
+
+
+@dataclass
+class SetwiseLayout:
+    """Setwise prompts: plain causal sequences scored at their marker rows."""
+    cu_seqlens: np.ndarray
+    prefix_len: np.ndarray        # = request lengths (plain causal)
+    marker_positions: np.ndarray  # readout rows, request by request, candidate order
+    position_ids: np.ndarray
+
+    @property
+    def T(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def B(self) -> int:
+        return len(self.prefix_len)
+
+    @property
+    def M(self) -> int:
+        return len(self.marker_positions)
+
+
+def mis_setwise_layout_size(query_tokens, n_cands, cand_lens):
+    L = load()
+    q, n, c = _i32(query_tokens), _i32(n_cands), _i32(cand_lens)
+    T, M = C.c_int64(), C.c_int64()
+    _check(L.mis_setwise_layout_size(len(q), _ptr_i32(q), _ptr_i32(n), _ptr_i32(c) if c.size else None,
+                                     C.byref(T), C.byref(M)), "mis_setwise_layout_size")
+    return T.value, M.value
+
+
+def mis_build_setwise_layout(query_tokens, n_cands, cand_lens,
+                             with_positions: bool = True) -> SetwiseLayout:
+    L = load()
+    q, n, c = _i32(query_tokens), _i32(n_cands), _i32(cand_lens)
+    T, M = mis_setwise_layout_size(q, n, c)
+    B = len(q)
+    cu, pl = np.zeros(B + 1, np.int32), np.zeros(B, np.int32)
+    mk = np.zeros(max(M, 1), np.int32)
+    pos = np.zeros(T if with_positions else 1, np.int32)
+    _check(L.mis_build_setwise_layout(B, _ptr_i32(q), _ptr_i32(n), _ptr_i32(c) if c.size else None,
+                                      _ptr_i32(cu), _ptr_i32(pl), _ptr_i32(mk),
+                                      _ptr_i32(pos) if with_positions else None,
+                                      T if with_positions else 0), "mis_build_setwise_layout")
+    return SetwiseLayout(cu, pl, mk[:M], pos if with_positions else np.zeros(0, np.int32))
 
 
 # ---------------------------------------------------------------------- plan

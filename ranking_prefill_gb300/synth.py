@@ -14,7 +14,11 @@ Recipe (the same for every consumer):
     the order Q, K, V, hidden, W_lm, each rounded to bf16 (round to nearest
     even). Q, K, V and hidden are N(0, 1); W_lm is N(0, 0.02^2).
 
-The five workloads mirror the shapes of the pages' workloads: a long shared
+The "setwise" workload reads a draw as setwise prompts (query, candidates,
+one marker per candidate; "Scaling JEV-like Decision Models with SGLang",
+Benchmark: Fused-Choice vs. Setwise Scoring).
+
+The five MIS workloads mirror the shapes of the pages' workloads: a long shared
 member/profile prefix followed by many short candidate items ("From
 Generation to Scoring", Section 6.1 Setup; "Turbocharging LinkedIn's
 recommendation systems with SGLang", Results / Figure 3; "Scaling JEV-like
@@ -45,6 +49,8 @@ class Workload:
     vocab: int
     label_sets: Tuple[int, ...] = (2,)   # K of each requested label set
     note: str = ""
+    layout: str = "mis"              # "mis": packed MIS requests; "setwise": the same
+                                     # lengths read as query / candidates, one marker each
 
 
 WORKLOADS = {
@@ -67,6 +73,13 @@ WORKLOADS = {
         "decision-256", 5, 256, (256, 256), (3, 10), (64, 64), 16, 8, 128, 1024,
         151936, (2, 3),
         "256 requests, prefix 256, U[3,10] items of 64 tokens, K=2 and K=3"),
+    # decision-256's draw (same seed) as setwise prompts: the prefix lengths are
+    # the query lengths and the items the candidates, followed by one marker each
+    "setwise-256": Workload(
+        "setwise-256", 5, 256, (256, 256), (3, 10), (64, 64), 16, 8, 128, 1024,
+        151936, (2, 3),
+        "decision-256's requests as setwise prompts: query 256, U[3,10] candidates of "
+        "64 tokens, one marker per candidate, plain causal", layout="setwise"),
 }
 
 # Index order used by tests and the benchmark (1-based, matching the seeds).

@@ -185,3 +185,30 @@ def test_layout_argument_errors(L):
     with pytest.raises(lib.MisError) as e:
         lib.mis_build_layout([2 ** 31 - 2], [0], [])
     assert e.value.status == lib.MIS_ERR_SHAPE
+
+
+def test_setwise_layout_bit_exact(L):
+    rng = np.random.default_rng(77)
+    cases = [([40], [3], [7, 12, 9]), ([0, 5], [2, 0], [3, 4]), ([1], [0], [])]
+    for _ in range(20):
+        B = int(rng.integers(1, 6))
+        qt = rng.integers(0, 300, B)
+        n = rng.integers(0, 12, B)
+        qt[(qt == 0) & (n == 0)] = 1
+        cases.append((qt.tolist(), n.tolist(), rng.integers(0, 80, int(n.sum())).tolist()))
+    for qt, n, lens in cases:
+        got = lib.mis_build_setwise_layout(qt, n, lens)
+        ref = O.setwise_layout(qt, n, lens)
+        assert np.array_equal(got.cu_seqlens, ref.causal.cu_seqlens)
+        assert np.array_equal(got.prefix_len, ref.causal.prefix_len)   # plain causal
+        assert np.array_equal(got.marker_positions, ref.marker_positions)
+        assert np.array_equal(got.position_ids, ref.causal.position_ids)
+        # the attention plan of a setwise batch is the causal plan
+        p = lib.Plan.host_only(got.cu_seqlens, got.prefix_len, None, None, 4, 2, 64)
+        assert np.array_equal(p.tile_map(), O.tile_map(ref.causal, 128, 128))
+    with pytest.raises(lib.MisError) as e:
+        lib.mis_build_setwise_layout([0, 3], [0, 1], [2])           # empty request
+    assert e.value.status == lib.MIS_ERR_SHAPE
+    with pytest.raises(lib.MisError) as e:
+        lib.mis_build_setwise_layout([3], [1], [-2])
+    assert e.value.status == lib.MIS_ERR_INVALID_ARG

@@ -357,3 +357,85 @@ def test_cost_ratio_against_printed_workload_numbers():
         n = len(lens)
         assert abs(O.cost_ratio(700, lens) - n * (1 + rho) / (n + rho)) < 1e-9
     assert O.cost_ratio(500, [30]) == 1.0      # one item: nothing to share
+
+
+# ------------------------------------------------------------------ setwise ----
+
+def _setwise_golden():
+    g = {}
+    with open(os.path.join(GOLDEN, "setwise_example.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                key, *vals = line.split()
+                g[key] = vals
+    return g
+
+
+def test_setwise_layout_follows_the_pages_example():
+    # three options A, B, C, then one marker per option; one score row per
+    # marker, in option order, every marker after the whole option list
+    g = _setwise_golden()
+    n = int(g["candidates"][0])
+    assert int(g["markers"][0]) == n and len(g["row_order"]) == n
+    q, lens = 40, [7, 12, 9]
+    sl = O.setwise_layout([q], [n], lens)
+    assert sl.M == n
+    cand_end = sl.cand_offsets[-1] + lens[-1]
+    assert int(g["marker_rows_after_last_candidate"][0]) == 1
+    assert (sl.marker_positions >= cand_end).all()                 # after the whole list
+    assert list(sl.marker_positions) == sorted(sl.marker_positions)  # A, B, C in order
+    assert sl.causal.T == q + sum(lens) + n
+    # candidate i starts where the text before it ends
+    starts = q + np.concatenate([[0], np.cumsum(lens)[:-1]])
+    assert list(sl.cand_offsets) == list(starts)
+    # every marker sees every candidate token (plain causal: no isolation)
+    for m in sl.marker_positions:
+        vis = O.mask_rows(sl.causal, 0, np.array([m]))[0]
+        assert vis[: cand_end].all()
+
+
+def test_setwise_attention_is_plain_causal_sdpa():
+    sl = O.setwise_layout([11, 0, 5], [3, 2, 0], [4, 0, 6, 3, 2])
+    hq, hkv, D = 4, 2, 16
+    q, k, v = _qkv(sl.causal.T, hq, hkv, D, 31)
+    o, _ = O.attention(q, k, v, sl.causal)
+    cu = sl.causal.cu_seqlens
+    for b in range(sl.causal.B):
+        s0, e0 = cu[b], cu[b + 1]
+        tq = torch.from_numpy(q[s0:e0]).permute(1, 0, 2)
+        tk = torch.from_numpy(k[s0:e0]).permute(1, 0, 2).repeat_interleave(hq // hkv, 0)
+        tv = torch.from_numpy(v[s0:e0]).permute(1, 0, 2).repeat_interleave(hq // hkv, 0)
+        ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True)
+        np.testing.assert_allclose(o[s0:e0], ref.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+
+
+def test_setwise_markers_read_every_candidate_unlike_mis():
+    # Changing candidate 1's values moves every marker's output in setwise,
+    # while under MIS only item 1's own rows move (eq. 4 isolates items).
+    q_t, lens = 9, [5, 6, 4]
+    sl = O.setwise_layout([q_t], [3], lens)
+    hq, hkv, D = 2, 1, 8
+    q, k, v = _qkv(sl.causal.T, hq, hkv, D, 32)
+    o1, _ = O.attention(q, k, v, sl.causal)
+    v2 = v.copy()
+    a = sl.cand_offsets[1]
+    v2[a:a + lens[1]] += 1.0
+    o2, _ = O.attention(q, k, v2, sl.causal)
+    moved = np.abs(o2 - o1).max(axis=(1, 2)) > 1e-9
+    assert moved[sl.marker_positions].all()
+    assert not moved[:a].any()                       # causal: rows before candidate 1 unchanged
+    lay = O.build_layout([q_t], [3], lens)
+    qm, km, vm = _qkv(lay.T, hq, hkv, D, 33)
+    m1, _ = O.attention(qm, km, vm, lay)
+    vm2 = vm.copy()
+    vm2[lay.item_offsets[1]:lay.item_ends[1]] += 1.0
+    m2, _ = O.attention(qm, km, vm2, lay)
+    moved = np.abs(m2 - m1).max(axis=(1, 2)) > 1e-9
+    assert moved[lay.delim_positions[1]] and not moved[lay.delim_positions[[0, 2]]].any()
+
+
+def test_setwise_layout_rejects_bad_requests():
+    with pytest.raises(ValueError):
+        O.setwise_layout([0], [0], [])                  # empty request
+    with pytest.raises(ValueError):
+        O.setwise_layout([3], [2], [1])                 # inconsistent counts
