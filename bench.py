@@ -10,6 +10,7 @@ TFLOP/s against the measured dense BF16 peak.
 
   python bench.py [--gpus N --steps K --warmup W] [--workload NAME]
   python bench.py --impl reference      # the fp64 CPU oracle on the host cores
+  python bench.py --sweep               # request-size sweep N = 1..200 vs eq. 5's R(N)
 
 Prints one JSON line (rank 0). Under torchrun every rank runs its own copy of
 the workload (requests are independent: no exchange), the timed region is
@@ -548,6 +549,72 @@ def _mis_same_candidates(w, shapes, labels, dev, stream, w_lm, t_attn, t_score, 
                     "markers see every candidate"}
 
 
+# ------------------------------------------------------- request-size sweep
+
+def run_sweep(args):
+    """Request-size sweep ("From Generation to Scoring", Section 6.4, RQ3): the
+    same members and candidates scored as requests of N items for N = 1..200.
+    Each request re-prefills its member's query. Reports per N the kernel time
+    per label (attention + scoring, L2 evicted between repetitions), the
+    speedup over N = 1, and eq. 5's prefill-token ratio R(N) computed from the
+    raw token counts (delimiters omitted, as in eq. 5)."""
+    import torch
+    from ranking_prefill_gb300 import lib, synth
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS["qwen3-0.6b-layer"]           # heads, head dim, model and vocabulary sizes
+    pool = synth.sweep_pool(args.sweep_members, w.vocab)
+    labels = [int(x) for x in pool.labels]
+    stream = torch.cuda.Stream(dev)
+    sp = stream.cuda_stream
+    flush = L2Flush(dev)
+    g = torch.Generator(device=dev).manual_seed(6)
+    w_lm = (torch.randn(w.vocab, w.d_model, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    rows = []
+    for n in synth.SWEEP_N:
+        shapes = synth.sweep_shapes(pool, n)
+        lay = lib.mis_build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens,
+                                   with_positions=False)
+        T, M = lay.T, lay.M
+        rnd = lambda *shape: torch.randn(*shape, generator=g, device=dev).to(torch.bfloat16)
+        q, k, v = rnd(T, w.hq, w.head_dim), rnd(T, w.hkv, w.head_dim), rnd(T, w.hkv, w.head_dim)
+        hidden = rnd(T, w.d_model)
+        o = torch.empty_like(q)
+        plan = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, w.hq,
+                        w.hkv, w.head_dim)
+        ws = torch.zeros(plan.workspace_size(), dtype=torch.uint8, device=dev)
+        delim = torch.as_tensor(lay.delim_positions, device=dev)
+        out = torch.empty(M, len(labels), dtype=torch.float32, device=dev)
+        wss = torch.zeros(lib.mis_label_scores_workspace_size(M, w.d_model, w.vocab, len(labels)),
+                          dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(stream):
+            plan.create(ws, sp)
+            ta = _median_time(lambda: lib.mis_attention_fwd_plan(plan, q, k, v, o, None, sp),
+                              stream, flush, reps=5)
+            ts = _median_time(lambda: lib.mis_label_scores(hidden, w_lm, delim, labels, out, None,
+                                                           wss, stream=sp), stream, flush, reps=5)
+        torch.cuda.synchronize()
+        assert lib.mis_get_device_status(ws) == 0 and lib.mis_get_device_status(wss) == 0
+        raw = int(shapes.prefix_tokens.sum()) + int(shapes.item_lens.sum())
+        rows.append({"N": n, "requests": int(len(shapes.prefix_tokens)), "tokens": T,
+                     "raw_tokens": raw, "pairs": plan.stats()["visible_pairs"],
+                     "attention_ms": round(ta * 1e3, 4), "scoring_ms": round(ts * 1e3, 4),
+                     "labels_per_s": round(M / (ta + ts), 1)})
+        del q, k, v, hidden, o, ws, out, wss, plan
+        torch.cuda.empty_cache()
+    b = rows[0]
+    for r in rows:
+        r["speedup_vs_n1"] = round(r["labels_per_s"] / b["labels_per_s"], 3)
+        r["attention_speedup_vs_n1"] = round(b["attention_ms"] / r["attention_ms"], 3)
+        r["R_eq5"] = round(b["raw_tokens"] / r["raw_tokens"], 3)
+        r["pairs_ratio_vs_n1"] = round(b["pairs"] / r["pairs"], 3)
+    return {"sweep": "request size", "members": args.sweep_members,
+            "candidates_per_member": synth.SWEEP_CANDIDATES, "labels": M,
+            "model": {"hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim, "d_model": w.d_model,
+                      "vocab": w.vocab},
+            "query_tokens": [int(x) for x in pool.query_tokens], "rows": rows}
+
+
 # ---------------------------------------------------------------- CPU oracle
 
 def _oracle_sample(w, shapes, vals, labels, budget_s, seed=0):
@@ -635,6 +702,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3-0.6b-layer")
+    ap.add_argument("--sweep", action="store_true",
+                    help="request-size sweep N = 1..200 (prints its own JSON table)")
+    ap.add_argument("--sweep-members", type=int, default=16)
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -651,7 +721,9 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         tdist.init_process_group("nccl")
         dist = tdist
-    if args.impl == "reference":
+    if args.sweep:
+        res = run_sweep(args) if rank == 0 else None
+    elif args.impl == "reference":
         res = run_reference(args, rank, world)
     else:
         res = run_ours(args, rank, world, dist)

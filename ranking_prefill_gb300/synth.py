@@ -162,3 +162,48 @@ def shard_requests(n_requests: int, rank: int, world: int) -> np.ndarray:
     start = rank * base + min(rank, extra)
     stop = start + base + (1 if rank < extra else 0)
     return np.arange(start, stop, dtype=np.int64)
+
+
+# ---------------------------------------------------------------------------
+# Request-size sweep ("From Generation to Scoring", Section 6.4, RQ3 and
+# Figure 6): members with one query each and 200 candidates each; for a given
+# N every member's candidates are split, in order, into requests of N items,
+# and each request carries the member's whole query. Query lengths follow
+# Section 6.1's workload (mean 744, median 543, 95th percentile 2,047 tokens):
+# log-normal with median 543 and sigma = sqrt(2 ln(744 / 543)), which puts
+# its 95th percentile at about 2,000. Members take the distribution's
+# quantiles at (i + 1/2) / members (a stratified draw: 16 members already
+# give mean 721 and median 544); candidates are nearly constant, U[24, 32]
+# tokens (mean 28), drawn from the seed.
+# ---------------------------------------------------------------------------
+
+SWEEP_CANDIDATES = 200
+SWEEP_N = (1, 2, 5, 10, 20, 50, 100, 200)
+
+
+@dataclass
+class SweepPool:
+    query_tokens: np.ndarray     # int32 [members]
+    cand_lens: np.ndarray        # int32 [members, SWEEP_CANDIDATES]
+    labels: np.ndarray           # int32 [2]
+
+
+def sweep_pool(members: int, vocab: int = 151936, seed: int = 6) -> SweepPool:
+    from statistics import NormalDist
+    rng = np.random.default_rng(seed)
+    sigma = float(np.sqrt(2.0 * np.log(744.0 / 543.0)))
+    z = np.array([NormalDist().inv_cdf((i + 0.5) / members) for i in range(members)])
+    q = np.clip(np.rint(543.0 * np.exp(sigma * z)), 1, 16384)
+    c = rng.integers(24, 32 + 1, size=(members, SWEEP_CANDIDATES))
+    labels = rng.choice(vocab, size=2, replace=False)
+    return SweepPool(q.astype(np.int32), c.astype(np.int32), labels.astype(np.int32))
+
+
+def sweep_shapes(pool: SweepPool, n: int) -> Shapes:
+    """The pool as requests of ``n`` items each (``n`` divides 200)."""
+    if SWEEP_CANDIDATES % n:
+        raise ValueError("N must divide the candidate count")
+    per = SWEEP_CANDIDATES // n
+    prefix = np.repeat(pool.query_tokens, per).astype(np.int32)
+    n_items = np.full(len(prefix), n, np.int32)
+    return Shapes(prefix, n_items, pool.cand_lens.reshape(-1).astype(np.int32), [pool.labels])
