@@ -29,6 +29,10 @@ What it computes, and where each step comes from:
 * ``tile_map`` — which (q-tile, k-tile) blocks of the mask are empty, full or
   partial, counted element by element from ``mask_rows``.
 * ``cost_ratio`` — eq. (5), the prefill-token reduction factor R(N).
+* ``rope`` — rotary position embedding of Q and K at given position ids, the
+  step that consumes the reused position ids of "From Generation to
+  Scoring" Section 4.1 ("Positional encoding is also adjusted accordingly",
+  "Turbocharging ...", section "SGLang changes").
 * ``setwise_layout`` — the anchor-based setwise prompt of "Scaling JEV-like
   Decision Models with SGLang" (section "Benchmark: Fused-Choice vs. Setwise
   Scoring"): query, every candidate, then one marker per candidate, as one
@@ -195,6 +199,30 @@ def causal_layout(lengths: Sequence[int]) -> Layout:
     z = np.zeros(0, np.int32)
     return Layout(cu, np.asarray(lengths, np.int32), np.zeros(len(lengths) + 1, np.int32),
                   z, z, z, pos, req_of, np.full(T, -1, np.int32))
+
+
+# ---------------------------------------------------------------------------
+# rotary position embedding at the (reused) position ids
+# ---------------------------------------------------------------------------
+
+def rope(x: np.ndarray, positions: Sequence[int], base: float = 1.0e6) -> np.ndarray:
+    """Rotate every head vector of ``x`` [T, H, D] by its row's position.
+
+    Rotate-half form: for i < D/2 the pair (x[i], x[i + D/2]) of a row at
+    position p turns by the angle p * base^(-2i/D). The pages fix the position
+    ids (Section 4.1: query 0..Lq-1, offset d of every item -> Lq + d) but not
+    the encoding; rotary embedding with the Qwen3 family's base 10^6 is the
+    reading taken for the Qwen3-shaped workloads (the base is a parameter).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    T, H, D = x.shape
+    half = D // 2
+    pos = np.asarray(positions, dtype=np.float64).reshape(T, 1, 1)
+    inv = base ** (-2.0 * np.arange(half, dtype=np.float64) / D)
+    ang = pos * inv.reshape(1, 1, half)
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
 
 
 # ---------------------------------------------------------------------------

@@ -439,3 +439,61 @@ def test_setwise_layout_rejects_bad_requests():
         O.setwise_layout([0], [0], [])                  # empty request
     with pytest.raises(ValueError):
         O.setwise_layout([3], [2], [1])                 # inconsistent counts
+
+
+# --------------------------------------------------------------------- rope ----
+
+def test_rope_closed_forms():
+    x = np.zeros((3, 1, 2))
+    x[:, 0, 0] = 1.0
+    r = O.rope(x, [0, 1, 5], base=123.0)          # D = 2: one pair, frequency base^0 = 1
+    np.testing.assert_allclose(r[:, 0, 0], np.cos([0.0, 1.0, 5.0]), atol=1e-15)
+    np.testing.assert_allclose(r[:, 0, 1], np.sin([0.0, 1.0, 5.0]), atol=1e-15)
+    y = np.random.default_rng(3).standard_normal((4, 2, 16))
+    np.testing.assert_array_equal(O.rope(y, [0, 0, 0, 0]), y)          # position 0: identity
+
+
+def test_rope_is_a_rotation_by_position():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((6, 3, 32))
+    a, b = rng.integers(0, 5000, 6), rng.integers(0, 5000, 6)
+    # composing turns adds positions; each (i, i + D/2) pair keeps its length
+    np.testing.assert_allclose(O.rope(O.rope(x, a), b), O.rope(x, a + b), atol=1e-9)
+    r = O.rope(x, a)
+    np.testing.assert_allclose(r[..., :16] ** 2 + r[..., 16:] ** 2,
+                               x[..., :16] ** 2 + x[..., 16:] ** 2, atol=1e-12)
+    # the same turn written with complex numbers: (x1 + i x2) * exp(i p f)
+    f = 1.0e6 ** (-2.0 * np.arange(16) / 32)
+    z = (x[..., :16] + 1j * x[..., 16:]) * np.exp(1j * a[:, None, None] * f)
+    np.testing.assert_allclose(r, np.concatenate([z.real, z.imag], -1), atol=1e-9)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    rng = np.random.default_rng(5)
+    q, k = rng.standard_normal((1, 1, 64)), rng.standard_normal((1, 1, 64))
+    for p, pk, shift in [(10, 3, 700), (900, 900, 12345), (5, 40, 2)]:
+        s1 = (O.rope(q, [p]) * O.rope(k, [pk])).sum()
+        s2 = (O.rope(q, [p + shift]) * O.rope(k, [pk + shift])).sum()
+        s3 = (O.rope(q, [p - pk]) * k).sum()
+        assert abs(s1 - s2) < 1e-9 and abs(s1 - s3) < 1e-9
+
+
+def test_mis_equals_sis_only_with_reused_positions():
+    # Section 4.1: the mask alone is not enough; with the reused position ids
+    # every item's rows equal those of its own [q; item] prompt
+    s = synth.custom_shapes([20], [3], [5, 7, 4])
+    lay = O.build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+    hq, hkv, D = 2, 1, 16
+    q, k, v = _qkv(lay.T, hq, hkv, D, 41)
+    o_reuse, _ = O.attention(O.rope(q, lay.position_ids), O.rope(k, lay.position_ids), v, lay)
+    packed = np.arange(lay.T)
+    o_packed, _ = O.attention(O.rope(q, packed), O.rope(k, packed), v, lay)
+    S = int(lay.prefix_len[0])
+    for i in range(lay.M):
+        rows = np.concatenate([np.arange(S), np.arange(lay.item_offsets[i], lay.item_ends[i])])
+        one = O.causal_layout([len(rows)])
+        pos = np.arange(len(rows))
+        o1, _ = O.attention(O.rope(q[rows], pos), O.rope(k[rows], pos), v[rows], one)
+        np.testing.assert_allclose(o_reuse[rows[S:]], o1[S:], rtol=0, atol=1e-12)
+        if i > 0:   # a later item at packed positions sees the query from farther away
+            assert np.abs(o_packed[rows[S:]] - o1[S:]).max() > 1e-6
