@@ -165,6 +165,7 @@ class HostLayout:
             self.item_ptr, self.item_offsets = l.item_ptr, l.item_offsets
             self.readout = l.delim_positions
         self.cu_seqlens, self.prefix_len = l.cu_seqlens, l.prefix_len
+        self.position_ids = l.position_ids
         self.T, self.M = l.T, len(self.readout)
 
     def plan_args(self):
@@ -209,10 +210,14 @@ def run_ours(args, rank, world, dist):
     out = torch.empty(M, K, dtype=torch.float32, device=dev)
     lay0 = HostLayout(w, shapes)
     plan0 = lib.Plan(*lay0.plan_args(), w.hq, w.hkv, w.head_dim)
-    # plan workspace, followed by the batch's readout rows (uploaded together)
+    # plan workspace, followed by the batch's readout rows (and, with --rope,
+    # its position ids), uploaded together
     wsz = plan0.workspace_size()
-    ws_plan = torch.zeros(wsz + 4 * M, dtype=torch.uint8, device=dev)
+    n_extra = M + (T if args.rope else 0)
+    ws_plan = torch.zeros(wsz + 4 * n_extra, dtype=torch.uint8, device=dev)
     delim_dev = ws_plan[wsz:wsz + 4 * M].view(torch.int32)
+    pos_dev = ws_plan[wsz + 4 * M:wsz + 4 * n_extra].view(torch.int32)
+    qr, kr = (torch.empty_like(q), torch.empty_like(k)) if args.rope else (q, k)
     ws_score = torch.zeros(lib.mis_label_scores_workspace_size(M, w.d_model, w.vocab, K),
                            dtype=torch.uint8, device=dev)
     flush = L2Flush(dev)
@@ -224,14 +229,20 @@ def run_ours(args, rank, world, dist):
 
     def step(times=None):
         # a1: layout (host)
-        lay = HostLayout(w, shapes)
+        lay = HostLayout(w, shapes, with_positions=args.rope)
         # a2: plan (host); one asynchronous upload of the plan and the readout rows
+        extra = np.concatenate([lay.readout, lay.position_ids]) if args.rope else lay.readout
         plan = planner.plan(*lay.plan_args(), w.hq, w.hkv, w.head_dim, ws_plan, stream=sp,
-                            extra=lay.readout)
-        # a3: MIS attention
+                            extra=extra)
         if times is not None:
             times["a0"].record(stream)
-        lib.mis_attention_fwd_plan(plan, q, k, v, o, None, sp)
+        # (with --rope) rotary embedding of Q and K at the reused position ids
+        if args.rope:
+            lib.mis_rope_qk(q, k, qr, kr, pos_dev, stream=sp)
+            if times is not None:
+                times["r1"].record(stream)
+        # a3: MIS attention
+        lib.mis_attention_fwd_plan(plan, qr, kr, v, o, None, sp)
         if times is not None:
             times["a1"].record(stream)
         # a4-a6: gather + LM head + full-vocab LSE + label read-out
@@ -255,7 +266,7 @@ def run_ours(args, rank, world, dist):
         with ClockSampler(local) as clk:
             for _ in range(args.steps):
                 flush()                              # L2 eviction between timed steps (untimed)
-                t = {"st": ev(), "a0": ev(), "a1": ev(), "s1": ev()}
+                t = {"st": ev(), "a0": ev(), "r1": ev(), "a1": ev(), "s1": ev()}
                 t["st"].record(stream)
                 step(t)
                 recs.append(t)
@@ -263,7 +274,8 @@ def run_ours(args, rank, world, dist):
         if dist is not None:
             dist.barrier()
     step_ms = [r["st"].elapsed_time(r["s1"]) for r in recs]
-    attn_ms = [r["a0"].elapsed_time(r["a1"]) for r in recs]
+    attn_ms = [r["r1" if args.rope else "a0"].elapsed_time(r["a1"]) for r in recs]
+    rope_ms = [r["a0"].elapsed_time(r["r1"]) for r in recs] if args.rope else []
     score_ms = [r["a1"].elapsed_time(r["s1"]) for r in recs]
     total_ms = float(sum(step_ms))
     total_ms = max_over_ranks(total_ms, dist, dev)
@@ -324,9 +336,18 @@ def run_ours(args, rank, world, dist):
                       "hbm_gbs_qkvo": round(attn_bytes / t_attn / 1e9, 1)},
         "scoring": {"ms": round(t_score * 1e3, 4), "w_lm_stream_gbs": round(score_gbs, 1),
                     "tflops": round(score_tflops, 1)},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (5 if args.rope else 4) * args.steps,
         "clocks": clk.summary(),
     }
+    if args.rope:
+        t_rope = statistics.mean(rope_ms) / 1e3
+        rope_bytes = T * (w.hq + w.hkv) * w.head_dim * 2 * 2 + T * 4
+        result["rope"] = {"ms": round(t_rope * 1e3, 4), "bytes": rope_bytes,
+                          "hbm_gbs": round(rope_bytes / t_rope / 1e9, 1),
+                          "frac_of_hbm_peak": round(rope_bytes / t_rope / 1e9 / peaks["hbm_gbs"], 4),
+                          "note": "rotary embedding of Q and K at the reused position ids, "
+                                  "inside the timed step before the attention"}
+        result["config"]["rope"] = "base 1e6, rotate-half, reused position ids"
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, w, shapes, vals, labels, dev, stream, dist, world)
     if not args.no_comparators:
@@ -705,6 +726,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="request-size sweep N = 1..200 (prints its own JSON table)")
     ap.add_argument("--sweep-members", type=int, default=16)
+    ap.add_argument("--rope", action="store_true",
+                    help="rotate Q and K at the reused position ids inside the timed step")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -712,6 +735,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.rope:
+        args.no_e2e = True        # the end-to-end leg times the default path only
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     dist = None

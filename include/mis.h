@@ -233,6 +233,30 @@ mis_status_t mis_attention_fwd(const void* q, const void* k, const void* v, void
                                size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Rotary position embedding of Q and K at the reused position ids of "From
+ * Generation to Scoring" Section 4.1 (query 0..S-1, offset d of every item
+ * set -> S + d, as mis_build_layout emits them), so that every item is
+ * rotated exactly as in its own single-item prompt ("Turbocharging ...",
+ * section "SGLang changes": positional encoding adjusted so each item aligns
+ * with its single-item position). The step before mis_attention_fwd*.
+ * Rotate-half form: for i < D/2 the pair (x[i], x[i + D/2]) of a row at
+ * position p turns by p * base^(-2i/D) (base > 1; 1e6 for the Qwen3 family).
+ *   q, k          — device bf16 [T, Hq, D] and [T, Hkv, D], row strides in
+ *                   elements (>= H*D, multiples of 8), 16-byte aligned
+ *   q_out, k_out  — device bf16 outputs in the same shapes; q_out == q and
+ *                   k_out == k (same strides) rotate in place; other overlaps
+ *                   are not allowed
+ *   position_ids  — device int32 [T]
+ * fp32 arithmetic (angles from inverse frequencies computed in fp64 on the
+ * host), bf16 results rounded to nearest even. One kernel launch, stream
+ * ordered; T = 0 enqueues nothing.
+ * ------------------------------------------------------------------------ */
+mis_status_t mis_rope_qk(const void* q, const void* k, void* q_out, void* k_out,
+                         int64_t q_row_stride, int64_t k_row_stride, int64_t q_out_row_stride,
+                         int64_t k_out_row_stride, int32_t T, int32_t Hq, int32_t Hkv, int32_t D,
+                         const int32_t* position_ids, double base, void* stream);
+
+/* ------------------------------------------------------------------------
  * Label scoring at the readout rows ("From Generation to Scoring", Section
  * 3.3 and eq. 2; "Turbocharging ...", section "SGLang changes": an N x K
  * matrix of label log-probs; "Scaling JEV-like Decision Models with SGLang",

@@ -17,7 +17,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmis_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-CU_SOURCES = ["mis_attn.cu", "mis_score.cu"]
+CU_SOURCES = ["mis_attn.cu", "mis_score.cu", "mis_rope.cu"]
 CPP_SOURCES = ["mis_plan.cpp", "mis_abi.cpp"]
 
 

@@ -34,7 +34,8 @@ EXPORTS = ["mis_status_string", "mis_abi_version", "mis_layout_size", "mis_build
            "mis_attention_fwd", "mis_label_scores_workspace_size", "mis_label_scores",
            "mis_get_device_status", "mis_set_wait_limit_ns", "mis_label_scores_noalloc",
            "mis_inject_stall", "mis_planner_create", "mis_planner_plan", "mis_planner_destroy",
-           "mis_set_schedule", "mis_setwise_layout_size", "mis_build_setwise_layout"]
+           "mis_set_schedule", "mis_setwise_layout_size", "mis_build_setwise_layout",
+           "mis_rope_qk"]
 
 
 class MisError(RuntimeError):
@@ -95,6 +96,8 @@ def load(path: str = LIB_PATH):
         "mis_set_wait_limit_ns": (C.c_uint64, [C.c_uint64]),
         "mis_inject_stall": (C.c_uint32, [C.c_uint32]),
         "mis_set_schedule": (C.c_int32, [C.c_int32]),
+        "mis_rope_qk": (C.c_int, [vp, vp, vp, vp, i64, i64, i64, i64, C.c_int32, C.c_int32,
+                                  C.c_int32, C.c_int32, vp, C.c_double, vp]),
         "mis_setwise_layout_size": (C.c_int, [C.c_int32, i32p, i32p, i32p, C.POINTER(i64),
                                               C.POINTER(i64)]),
         "mis_build_setwise_layout": (C.c_int, [C.c_int32, i32p, i32p, i32p, i32p, i32p, i32p,
@@ -379,6 +382,17 @@ def mis_attention_fwd(q, k, v, o, lse, cu_seqlens, prefix_len, item_ptr, item_of
 
 
 # ------------------------------------------------------------------- scoring
+
+def mis_rope_qk(q, k, q_out, k_out, position_ids, base: float = 1.0e6, stream=None):
+    """Rotary embedding of q [T, Hq, D] and k [T, Hkv, D] (bf16 device tensors
+    with unit stride inside a row) at device int32 position ids [T]."""
+    L = load()
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    _check(L.mis_rope_qk(_dptr(q), _dptr(k), _dptr(q_out), _dptr(k_out), q.stride(0), k.stride(0),
+                         q_out.stride(0), k_out.stride(0), T, Hq, Hkv, D, _dptr(position_ids),
+                         float(base), _stream(stream)), "mis_rope_qk")
+
 
 def mis_label_scores_workspace_size(M: int, d: int, V: int, K: int) -> int:
     return int(load().mis_label_scores_workspace_size(M, d, V, K))

@@ -212,3 +212,23 @@ def test_setwise_layout_bit_exact(L):
     with pytest.raises(lib.MisError) as e:
         lib.mis_build_setwise_layout([3], [1], [-2])
     assert e.value.status == lib.MIS_ERR_INVALID_ARG
+
+
+def test_rope_argument_checks(L):
+    # all rejected (or, for T = 0, accepted) before anything is enqueued
+    fake = C.c_void_p(1 << 20)          # 16-byte aligned, never dereferenced
+    ok_args = dict(qs=16 * 128, ks=8 * 128, T=4, Hq=16, Hkv=8, D=128, base=1e6)
+
+    def call(q=fake, k=fake, qo=fake, ko=fake, pos=fake, **kw):
+        a = dict(ok_args, **kw)
+        return L.mis_rope_qk(q, k, qo, ko, a["qs"], a["ks"], a["qs"], a["ks"], a["T"], a["Hq"],
+                             a["Hkv"], a["D"], pos, a["base"], None)
+    assert call(T=0) == lib.MIS_OK
+    assert call(D=96) == lib.MIS_ERR_UNSUPPORTED
+    assert call(base=1.0) == lib.MIS_ERR_INVALID_ARG
+    assert call(base=float("inf")) == lib.MIS_ERR_INVALID_ARG
+    assert call(pos=None) == lib.MIS_ERR_INVALID_ARG
+    assert call(q=C.c_void_p((1 << 20) + 8)) == lib.MIS_ERR_INVALID_ARG      # misaligned
+    assert call(qs=16 * 128 - 8) == lib.MIS_ERR_SHAPE                         # row too short
+    assert call(ks=8 * 128 + 4) == lib.MIS_ERR_SHAPE                          # stride not 8-multiple
+    assert call(Hq=0) == lib.MIS_ERR_INVALID_ARG

@@ -1,0 +1,114 @@
+"""GPU parity of mis_rope_qk against the fp64 oracle, and of rotary
+attention at the reused position ids ("From Generation to Scoring", Section
+4.1: with the mask and the reused position ids every item's rows equal those
+of its own single-item prompt)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from ranking_prefill_gb300 import lib, synth
+from gpu_helpers import ATTN_TOL, SCORE_TOL, f64
+
+pytestmark = pytest.mark.gpu
+
+ROPE_TOL = 8e-3    # max |gpu - oracle| / max(|oracle|, 1): bf16 rounding (2^-9) + fp32 angle rounding
+
+
+def _rope_err(got, ref):
+    return float((np.abs(f64(got) - ref) / np.maximum(np.abs(ref), 1.0)).max())
+
+
+@pytest.mark.parametrize("hq,hkv,D,base,maxpos,pad", [(16, 8, 128, 1e6, 5000, 0),
+                                                       (4, 4, 64, 1e4, 20000, 8),
+                                                       (32, 8, 128, 5e5, 300, 16)])
+def test_rope_matches_oracle(hq, hkv, D, base, maxpos, pad):
+    T = 1500
+    rng = np.random.default_rng(D + hq)
+    pos = rng.integers(0, maxpos, T).astype(np.int32)
+    v = synth.draw_values(int(hq + D), T, hq, hkv, D, want=("q", "k"))
+    dev = torch.device("cuda")
+
+    def place(t, h):
+        buf = torch.zeros(T, h * D + pad, dtype=torch.bfloat16, device=dev)
+        view = buf.as_strided((T, h, D), (h * D + pad, D, 1))
+        view.copy_(t.to(dev))
+        return view
+    q, k = place(v["q"], hq), place(v["k"], hkv)
+    qo, ko = place(torch.zeros_like(v["q"]), hq), place(torch.zeros_like(v["k"]), hkv)
+    pd = torch.as_tensor(pos, device=dev)
+    lib.mis_rope_qk(q, k, qo, ko, pd, base)
+    torch.cuda.synchronize()
+    assert _rope_err(qo, O.rope(f64(v["q"]), pos, base)) <= ROPE_TOL
+    assert _rope_err(ko, O.rope(f64(v["k"]), pos, base)) <= ROPE_TOL
+    assert bool((q.float() == v["q"].to(dev).float()).all())          # inputs untouched
+    # in place gives the same bits as out of place
+    lib.mis_rope_qk(q, k, q, k, pd, base)
+    torch.cuda.synchronize()
+    assert bool((q.float() == qo.float()).all()) and bool((k.float() == ko.float()).all())
+
+
+def test_rotary_mis_attention_matches_oracle():
+    s = synth.custom_shapes([300, 40], [6, 3], [12, 0, 40, 7, 130, 2, 25, 1, 60])
+    lay = lib.mis_build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+    hq, hkv, D = 8, 2, 128
+    v = synth.draw_values(51, lay.T, hq, hkv, D, want=("q", "k", "v"))
+    dev = torch.device("cuda")
+    q, k, vv = (v[x].to(dev) for x in ("q", "k", "v"))
+    qr, kr = torch.empty_like(q), torch.empty_like(k)
+    lib.mis_rope_qk(q, k, qr, kr, torch.as_tensor(lay.position_ids, device=dev))
+    o = torch.empty_like(q)
+    plan = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, hq, hkv, D)
+    ws = torch.zeros(plan.workspace_size(), dtype=torch.uint8, device=dev)
+    plan.create(ws)
+    lib.mis_attention_fwd_plan(plan, qr, kr, vv, o, None)
+    torch.cuda.synchronize()
+    assert lib.mis_get_device_status(ws) == lib.MIS_OK
+    olay = O.build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+    ro, _ = O.attention(O.rope(f64(v["q"]), olay.position_ids), O.rope(f64(v["k"]), olay.position_ids),
+                        f64(v["v"]), olay)
+    assert np.abs(f64(o) - ro).max() <= ATTN_TOL
+
+
+def test_rotary_mis_equals_single_item_prompts_on_gpu():
+    # one query, 40 items: MIS with reused positions against 40 separate
+    # [q; item] prompts at their own positions, through rope -> attention ->
+    # scoring (the attention output as hidden state)
+    pool = synth.sweep_pool(1, vocab=3000, seed=21)
+    pool.query_tokens[0] = 700
+    pool.cand_lens = pool.cand_lens[:, :40].copy()
+    P, lens = int(pool.query_tokens[0]), pool.cand_lens[0]
+    hq, hkv, D = 8, 4, 128
+    dev = torch.device("cuda")
+    mis = lib.mis_build_layout([P], [40], lens)
+    olay = O.build_layout([P], [40], lens)
+    v = synth.draw_values(52, mis.T, hq, hkv, D, want=("q", "k", "v"))
+    S = P + 1
+    rows = np.concatenate([np.concatenate([np.arange(S), np.arange(olay.item_offsets[i], olay.item_ends[i])])
+                           for i in range(40)])
+    sis = lib.mis_build_layout([P] * 40, [1] * 40, lens)
+    g = torch.Generator().manual_seed(53)
+    w_lm = (torch.randn(3000, hq * D, generator=g) * 0.02).to(torch.bfloat16).to(dev)
+    labels = [int(x) for x in pool.labels]
+
+    def run(lay, idx):
+        t = torch.as_tensor(idx, dtype=torch.long)
+        q, k, vv = (v[x][t].to(dev) for x in ("q", "k", "v"))
+        lib.mis_rope_qk(q, k, q, k, torch.as_tensor(lay.position_ids, device=dev))
+        o = torch.empty_like(q)
+        plan = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, hq, hkv, D)
+        ws = torch.zeros(plan.workspace_size(), dtype=torch.uint8, device=dev)
+        plan.create(ws)
+        lib.mis_attention_fwd_plan(plan, q, k, vv, o, None)
+        out = torch.empty(lay.M, 2, dtype=torch.float32, device=dev)
+        sws = torch.zeros(lib.mis_label_scores_workspace_size(lay.M, hq * D, 3000, 2),
+                          dtype=torch.uint8, device=dev)
+        rd = torch.as_tensor(lay.delim_positions, device=dev)
+        lib.mis_label_scores(o.view(lay.T, hq * D), w_lm, rd, labels, out, None, sws)
+        torch.cuda.synchronize()
+        assert lib.mis_get_device_status(ws) == lib.MIS_OK
+        return o[rd.long()].float(), out
+    om, sm = run(mis, np.arange(mis.T))
+    os_, ss = run(sis, rows)
+    assert (om - os_).abs().max().item() <= 1e-2
+    assert (sm - ss).abs().max().item() <= SCORE_TOL
