@@ -33,6 +33,11 @@ What it computes, and where each step comes from:
   step that consumes the reused position ids of "From Generation to
   Scoring" Section 4.1 ("Positional encoding is also adjusted accordingly",
   "Turbocharging ...", section "SGLang changes").
+* ``cached_layout`` / ``attention_cached`` — items scored over a prefix whose
+  K/V was computed earlier and kept in a cache (the "in-batch prefix cache"
+  and the "knock-knock" second request of "Turbocharging LinkedIn's
+  recommendation systems with SGLang"): each item row sees its request's
+  cached prefix and its own item causally, as in eq. (4).
 * ``setwise_layout`` — the anchor-based setwise prompt of "Scaling JEV-like
   Decision Models with SGLang" (section "Benchmark: Fused-Choice vs. Setwise
   Scoring"): query, every candidate, then one marker per candidate, as one
@@ -146,6 +151,104 @@ class SetwiseLayout:
     @property
     def M(self) -> int:
         return len(self.marker_positions)
+
+
+@dataclass
+class CachedLayout:
+    """Item requests over cached prefix K/V (all int32).
+
+    The new sequence holds only item sets (item tokens + trailing DELIM);
+    request b's prefix (its |Q| = S_b rows: prefix tokens and the leading
+    DELIM) sits in the cache at rows [cache_start[b], cache_start[b] + S_b).
+    """
+
+    cu_seqlens: np.ndarray       # [B+1] rows of the new sequence per request
+    item_ptr: np.ndarray         # [B+1]
+    item_offsets: np.ndarray     # [M] first new-sequence row of each item set
+    item_ends: np.ndarray        # [M]
+    delim_positions: np.ndarray  # [M] readout rows (new sequence)
+    position_ids: np.ndarray     # [T] reused positions S_b + d
+    cache_start: np.ndarray      # [B]
+    cache_len: np.ndarray        # [B] S_b
+    request_of: np.ndarray       # [T]
+    item_of: np.ndarray          # [T]
+
+    @property
+    def T(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def B(self) -> int:
+        return len(self.cache_len)
+
+    @property
+    def M(self) -> int:
+        return len(self.item_offsets)
+
+
+def cached_layout(cache_start: Sequence[int], cache_len: Sequence[int],
+                  n_items: Sequence[int], item_lens: Sequence[int]) -> CachedLayout:
+    """Pack the item sets of each request, token by token, after a cached prefix."""
+    cache_start = [int(x) for x in cache_start]
+    cache_len = [int(x) for x in cache_len]
+    n_items = [int(x) for x in n_items]
+    item_lens = [int(x) for x in item_lens]
+    if not (len(cache_start) == len(cache_len) == len(n_items)) or sum(n_items) != len(item_lens):
+        raise ValueError("inconsistent request description")
+    cu, iptr, offs, ends, delims, pos, req_of, item_of = [0], [0], [], [], [], [], [], []
+    t = it = 0
+    for b, (S, n) in enumerate(zip(cache_len, n_items)):
+        if S < 1 or n < 1 or cache_start[b] < 0:
+            raise ValueError("each request needs a cached prefix and at least one item")
+        for _ in range(n):
+            offs.append(t)
+            for d in range(item_lens[it] + 1):     # item tokens then its trailing DELIM
+                pos.append(S + d)
+                req_of.append(b)
+                item_of.append(it)
+                t += 1
+            ends.append(t)
+            delims.append(t - 1)
+            it += 1
+        cu.append(t)
+        iptr.append(it)
+    i32 = lambda a: np.asarray(a, dtype=np.int32)
+    return CachedLayout(i32(cu), i32(iptr), i32(offs), i32(ends), i32(delims), i32(pos),
+                        i32(cache_start), i32(cache_len), i32(req_of), i32(item_of))
+
+
+def attention_cached(q: np.ndarray, k: np.ndarray, v: np.ndarray, k_cache: np.ndarray,
+                     v_cache: np.ndarray, lay: CachedLayout, scale: Optional[float] = None,
+                     rows: Optional[Iterable[int]] = None):
+    """Softmax attention of new-sequence rows over [cached prefix ; own item].
+
+    Row j of item i of request b sees every cached key of b (the prefix
+    precedes all item tokens, so eq. (4)'s k <= j holds) and the keys of item i
+    up to j. Naive fp64, the cached keys first, then the item keys in order.
+    Returns (O [R, Hq, D], LSE [R, Hq]).
+    """
+    T, Hq, D = q.shape
+    group = Hq // k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rows = np.arange(T) if rows is None else np.asarray(list(rows), dtype=np.int64)
+    out = np.zeros((len(rows), Hq, D), dtype=np.float64)
+    lse = np.zeros((len(rows), Hq), dtype=np.float64)
+    for n, j in enumerate(rows):
+        b, i = int(lay.request_of[j]), int(lay.item_of[j])
+        c0, S = int(lay.cache_start[b]), int(lay.cache_len[b])
+        keys = np.concatenate([np.asarray(k_cache[c0:c0 + S], np.float64),
+                               np.asarray(k[lay.item_offsets[i]:j + 1], np.float64)])
+        vals = np.concatenate([np.asarray(v_cache[c0:c0 + S], np.float64),
+                               np.asarray(v[lay.item_offsets[i]:j + 1], np.float64)])
+        qj = np.asarray(q[j], np.float64)
+        for h in range(Hq):
+            sc = scale * (keys[:, h // group, :] @ qj[h])
+            m = sc.max()
+            p = np.exp(sc - m)
+            out[n, h] = (p @ vals[:, h // group, :]) / p.sum()
+            lse[n, h] = m + np.log(p.sum())
+    return out, lse
 
 
 def setwise_layout(query_tokens: Sequence[int], n_cands: Sequence[int],

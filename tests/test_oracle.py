@@ -497,3 +497,67 @@ def test_mis_equals_sis_only_with_reused_positions():
         np.testing.assert_allclose(o_reuse[rows[S:]], o1[S:], rtol=0, atol=1e-12)
         if i > 0:   # a later item at packed positions sees the query from farther away
             assert np.abs(o_packed[rows[S:]] - o1[S:]).max() > 1e-6
+
+
+# --------------------------------------------------------- cached prefix ----
+
+def _cached_case(seed):
+    rng = np.random.default_rng(seed)
+    B = 3
+    P = rng.integers(1, 60, B)                   # prefix tokens (without DELIM)
+    n = rng.integers(1, 5, B)
+    lens = rng.integers(0, 9, int(n.sum()))
+    S = P + 1
+    # prefixes stored back to back in the cache, in reverse order, with a gap
+    cstart = np.zeros(B, np.int64)
+    t = 3
+    for b in reversed(range(B)):
+        cstart[b] = t
+        t += S[b] + 2
+    return P, n, lens, S, cstart, t
+
+
+def test_cached_prefix_attention_equals_packed_mis():
+    # the same prefixes and items packed as MIS requests: identical item rows
+    P, n, lens, S, cstart, cache_T = _cached_case(61)
+    hq, hkv, D = 4, 2, 16
+    packed = O.build_layout(P, n, lens)
+    q, k, v = _qkv(packed.T, hq, hkv, D, 62)
+    cl = O.cached_layout(cstart, S, n, lens)
+    kc = np.zeros((cache_T, hkv, D)); vc = np.zeros((cache_T, hkv, D))
+    item_rows = []
+    for b in range(packed.B):
+        s0 = packed.cu_seqlens[b]
+        kc[cstart[b]:cstart[b] + S[b]] = k[s0:s0 + S[b]]
+        vc[cstart[b]:cstart[b] + S[b]] = v[s0:s0 + S[b]]
+        item_rows.append(np.arange(s0 + S[b], packed.cu_seqlens[b + 1]))
+    item_rows = np.concatenate(item_rows)
+    assert len(item_rows) == cl.T
+    ref, ref_lse = O.attention(q, k, v, packed, rows=item_rows)
+    got, got_lse = O.attention_cached(q[item_rows], k[item_rows], v[item_rows], kc, vc, cl)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(got_lse, ref_lse, rtol=0, atol=1e-12)
+    assert np.array_equal(cl.position_ids, packed.position_ids[item_rows])
+    assert np.array_equal(item_rows[cl.delim_positions], packed.delim_positions)
+
+
+def test_single_item_requests_over_one_cached_prefix_equal_mis():
+    # "single-item scoring with prefix caching": every item its own request
+    # over the same cached prefix gives the MIS item rows again
+    S, lens = 30, [4, 0, 7]
+    hq, hkv, D = 2, 1, 8
+    cl = O.cached_layout([0], [S], [3], lens)
+    one = O.cached_layout([0, 0, 0], [S, S, S], [1, 1, 1], lens)
+    q, k, v = _qkv(cl.T, hq, hkv, D, 63)
+    kc, vc, _ = _qkv(S, hq, hkv, D, 64)
+    kc, vc = kc[:, :hkv], vc[:, :hkv]
+    a, _ = O.attention_cached(q, k, v, kc, vc, cl)
+    b, _ = O.attention_cached(q, k, v, kc, vc, one)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_cached_layout_rejects_bad_requests():
+    with pytest.raises(ValueError):
+        O.cached_layout([0], [0], [1], [3])        # no cached prefix
+    with pytest.raises(ValueError):
+        O.cached_layout([0], [4], [0], [])         # no item
