@@ -233,6 +233,62 @@ mis_status_t mis_attention_fwd(const void* q, const void* k, const void* v, void
                                size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Items over a cached prefix: the prefix K/V of each request was computed
+ * earlier and kept in a cache buffer ("Turbocharging LinkedIn's
+ * recommendation systems with SGLang": the in-batch prefix cache, which
+ * reuses query-prefix KV within one forward pass, and the "knock-knock"
+ * second request, which appends the items to a prefix prefilled while
+ * retrieval ran). The new sequence holds only item sets; each item row sees
+ * its request's cached prefix (all of it: the prefix precedes every item
+ * token) and its own item causally, as eq. (4) of "From Generation to
+ * Scoring" gives for item rows. Single-item scoring with prefix caching is
+ * the same call with one item per request, all requests pointing at one
+ * cache range.
+ *   B, T, Hq, Hkv, D, scale — as in mis_attn_desc (T = rows of the new sequence)
+ *   cu_seqlens   — [B+1] new-sequence rows of each request (items only)
+ *   item_ptr     — [B+1] CSR into item_offsets; every request has >= 1 item
+ *   item_offsets — new-sequence first row of each item set (the first of a
+ *                  request equals cu_seqlens[b]); each set ends where the next
+ *                  starts or at cu_seqlens[b+1]
+ *   cache_start  — [B] first cache row of request b's prefix (its |Q| rows:
+ *                  prefix tokens and the leading DELIM)
+ *   cache_len    — [B] S_b >= 1; cache_start[b] + S_b <= cache_T
+ *   cache_T      — rows of the cache K/V buffers
+ * Plans are made with mis_cached_plan_create (same workspace rules as
+ * mis_plan_create) and run with mis_attention_fwd_cached; mis_plan_get_stats
+ * and mis_plan_destroy apply. Key tiles of mis_plan_tile_map: indices below
+ * ceil(S_b/128) are the cache tiles of the request, the rest the new
+ * sequence's 128-row tiles counted from the request's first new row.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t B, T, Hq, Hkv, D;
+  float scale;
+  const int32_t* cu_seqlens;
+  const int32_t* item_ptr;
+  const int32_t* item_offsets;
+  const int32_t* cache_start;
+  const int32_t* cache_len;
+  int32_t cache_T;
+} mis_cached_desc;
+
+size_t mis_cached_plan_workspace_size(const mis_cached_desc* desc);
+mis_status_t mis_cached_plan_create(const mis_cached_desc* desc, void* workspace, size_t ws_bytes,
+                                    void* stream, mis_plan_t* out);
+
+/* Attention of the new rows over [cached prefix ; own item]. q, k, v, o as
+ * in mis_attention_fwd_plan for the T new rows; k_cache / v_cache device
+ * bf16 [cache_T, Hkv, D] with row strides kc_row_stride / vc_row_stride (the
+ * same rules). lse (optional) is [Hq, T] over the new rows. A plan of the
+ * other kind returns MIS_ERR_INVALID_ARG (and mis_attention_fwd_plan refuses
+ * cached plans the same way). */
+mis_status_t mis_attention_fwd_cached(mis_plan_t plan, const void* q, const void* k,
+                                      const void* v, const void* k_cache, const void* v_cache,
+                                      void* o, float* lse, int64_t q_row_stride,
+                                      int64_t k_row_stride, int64_t v_row_stride,
+                                      int64_t kc_row_stride, int64_t vc_row_stride,
+                                      int64_t o_row_stride, void* stream);
+
+/* ------------------------------------------------------------------------
  * Rotary position embedding of Q and K at the reused position ids of "From
  * Generation to Scoring" Section 4.1 (query 0..S-1, offset d of every item
  * set -> S + d, as mis_build_layout emits them), so that every item is

@@ -251,6 +251,38 @@ def attention_cached(q: np.ndarray, k: np.ndarray, v: np.ndarray, k_cache: np.nd
     return out, lse
 
 
+def tile_map_cached(lay: CachedLayout, BM: int, BN: int) -> np.ndarray:
+    """Non-empty (request, q-tile, k-tile, FULL/PARTIAL) blocks of cached-prefix requests.
+
+    Query tiles cover each request's new rows from its first one. Key tiles
+    0 .. ceil(S/BN)-1 cover its cached prefix [cache_start, cache_start + S)
+    from its first row, and the next ones its new rows from the first one;
+    a tile is clipped at the end of its range. Visibility by enumeration:
+    every cached key of the request, and keys of the row's own item up to
+    the row.
+    """
+    out = []
+    for b in range(lay.B):
+        s0, e0 = int(lay.cu_seqlens[b]), int(lay.cu_seqlens[b + 1])
+        S = int(lay.cache_len[b])
+        nc = (S + BN - 1) // BN
+        rows = np.arange(s0, e0)
+        item = lay.item_of[s0:e0]
+        for t in range(0, (e0 - s0 + BM - 1) // BM):
+            r = rows[t * BM:(t + 1) * BM]
+            it = item[t * BM:(t + 1) * BM]
+            for u in range(nc):                       # cached keys: visible from every row
+                n = min(BN, S - u * BN)
+                out.append((b, t, u, FULL if n > 0 else EMPTY))
+            for u in range(0, (e0 - s0 + BN - 1) // BN):
+                kk = np.arange(s0 + u * BN, min(s0 + (u + 1) * BN, e0))
+                vis = (item[kk - s0][None, :] == it[:, None]) & (kk[None, :] <= r[:, None])
+                if vis.any():
+                    out.append((b, t, nc + u, FULL if vis.all() else PARTIAL))
+    out = [x for x in out if x[3] != EMPTY]
+    return np.asarray(out, dtype=np.int32).reshape(-1, 4)
+
+
 def setwise_layout(query_tokens: Sequence[int], n_cands: Sequence[int],
                    cand_lens: Sequence[int]) -> SetwiseLayout:
     """Setwise (anchor-based) prompts, token by token.

@@ -177,14 +177,21 @@ size_t mis_plan_workspace_size(const mis_attn_desc* desc) {
   }
 }
 
-mis_status_t mis_plan_create(const mis_attn_desc* desc, void* workspace, size_t ws_bytes,
-                             void* stream, mis_plan_t* out) {
+}  // extern "C"
+
+namespace {
+
+// Build a plan with `build` and upload it into `workspace` (or keep it
+// host-only when workspace is NULL and ws_bytes is 0).
+template <typename Desc, typename Build>
+mis_status_t create_plan(const Desc* desc, Build build, void* workspace, size_t ws_bytes,
+                         void* stream, mis_plan_t* out) {
   if (!out) return MIS_ERR_INVALID_ARG;
   *out = nullptr;
   mis_plan_s* h = nullptr;
   try {
     h = new mis_plan_s();
-    mis_status_t st = build_plan(desc, &h->p);
+    mis_status_t st = build(desc, &h->p);
     if (st != MIS_OK) { delete h; return st; }
     HostPlan& p = h->p;
     if (!workspace && ws_bytes == 0) {   // host-only plan: inspection, no launches
@@ -218,6 +225,30 @@ mis_status_t mis_plan_create(const mis_attn_desc* desc, void* workspace, size_t 
     delete h;
     return MIS_ERR_INVALID_ARG;
   }
+}
+
+}  // namespace
+
+extern "C" {
+
+mis_status_t mis_plan_create(const mis_attn_desc* desc, void* workspace, size_t ws_bytes,
+                             void* stream, mis_plan_t* out) {
+  return create_plan(desc, build_plan, workspace, ws_bytes, stream, out);
+}
+
+size_t mis_cached_plan_workspace_size(const mis_cached_desc* desc) {
+  try {
+    HostPlan p;
+    if (build_plan_cached(desc, &p) != MIS_OK) return 0;
+    return p.total;
+  } catch (...) {
+    return 0;
+  }
+}
+
+mis_status_t mis_cached_plan_create(const mis_cached_desc* desc, void* workspace, size_t ws_bytes,
+                                    void* stream, mis_plan_t* out) {
+  return create_plan(desc, build_plan_cached, workspace, ws_bytes, stream, out);
 }
 
 }  // extern "C"
@@ -349,6 +380,7 @@ mis_status_t mis_attention_fwd_plan(mis_plan_t plan, const void* q, const void* 
                                     int64_t os, void* stream) {
   if (!plan) return MIS_ERR_INVALID_ARG;
   HostPlan& p = plan->p;
+  if (p.cached) return MIS_ERR_INVALID_ARG;       // needs the cache buffers
   if (!p.workspace) return MIS_ERR_WORKSPACE;
   if (!q || !k || !v || !o) return MIS_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return MIS_ERR_INVALID_ARG;
@@ -357,7 +389,30 @@ mis_status_t mis_attention_fwd_plan(mis_plan_t plan, const void* q, const void* 
   if (qs < wq || os < wq || ks < wk || vs < wk) return MIS_ERR_SHAPE;
   if ((qs | ks | vs | os) & 7) return MIS_ERR_SHAPE;
   try {
-    return launch_attention(p, q, k, v, o, lse, qs, ks, vs, os, stream);
+    return launch_attention(p, q, k, v, nullptr, nullptr, o, lse, qs, ks, vs, 0, 0, os, stream);
+  } catch (...) {
+    return MIS_ERR_CUDA;
+  }
+}
+
+mis_status_t mis_attention_fwd_cached(mis_plan_t plan, const void* q, const void* k,
+                                      const void* v, const void* k_cache, const void* v_cache,
+                                      void* o, float* lse, int64_t qs, int64_t ks, int64_t vs,
+                                      int64_t kcs, int64_t vcs, int64_t os, void* stream) {
+  if (!plan) return MIS_ERR_INVALID_ARG;
+  HostPlan& p = plan->p;
+  if (!p.cached) return MIS_ERR_INVALID_ARG;
+  if (!p.workspace) return MIS_ERR_WORKSPACE;
+  if (!q || !k || !v || !o || !k_cache || !v_cache) return MIS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(k_cache) ||
+      !aligned16(v_cache))
+    return MIS_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return MIS_ERR_INVALID_ARG;
+  const int64_t wq = (int64_t)p.Hq * p.D, wk = (int64_t)p.Hkv * p.D;
+  if (qs < wq || os < wq || ks < wk || vs < wk || kcs < wk || vcs < wk) return MIS_ERR_SHAPE;
+  if ((qs | ks | vs | kcs | vcs | os) & 7) return MIS_ERR_SHAPE;
+  try {
+    return launch_attention(p, q, k, v, k_cache, v_cache, o, lse, qs, ks, vs, kcs, vcs, os, stream);
   } catch (...) {
     return MIS_ERR_CUDA;
   }

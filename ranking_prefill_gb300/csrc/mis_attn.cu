@@ -89,6 +89,7 @@ struct AttnParams {
   float* lse;
   int64_t o_stride;
   int32_t T;
+  int32_t qbase;          // virtual row of new row 0 (0 unless the plan reads a prefix cache)
   int32_t group;          // Hq / Hkv
   int32_t n_head_groups;  // units per query tile: Hq / 2 (pair) or Hq (split)
   float scale_log2;       // softmax scale * log2(e)
@@ -111,7 +112,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap,
-                    const __grid_constant__ CUtensorMap omap, const AttnParams p) {
+                    const __grid_constant__ CUtensorMap omap,
+                    const __grid_constant__ CUtensorMap kcmap,
+                    const __grid_constant__ CUtensorMap vcmap, const AttnParams p) {
   using C = AttnCfg<D>;
   constexpr int KS = C::kKStages, VS = C::kVStages;
   constexpr int NB = D / 64;                          // 64-column boxes per row
@@ -165,6 +168,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&qmap); tma_prefetch_desc(&kmap); tma_prefetch_desc(&vmap);
     tma_prefetch_desc(&omap);
+    if (p.qbase) { tma_prefetch_desc(&kcmap); tma_prefetch_desc(&vcmap); }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -198,21 +202,26 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
         for (int t = 0; t < nh; ++t)
           for (int b = 0; b < NB; ++b)
             tma_load_3d(smem_u32(sQ + t * C::kTile + b * C::kBox), &qmap, bar(bQF), b * 64, h0 + t,
-                        un.q0);
+                        un.q0 - p.qbase);
         q_issued = lu + 1;
         for (int it = 0; it < un.nk; ++it) {
           const int gi = gk + it;
           const int32_t c0 = (int32_t)(p.klist[un.kofs + it] & ~kNeedMask);
+          // key rows below qbase are cache rows (cached-prefix plans only)
+          const bool from_cache = c0 < p.qbase;
+          const CUtensorMap* km = from_cache ? &kcmap : &kmap;
+          const CUtensorMap* vm = from_cache ? &vcmap : &vmap;
+          const int32_t kr = from_cache ? c0 : c0 - p.qbase;
           const int sk = gi % KS, sv = gi % VS;
           if (gi >= KS && !(ok = wait(bar(bKE + sk), ((gi / KS) - 1) & 1, W, 0x100))) break;
           mbar_arrive_expect_tx(bar(bKF + sk), C::kTile);
           for (int b = 0; b < NB; ++b)
-            tma_load_3d(smem_u32(sK + sk * C::kTile + b * C::kBox), &kmap, bar(bKF + sk), b * 64, g, c0);
+            tma_load_3d(smem_u32(sK + sk * C::kTile + b * C::kBox), km, bar(bKF + sk), b * 64, g, kr);
           k_issued = gi + 1;
           if (gi >= VS && !(ok = wait(bar(bVE + sv), ((gi / VS) - 1) & 1, W, 0x180))) break;
           mbar_arrive_expect_tx(bar(bVF + sv), C::kTile);
           for (int b = 0; b < NB; ++b)
-            tma_load_3d(smem_u32(sV + sv * C::kTile + b * C::kBox), &vmap, bar(bVF + sv), b * 64, g, c0);
+            tma_load_3d(smem_u32(sV + sv * C::kTile + b * C::kBox), vm, bar(bVF + sv), b * 64, g, kr);
           v_issued = gi + 1;
         }
         gk += un.nk;
@@ -353,7 +362,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
       const int j = un.q0 + r;
       const bool valid = j < R.e0;
       const int jj = valid ? j : -1;                    // invalid rows see nothing
-      const int lo = valid ? p.seg_start[j] : 0x7fffffff;
+      const int lo = valid ? p.seg_start[j - p.qbase] : 0x7fffffff;
       const int nk = un.nk;
       // key tiles of this stream: all (pair) or t, t+2, ... (split)
       const int kstep = split ? 2 : 1, kfirst = split ? t : 0;
@@ -449,7 +458,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      __nv_bfloat16* orow = p.o + (int64_t)(valid ? j : 0) * p.o_stride + (int64_t)h * D;
+      __nv_bfloat16* orow = p.o + (int64_t)(valid ? j - p.qbase : 0) * p.o_stride + (int64_t)h * D;
       // O leaves through a 32-row x 64-column staging buffer per warp and a
       // TMA tensor store (asynchronous, whole rows); a warp whose 32 rows run
       // past the request's end stores its valid rows directly instead, since
@@ -469,7 +478,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) {
-            tma_store_3d(&omap, sOw, col0, h, row0);
+            tma_store_3d(&omap, sOw, col0, h, row0 - p.qbase);
             bulk_commit();
           }
         } else if (valid) {
@@ -503,7 +512,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
           }
           store64(pk, hh * 64);
         }
-        if (p.lse && valid) p.lse[(int64_t)h * p.T + j] = (m_ref + log2f(l)) * kLn2;
+        if (p.lse && valid) p.lse[(int64_t)h * p.T + (j - p.qbase)] = (m_ref + log2f(l)) * kLn2;
       } else {
         // merge the two streams' partial results of this row:
         //   m = max(m_0, m_1), a_s = 2^(m_s - m), L = a_0 l_0 + a_1 l_1,
@@ -560,7 +569,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
           for (int q = 0; q < 4; ++q)
             dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
-        if (p.lse && valid && t == 0) p.lse[(int64_t)h * p.T + j] = (m + log2f(L)) * kLn2;
+        if (p.lse && valid && t == 0) p.lse[(int64_t)h * p.T + (j - p.qbase)] = (m + log2f(L)) * kLn2;
       }
       ++lu;
     }
@@ -576,8 +585,9 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
 }
 
 template <int D>
-mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v, void* o,
-                      float* lse, int64_t qs, int64_t ks, int64_t vs, int64_t os, void* stream) {
+mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
+                      const void* kc, const void* vc, void* o, float* lse, int64_t qs, int64_t ks,
+                      int64_t vs, int64_t kcs, int64_t vcs, int64_t os, void* stream) {
   using C = AttnCfg<D>;
   bool ok = true;
   const uint32_t box[3] = {64, 1, (uint32_t)kBM};
@@ -592,6 +602,14 @@ mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
   const uint32_t obox[3] = {64, 1, 32};
   const uint64_t ostr[2] = {(uint64_t)D * 2, (uint64_t)os * 2};
   CUtensorMap om = make_tmap_bf16(o, 3, qd, ostr, obox, &ok);
+  CUtensorMap kcm = km, vcm = vm;
+  if (pl.cached) {
+    const uint64_t cd[3] = {(uint64_t)D, (uint64_t)pl.Hkv, (uint64_t)pl.cache_T};
+    const uint64_t kcstr[2] = {(uint64_t)D * 2, (uint64_t)kcs * 2};
+    const uint64_t vcstr[2] = {(uint64_t)D * 2, (uint64_t)vcs * 2};
+    kcm = make_tmap_bf16(kc, 3, cd, kcstr, box, &ok);
+    vcm = make_tmap_bf16(vc, 3, cd, vcstr, box, &ok);
+  }
   if (!ok) return MIS_ERR_CUDA;
 
   uint8_t* ws = static_cast<uint8_t*>(pl.workspace);
@@ -605,6 +623,7 @@ mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
   prm.lse = lse;
   prm.o_stride = os;
   prm.T = pl.T;
+  prm.qbase = pl.cached ? pl.qbase : 0;
   prm.group = pl.Hq / pl.Hkv;
   prm.n_head_groups = pl.n_head_groups;
   prm.scale_log2 = pl.scale * 1.4426950408889634f;
@@ -624,7 +643,8 @@ mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
   const int64_t total = (int64_t)pl.work.size() * pl.n_head_groups;
   if (total > 0x7fffffff) return MIS_ERR_UNSUPPORTED;
   dim3 grid((unsigned)std::min<int64_t>(total, num_sms()));
-  return launch_pdl(kern, grid, dim3(kThreads), C::kSmem, st, qm, km, vm, om, prm) == cudaSuccess
+  return launch_pdl(kern, grid, dim3(kThreads), C::kSmem, st, qm, km, vm, om, kcm, vcm, prm) ==
+                 cudaSuccess
              ? MIS_OK
              : MIS_ERR_CUDA;
 }
@@ -632,10 +652,13 @@ mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
 }  // namespace
 
 mis_status_t launch_attention(HostPlan& p, const void* q, const void* k, const void* v,
-                              void* o, float* lse, int64_t qs, int64_t ks, int64_t vs, int64_t os,
-                              void* stream) {
-  if (p.D == 128) return launch_d<128>(p, q, k, v, o, lse, qs, ks, vs, os, stream);
-  if (p.D == 64) return launch_d<64>(p, q, k, v, o, lse, qs, ks, vs, os, stream);
+                              const void* k_cache, const void* v_cache, void* o, float* lse,
+                              int64_t qs, int64_t ks, int64_t vs, int64_t kcs, int64_t vcs,
+                              int64_t os, void* stream) {
+  if (p.D == 128)
+    return launch_d<128>(p, q, k, v, k_cache, v_cache, o, lse, qs, ks, vs, kcs, vcs, os, stream);
+  if (p.D == 64)
+    return launch_d<64>(p, q, k, v, k_cache, v_cache, o, lse, qs, ks, vs, kcs, vcs, os, stream);
   return MIS_ERR_UNSUPPORTED;
 }
 

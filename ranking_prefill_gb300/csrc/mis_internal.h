@@ -57,7 +57,17 @@ struct HostPlan {
   void* workspace = nullptr;       // device base, set by mis_plan_create
   bool status_clear = false;       // the upload zeroed the status words; the
                                    // first launch need not clear them again
+  // cached-prefix plans: keys of request b's shared set live in a separate
+  // cache buffer. Rows are numbered on one virtual axis: cache rows
+  // [0, cache_T), new rows from qbase on (qbase leaves at least one empty
+  // 128-row tile after the cache, so no cache key tile reaches a new row).
+  bool cached = false;
+  int32_t cache_T = 0;
+  int32_t qbase = 0;
 };
+
+// Validates a cached-prefix descriptor and fills the plan (cached = true).
+mis_status_t build_plan_cached(const mis_cached_desc* d, HostPlan* p);
 
 // Validates the descriptor and fills everything but `workspace`.
 mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p);
@@ -96,9 +106,11 @@ int32_t schedule_override();
 
 // Kernel launchers (defined in the .cu files). Return MIS_ERR_CUDA on launch
 // failure. Pointers are already validated.
+// k_cache / v_cache (and their strides) are used by cached plans only.
 mis_status_t launch_attention(HostPlan& p, const void* q, const void* k, const void* v,
-                              void* o, float* lse, int64_t qs, int64_t ks, int64_t vs, int64_t os,
-                              void* stream);
+                              const void* k_cache, const void* v_cache, void* o, float* lse,
+                              int64_t qs, int64_t ks, int64_t vs, int64_t kcs, int64_t vcs,
+                              int64_t os, void* stream);
 
 struct ScoreArgs {
   const void* hidden; int64_t hidden_stride; int32_t T;

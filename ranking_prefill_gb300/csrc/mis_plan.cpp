@@ -51,6 +51,14 @@ double snake_makespan(const std::vector<double>& cost, int reps, int n_blocks) {
   return *std::max_element(load.begin(), load.end());
 }
 
+// A query tile while the plan is built: its key-tile list and its costs.
+struct Tmp { int32_t req, q0, kofs, nk; int64_t cost, cost_even, cost_odd; int64_t order; };
+
+// Shared tail of both planners: unit order, schedule, statistics and the
+// workspace layout. `T` is the row count seg_start covers.
+mis_status_t finish_plan(HostPlan* p, std::vector<Tmp>& tmp, int32_t B, int32_t T,
+                         int64_t visible, int64_t causal_tiles);
+
 }  // namespace
 
 mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
@@ -103,7 +111,6 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
   }
 
   // ---- tiles ----
-  struct Tmp { int32_t req, q0, kofs, nk; int64_t cost, cost_even, cost_odd; int64_t order; };
   std::vector<Tmp> tmp;
   int64_t visible = 0, causal_tiles = 0;
   for (int b = 0; b < B; ++b) {
@@ -147,6 +154,13 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
       tmp.push_back(w);
     }
   }
+  return finish_plan(p, tmp, B, T, visible, causal_tiles);
+}
+
+namespace {
+
+mis_status_t finish_plan(HostPlan* p, std::vector<Tmp>& tmp, int32_t B, int32_t T,
+                         int64_t visible, int64_t causal_tiles) {
   if (p->klist.size() > (size_t)std::numeric_limits<int32_t>::max()) return MIS_ERR_SHAPE;
   // Order: request by request, requests with the most expensive query tile
   // first, and inside a request the query tiles longest first. Blocks that run
@@ -202,6 +216,108 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
   p->total = off;
   p->stats.workspace_bytes = (int64_t)off;
   return MIS_OK;
+}
+
+}  // namespace
+
+
+}  // namespace mis
+
+namespace mis {
+
+// Cached-prefix plan: the new rows are item sets only; request b's shared set
+// Q is rows [cache_start, cache_start + S_b) of the cache. On the virtual row
+// axis (cache rows from 0, new rows from qbase) every row of item set a sees
+// [s0, pend) = its cached prefix and [lo(j), j] = its own item, which is the
+// same two-interval form as a packed request, so the kernel's visibility
+// test is unchanged. Cache key tiles never mix with new rows: qbase starts at
+// least one 128-row tile past the cache end.
+mis_status_t build_plan_cached(const mis_cached_desc* d, HostPlan* p) {
+  if (!d || !p) return MIS_ERR_INVALID_ARG;
+  if (d->B < 1 || d->T < 1 || d->Hq < 1 || d->Hkv < 1 || d->cache_T < 1) return MIS_ERR_INVALID_ARG;
+  if (!d->cu_seqlens || !d->item_ptr || !d->item_offsets || !d->cache_start || !d->cache_len)
+    return MIS_ERR_INVALID_ARG;
+  if (d->Hq % d->Hkv) return MIS_ERR_SHAPE;
+  if (d->D != 64 && d->D != 128) return MIS_ERR_UNSUPPORTED;
+  if (!(d->scale >= 0.f) || std::isinf(d->scale)) return MIS_ERR_INVALID_ARG;
+  const int32_t B = d->B, T = d->T;
+  const int32_t* cu = d->cu_seqlens;
+  if (cu[0] != 0 || cu[B] != T) return MIS_ERR_SHAPE;
+  for (int b = 0; b < B; ++b)
+    if (cu[b + 1] <= cu[b]) return MIS_ERR_SHAPE;
+  const int64_t qbase = (int64_t)align_up((size_t)d->cache_T, kBN) + kBN;
+  if (qbase + T >= ((int64_t)1 << 31) - kBN) return MIS_ERR_SHAPE;
+
+  p->B = B; p->T = T; p->Hq = d->Hq; p->Hkv = d->Hkv; p->D = d->D;
+  p->scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt((float)d->D);
+  p->req.assign(B, ReqInfo{});
+  p->seg_start.assign(T, 0);
+  p->work.clear(); p->klist.clear(); p->tile_map.clear();
+  p->stats = mis_plan_stats{};
+  p->cached = true;
+  p->cache_T = d->cache_T;
+  p->qbase = (int32_t)qbase;
+  const int32_t Vb = (int32_t)qbase;
+
+  for (int b = 0; b < B; ++b) {
+    const int32_t S = d->cache_len[b], cs = d->cache_start[b];
+    if (S < 1 || cs < 0 || (int64_t)cs + S > d->cache_T) return MIS_ERR_SHAPE;
+    const int32_t i0 = d->item_ptr[b], i1 = d->item_ptr[b + 1];
+    if (i0 < 0 || i1 <= i0 || (b == 0 && i0 != 0)) return MIS_ERR_SHAPE;
+    if (d->item_offsets[i0] != cu[b]) return MIS_ERR_SHAPE;
+    for (int32_t i = i0; i < i1; ++i) {
+      const int32_t a = d->item_offsets[i];
+      const int32_t e = (i + 1 < i1) ? d->item_offsets[i + 1] : cu[b + 1];
+      if (a < cu[b] || e <= a || e > cu[b + 1]) return MIS_ERR_SHAPE;
+      for (int32_t j = a; j < e; ++j) p->seg_start[j] = Vb + a;
+    }
+    p->req[b] = ReqInfo{cs, Vb + cu[b + 1], cs + S, 0};
+  }
+
+  std::vector<Tmp> tmp;
+  int64_t visible = 0, causal_tiles = 0;
+  for (int b = 0; b < B; ++b) {
+    const ReqInfo& R = p->req[b];
+    const int32_t S = R.pend - R.s0, base = Vb + cu[b], L = cu[b + 1] - cu[b];
+    for (int32_t r = cu[b]; r < cu[b + 1]; ++r)
+      visible += (int64_t)S + (Vb + r - p->seg_start[r] + 1);
+    const int32_t ncache = (S + kBN - 1) / kBN;
+    const int32_t nqt = (L + kBM - 1) / kBM;
+    for (int32_t t = 0; t < nqt; ++t) {
+      const int32_t r0 = base + t * kBM;
+      const int32_t r1 = std::min(r0 + kBM, R.e0);
+      // a causal pass over [prefix ; items] would need every prefix tile and
+      // every new-row tile up to the query tile
+      causal_tiles += ncache + (r1 - 1 - base) / kBN + 1;
+      const int32_t lo_min = p->seg_start[r0 - Vb], lo_max = p->seg_start[r1 - 1 - Vb];
+      Tmp w{b, r0, (int32_t)p->klist.size(), 0, 0, 0, 0, (int64_t)tmp.size()};
+      auto emit = [&](int32_t u, int32_t c0, bool full, bool need_mask) {
+        p->klist.push_back((uint32_t)c0 | (need_mask ? kNeedMask : 0u));
+        p->tile_map.insert(p->tile_map.end(), {b, t, u, full ? 1 : 2});
+        if (full) ++p->stats.n_full; else ++p->stats.n_partial;
+        const int c = need_mask ? 5 : 4;
+        (w.nk % 2 ? w.cost_odd : w.cost_even) += c;
+        ++w.nk;
+        w.cost += c;
+      };
+      // the cached prefix: every row sees all of it; a tile that runs past the
+      // prefix end holds other rows of the cache and is masked there
+      for (int32_t u = 0; u < ncache; ++u) {
+        const int32_t c0 = R.s0 + u * kBN;
+        emit(u, c0, true, c0 + kBN > R.pend);
+      }
+      // the band of the query tile's own items
+      const int32_t ba = (lo_min - base) / kBN, bb = (r1 - 1 - base) / kBN + 1;
+      for (int32_t v = ba; v < bb; ++v) {
+        const int32_t c0 = base + v * kBN;
+        const int32_t c1 = std::min(c0 + kBN, R.e0);
+        const bool full = (c1 - 1 <= r0) && (c0 >= lo_max);
+        emit(ncache + v, c0, full, !full || c0 + kBN > R.e0);
+      }
+      tmp.push_back(w);
+    }
+  }
+  return finish_plan(p, tmp, B, T, visible, causal_tiles);
 }
 
 }  // namespace mis

@@ -35,7 +35,8 @@ EXPORTS = ["mis_status_string", "mis_abi_version", "mis_layout_size", "mis_build
            "mis_get_device_status", "mis_set_wait_limit_ns", "mis_label_scores_noalloc",
            "mis_inject_stall", "mis_planner_create", "mis_planner_plan", "mis_planner_destroy",
            "mis_set_schedule", "mis_setwise_layout_size", "mis_build_setwise_layout",
-           "mis_rope_qk"]
+           "mis_rope_qk", "mis_cached_plan_workspace_size", "mis_cached_plan_create",
+           "mis_attention_fwd_cached"]
 
 
 class MisError(RuntimeError):
@@ -50,6 +51,13 @@ class mis_attn_desc(C.Structure):
                 # const int32_t* fields, passed as plain addresses
                 ("cu_seqlens", C.c_void_p), ("prefix_len", C.c_void_p),
                 ("item_ptr", C.c_void_p), ("item_offsets", C.c_void_p)]
+
+
+class mis_cached_desc(C.Structure):
+    _fields_ = [("B", C.c_int32), ("T", C.c_int32), ("Hq", C.c_int32), ("Hkv", C.c_int32),
+                ("D", C.c_int32), ("scale", C.c_float),
+                ("cu_seqlens", C.c_void_p), ("item_ptr", C.c_void_p), ("item_offsets", C.c_void_p),
+                ("cache_start", C.c_void_p), ("cache_len", C.c_void_p), ("cache_T", C.c_int32)]
 
 
 class mis_plan_stats(C.Structure):
@@ -96,6 +104,10 @@ def load(path: str = LIB_PATH):
         "mis_set_wait_limit_ns": (C.c_uint64, [C.c_uint64]),
         "mis_inject_stall": (C.c_uint32, [C.c_uint32]),
         "mis_set_schedule": (C.c_int32, [C.c_int32]),
+        "mis_cached_plan_workspace_size": (sz, [C.POINTER(mis_cached_desc)]),
+        "mis_cached_plan_create": (C.c_int, [C.POINTER(mis_cached_desc), vp, sz, vp, C.POINTER(vp)]),
+        "mis_attention_fwd_cached": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64,
+                                               i64, i64, vp]),
         "mis_rope_qk": (C.c_int, [vp, vp, vp, vp, i64, i64, i64, i64, C.c_int32, C.c_int32,
                                   C.c_int32, C.c_int32, vp, C.c_double, vp]),
         "mis_setwise_layout_size": (C.c_int, [C.c_int32, i32p, i32p, i32p, C.POINTER(i64),
@@ -319,6 +331,62 @@ class Plan:
             self.destroy()
         except Exception:
             pass
+
+
+class CachedPlan(Plan):
+    """Plan of item requests over a cached prefix (mis_cached_plan_create)."""
+
+    def __init__(self, cu_seqlens, item_ptr, item_offsets, cache_start, cache_len, cache_T,
+                 Hq, Hkv, D, scale: float = 0.0, workspace=None, stream=None):
+        self._L = load()
+        self._h = None
+        self.cu, self.ip, self.io = _i32(cu_seqlens), _i32(item_ptr), _i32(item_offsets)
+        self.cs, self.cl = _i32(cache_start), _i32(cache_len)
+        self.cdesc = mis_cached_desc(len(self.cl), int(self.cu[-1]), Hq, Hkv, D, scale,
+                                     _ptr_i32(self.cu), _ptr_i32(self.ip), _ptr_i32(self.io),
+                                     _ptr_i32(self.cs), _ptr_i32(self.cl), int(cache_T))
+        self.T, self.Hq, self.Hkv, self.D = int(self.cu[-1]), Hq, Hkv, D
+        self.workspace = workspace
+        if workspace is not None:
+            self.create(workspace, stream)
+
+    def workspace_size(self) -> int:
+        n = self._L.mis_cached_plan_workspace_size(C.byref(self.cdesc))
+        if n == 0:
+            h = C.c_void_p()
+            st = self._L.mis_cached_plan_create(C.byref(self.cdesc), None, 0, None, C.byref(h))
+            if st == 0:
+                self._L.mis_plan_destroy(h)
+            _check(st or lib_status_unknown(), "mis_cached_plan_workspace_size")
+        return int(n)
+
+    def create(self, workspace, stream=None):
+        self.destroy()
+        self.workspace = workspace
+        h = C.c_void_p()
+        if workspace is None:
+            _check(self._L.mis_cached_plan_create(C.byref(self.cdesc), None, 0, None, C.byref(h)),
+                   "mis_cached_plan_create")
+        else:
+            nbytes = workspace.numel() * workspace.element_size()
+            _check(self._L.mis_cached_plan_create(C.byref(self.cdesc), _dptr(workspace), nbytes,
+                                                  _stream(stream), C.byref(h)), "mis_cached_plan_create")
+        self._h = h
+        return self
+
+    @classmethod
+    def host_only(cls, *args, **kw):
+        p = cls(*args, **kw)
+        return p.create(None)
+
+
+def mis_attention_fwd_cached(plan: "CachedPlan", q, k, v, k_cache, v_cache, o, lse=None,
+                             stream=None):
+    L = load()
+    _check(L.mis_attention_fwd_cached(plan._h, _dptr(q), _dptr(k), _dptr(v), _dptr(k_cache),
+                                      _dptr(v_cache), _dptr(o), _dptr(lse), q.stride(0), k.stride(0),
+                                      v.stride(0), k_cache.stride(0), v_cache.stride(0), o.stride(0),
+                                      _stream(stream)), "mis_attention_fwd_cached")
 
 
 class Planner:

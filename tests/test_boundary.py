@@ -232,3 +232,42 @@ def test_rope_argument_checks(L):
     assert call(qs=16 * 128 - 8) == lib.MIS_ERR_SHAPE                         # row too short
     assert call(ks=8 * 128 + 4) == lib.MIS_ERR_SHAPE                          # stride not 8-multiple
     assert call(Hq=0) == lib.MIS_ERR_INVALID_ARG
+
+
+def _cached_random(rng):
+    B = int(rng.integers(1, 4))
+    S = rng.integers(1, 400, B)
+    n = rng.integers(1, 9, B)
+    lens = rng.integers(0, 150, int(n.sum()))
+    cstart, t = np.zeros(B, np.int64), int(rng.integers(0, 50))
+    for b in rng.permutation(B):
+        cstart[b] = t
+        t += int(S[b]) + int(rng.integers(0, 70))
+    return cstart, S, n, lens, t
+
+
+def test_cached_plan_tile_map_and_pairs_bit_exact(L):
+    rng = np.random.default_rng(91)
+    for case in range(25):
+        cstart, S, n, lens, cache_T = _cached_random(rng)
+        if case == 0:
+            S = np.array([128, 129, 127][: len(S)] + [1] * (len(S) - 3))[: len(S)]
+        cl = O.cached_layout(cstart, S, n, lens)
+        p = lib.CachedPlan.host_only(cl.cu_seqlens, cl.item_ptr, cl.item_offsets, cstart, S,
+                                     cache_T, 4, 2, 128)
+        assert np.array_equal(p.tile_map(), O.tile_map_cached(cl, 128, 128))
+        pairs = sum(int(S[cl.request_of[j]]) + j - int(cl.item_offsets[cl.item_of[j]]) + 1
+                    for j in range(cl.T))
+        assert p.stats()["visible_pairs"] == pairs
+    # errors
+    cl = O.cached_layout([0], [10], [2], [3, 4])
+    mk = lambda **kw: lib.CachedPlan.host_only(kw.get("cu", cl.cu_seqlens), kw.get("ip", cl.item_ptr),
+                                               kw.get("io", cl.item_offsets), kw.get("cs", [0]),
+                                               kw.get("cl", [10]), kw.get("T", 10), 4, 2, 64)
+    mk()
+    for kw, want in [(dict(T=9), lib.MIS_ERR_SHAPE), (dict(cl=[0]), lib.MIS_ERR_SHAPE),
+                     (dict(cs=[-1]), lib.MIS_ERR_SHAPE), (dict(ip=[0, 0]), lib.MIS_ERR_SHAPE),
+                     (dict(io=[1, 4]), lib.MIS_ERR_SHAPE)]:
+        with pytest.raises(lib.MisError) as e:
+            mk(**kw)
+        assert e.value.status == want, kw
