@@ -534,6 +534,82 @@ def run_comparators(w, shapes, vals, labels, dev, stream, q, k, v, hidden, w_lm,
             "chunks": n_chunks, "note": "each item packed as its own causal [prefix; item] sequence, "
             "batched varlen through the same kernels; row gathers untimed",
             "mis_speedup_kernels_only": round(t_sis / (t_attn + t_score), 2)}
+        res["prefix_cache"] = _prefix_cache(w, lay, labels, dev, stream, flush, q, k, v, hidden,
+                                            w_lm, t_attn, t_score, M)
+    return res
+
+
+def _prefix_cache(w, lay, labels, dev, stream, flush, q, k, v, hidden, w_lm, t_attn, t_score, M):
+    """The same requests with their prefixes in a K/V cache ("Turbocharging
+    LinkedIn's recommendation systems with SGLang": the in-batch prefix
+    cache and the knock-knock second request). Times the prefix prefill
+    (causal attention over each prefix: the first request, which fills the
+    cache), the item request (MIS among the items over the cached prefix,
+    then scoring) and single-item scoring with the prefix cache (one request
+    per item over the same cached rows). Row gathers are untimed."""
+    import torch
+    from ranking_prefill_gb300 import lib
+    sp = stream.cuda_stream
+    B = lay.B
+    S = lay.prefix_len.astype(np.int64)
+    cu = lay.cu_seqlens.astype(np.int64)
+    cum_s = np.concatenate([[0], np.cumsum(S)])
+    pre_rows = np.concatenate([np.arange(cu[b], cu[b] + S[b]) for b in range(B)])
+    item_rows = np.concatenate([np.arange(cu[b] + S[b], cu[b + 1]) for b in range(B)])
+    ip = lay.item_ptr.astype(np.int64)
+    req_of_item = np.repeat(np.arange(B), np.diff(ip))
+    # the item sequence: each request's item sets without its prefix
+    cu_i = (cu - cum_s).astype(np.int32)
+    io_i = (lay.item_offsets - cum_s[req_of_item + 1]).astype(np.int32)
+    rd_i = (lay.delim_positions - cum_s[req_of_item + 1]).astype(np.int32)
+    take = lambda t, rows: t.index_select(0, torch.as_tensor(rows, device=dev, dtype=torch.long))
+    kc, vc, qp = take(k, pre_rows), take(v, pre_rows), take(q, pre_rows)
+    qi, ki, vi, hi = take(q, item_rows), take(k, item_rows), take(v, item_rows), take(hidden, item_rows)
+    cache_T = int(cum_s[-1])
+    out = torch.empty(M, len(labels), dtype=torch.float32, device=dev)
+    res = {}
+    with torch.cuda.stream(stream):
+        # first request: causal prefill of the prefixes (fills the cache)
+        cpl = lib.Plan(cum_s.astype(np.int32), S.astype(np.int32), None, None, w.hq, w.hkv, w.head_dim)
+        wsp = torch.zeros(cpl.workspace_size(), dtype=torch.uint8, device=dev)
+        cpl.create(wsp, sp)
+        op = torch.empty_like(qp)
+        t_pre = _median_time(lambda: lib.mis_attention_fwd_plan(cpl, qp, kc, vc, op, None, sp), stream, flush)
+        # second request: the items over the cached prefix, then scoring
+        rd = torch.as_tensor(rd_i, device=dev)
+        wss = torch.zeros(lib.mis_label_scores_workspace_size(M, w.d_model, w.vocab, len(labels)),
+                          dtype=torch.uint8, device=dev)
+        t_sc = _median_time(lambda: lib.mis_label_scores(hi, w_lm, rd, labels, out, None, wss, stream=sp),
+                            stream, flush)
+        oi = torch.empty_like(qi)
+
+        def cached_time(cu_, ip_, io_, cs_, cl_):
+            pl = lib.CachedPlan(cu_, ip_, io_, cs_, cl_, cache_T, w.hq, w.hkv, w.head_dim)
+            wsc = torch.zeros(pl.workspace_size(), dtype=torch.uint8, device=dev)
+            pl.create(wsc, sp)
+            t = _median_time(lambda: lib.mis_attention_fwd_cached(pl, qi, ki, vi, kc, vc, oi, None, sp),
+                             stream, flush)
+            torch.cuda.synchronize()
+            assert lib.mis_get_device_status(wsc, sp) == 0
+            return t, pl.stats()
+        t_mis, st_mis = cached_time(cu_i, lay.item_ptr, io_i, cum_s[:-1].astype(np.int32), S.astype(np.int32))
+        # single-item scoring with the prefix cache: one request per item
+        ends_i = np.concatenate([io_i[1:], [cu_i[-1]]]).astype(np.int64)
+        ends_i[ip[1:][np.diff(ip) > 0] - 1] = cu_i[1:][np.diff(ip) > 0]
+        cu_s = np.concatenate([[0], np.cumsum(ends_i - io_i)]).astype(np.int32)
+        t_sis, _ = cached_time(cu_s, np.arange(M + 1, dtype=np.int32), cu_s[:-1],
+                               cum_s[req_of_item].astype(np.int32), S[req_of_item].astype(np.int32))
+    res = {"prefix_prefill_ms": round(t_pre * 1e3, 4),
+           "item_request": {"attention_ms": round(t_mis * 1e3, 4), "scoring_ms": round(t_sc * 1e3, 4),
+                            "items_per_s": round(M / (t_mis + t_sc), 1),
+                            "useful_tflops": round(useful_flops(st_mis["visible_pairs"], w.hq, w.head_dim)
+                                                   / t_mis / 1e12, 1),
+                            "vs_full_mis_step": round((t_attn + t_score) / (t_mis + t_sc), 3)},
+           "single_item_scoring_with_prefix_cache": {
+               "attention_ms": round(t_sis * 1e3, 4), "items_per_s": round(M / (t_sis + t_sc), 1),
+               "mis_item_request_speedup": round((t_sis + t_sc) / (t_mis + t_sc), 3)},
+           "knock_knock_total_ms": round((t_pre + t_mis + t_sc) * 1e3, 4),
+           "note": "prefix K/V gathered into a cache; item rows as their own sequence; gathers untimed"}
     return res
 
 

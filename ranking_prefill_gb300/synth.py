@@ -73,6 +73,13 @@ WORKLOADS = {
         "decision-256", 5, 256, (256, 256), (3, 10), (64, 64), 16, 8, 128, 1024,
         151936, (2, 3),
         "256 requests, prefix 256, U[3,10] items of 64 tokens, K=2 and K=3"),
+    # "Turbocharging LinkedIn's recommendation systems with SGLang", Results /
+    # Figure 3: one ranking request of a 12k-token prefix and 50 items of 150
+    # tokens (the shape of the page's MIS against single-item scoring with
+    # prefix caching); the page names no model, the qwen3-0.6b heads are used
+    "prefix12k-50x150": Workload(
+        "prefix12k-50x150", 7, 1, (12000, 12000), (50, 50), (150, 150), 16, 8, 128, 1024,
+        151936, (2,), "batch 1, prefix 12000, 50 items x 150 tokens"),
     # decision-256's draw (same seed) as setwise prompts: the prefix lengths are
     # the query lengths and the items the candidates, followed by one marker each
     "setwise-256": Workload(
