@@ -26,7 +26,7 @@
 // K/V tiles load while the current one finishes, and its first S product
 // runs during the epilogue.
 //
-// Warp roles (384 threads):
+// Warp roles (512 threads, four warpgroups):
 //   warp 0      : TMA producer (the unit's Q tiles, then K and V tiles
 //                 through separate rings: K is released once its S products
 //                 are issued, V after its PV products)
@@ -35,9 +35,19 @@
 //                   O_t += P_t V (TS: P_t from tensor memory, V MN-major)
 //                 in the order S_0(s), PV_1(s-1), S_1(s), PV_0(s) for step s,
 //                 so each stream's softmax overlaps the other's products
-//   warps 4..7  : softmax and epilogue of stream 0, warps 8..11: of stream 1.
-//                 One TMEM lane (= one query row) per thread: the row max and
-//                 sum stay in the thread, no shuffles.
+//   warps 4..7  : softmax of stream 0, warps 8..11: of stream 1. One TMEM
+//                 lane (= one query row) per thread: the row max and sum stay
+//                 in the thread, no shuffles. At the end of a unit a thread
+//                 leaves its row's (max, sum) in shared memory and moves on to
+//                 the next unit's first S tile at once.
+//   warps 12..15: epilogue. Once every PV of the unit is done they read O out
+//                 of tensor memory (handing each accumulator back to the MMA
+//                 thread as soon as it is read), merge the split schedule's
+//                 two partial results, normalise, and store O (and the LSE).
+//                 The epilogue of unit u thus overlaps the first softmax of
+//                 unit u+1 instead of delaying it.
+// Registers are rebalanced per warpgroup after the prologue (setmaxnreg):
+// the softmax warpgroups hold a whole 128-column S row per thread.
 // Tensor memory (512 columns): S_0 | S_1 | O_0 | O_1. P_t (bf16 pairs) is
 // written over the first half of S_t once S_t has been read. Because S_t(s)
 // is committed after PV_t(s-1) was issued, "S_t(s) ready" also means O_t and
@@ -70,12 +80,25 @@ struct AttnCfg {
   static constexpr int kTile = kBN * D * 2;            // a Q, K or V tile
   static constexpr int kKStages = (D == 128) ? 2 : 4;
   static constexpr int kVStages = (D == 128) ? 2 : 4;
-  static constexpr int kOWarp = 32 * 128;              // O staging per softmax warp: 32 rows x 64 bf16
-  static constexpr int kData = (2 + kKStages + kVStages) * kTile + 8 * kOWarp;
+  static constexpr int kOWarp = 32 * 128;              // O staging per epilogue warp: 32 rows x 64 bf16
+  static constexpr int kStats = 2 * 2 * kBM * 8;       // (max, sum) per row: 2 slots x 2 streams
+  static constexpr int kData = (2 + kKStages + kVStages) * kTile + 4 * kOWarp + kStats;
   static constexpr int kSmem = kData + 512 + 1024;     // barriers + alignment slack
 };
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
+// Per-thread register budgets after the prologue (control, epilogue, softmax
+// warpgroups); 128 + 128 + 256 threads must fit the launch's 512 x 128. The
+// split schedule's softmax keeps a few more values live, its epilogue merges
+// in 16-column pieces.
+template <bool kSplit>
+struct RegSplit {
+  static constexpr int kCtl = kSplit ? 80 : 88;
+  static constexpr int kEpi = kSplit ? 64 : 72;
+  static constexpr int kSoftmax = kSplit ? 184 : 176;
+  static_assert(128 * kCtl + 128 * kEpi + 256 * kSoftmax <= kThreads * 128,
+                "register split exceeds the launch allocation");
+};
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -122,9 +145,11 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   auto colS = [](int t) { return (uint32_t)(t * 128); };
   auto colO = [](int t) { return (uint32_t)(256 + t * D); };
   // barrier slots
+  //   ST_{s,t}: stream t's (max, sum) of a unit written to stats slot s;
+  //   SE_s: the epilogue has read slot s
   constexpr int bQF = 0, bQE = 1, bKF = 2, bKE = bKF + KS, bVF = bKE + KS, bVE = bVF + VS,
                 bSF = bVE + VS, bPF = bSF + 2, bOF = bPF + 2, bOE = bOF + 1, bDR = bOE + 2,
-                bXC = bDR + 1, nBar = bXC + 1;
+                bST = bDR + 1, bSE = bST + 4, nBar = bSE + 2;
 
   griddep_launch_dependents();
 
@@ -133,7 +158,9 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   uint8_t* sQ = smem;                                  // 2 tiles
   uint8_t* sK = smem + 2 * C::kTile;                   // KS tiles
   uint8_t* sV = sK + KS * C::kTile;                    // VS tiles
-  uint8_t* sO = sV + VS * C::kTile;                    // 8 x kOWarp: O staging of the softmax warps
+  uint8_t* sO = sV + VS * C::kTile;                    // 4 x kOWarp: O staging of the epilogue warps
+  // (max, sum) of every row at the end of a unit: [slot = unit & 1][stream][row]
+  float2* stats = reinterpret_cast<float2*>(sO + 4 * C::kOWarp);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kData);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + nBar);
   volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -157,11 +184,13 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(bSF + s), 1);
       mbar_init(bar(bPF + s), 4);                      // one arrival per softmax warp
-      mbar_init(bar(bOE + s), split ? 8 : 4);          // split: both streams read O_0 and O_1
+      mbar_init(bar(bOE + s), 4);                      // one arrival per epilogue warp
+      mbar_init(bar(bST + 2 * s), kBM);                // every thread of stream 0
+      mbar_init(bar(bST + 2 * s + 1), kBM);            // ... of stream 1
+      mbar_init(bar(bSE + s), kBM);                    // every epilogue thread
     }
     mbar_init(bar(bOF), 1);
     mbar_init(bar(bDR), 1);
-    mbar_init(bar(bXC), 256);                          // split: (max, sum) exchange, every thread
     fence_mbar_init();
     fence_proxy_async();
   }
@@ -185,162 +214,173 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
     return;
   }
   const Waiter W{abort_flag, p.status, p.wait_ns};
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int gk = 0, lu = 0, q_issued = 0, k_issued = 0, v_issued = 0;
-      bool ok = true;
-      for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {
-        const int u = unit_at(kk, total);
-        if (u < 0) continue;
-        const WorkItem un = p.units[u / n_hg];
-        const int h0 = (u % n_hg) * nh, g = h0 / p.group;
-        // Q of this unit once the previous unit's S products are done with it
-        if (lu > 0 && !(ok = wait(bar(bQE), (lu - 1) & 1, W, 0x80))) break;
-        mbar_arrive_expect_tx(bar(bQF), nh * C::kTile);
-        for (int t = 0; t < nh; ++t)
-          for (int b = 0; b < NB; ++b)
-            tma_load_3d(smem_u32(sQ + t * C::kTile + b * C::kBox), &qmap, bar(bQF), b * 64, h0 + t,
-                        un.q0 - p.qbase);
-        q_issued = lu + 1;
-        for (int it = 0; it < un.nk; ++it) {
-          const int gi = gk + it;
-          const int32_t c0 = (int32_t)(p.klist[un.kofs + it] & ~kNeedMask);
-          // key rows below qbase are cache rows (cached-prefix plans only)
-          const bool from_cache = c0 < p.qbase;
-          const CUtensorMap* km = from_cache ? &kcmap : &kmap;
-          const CUtensorMap* vm = from_cache ? &vcmap : &vmap;
-          const int32_t kr = from_cache ? c0 : c0 - p.qbase;
-          const int sk = gi % KS, sv = gi % VS;
-          if (gi >= KS && !(ok = wait(bar(bKE + sk), ((gi / KS) - 1) & 1, W, 0x100))) break;
-          mbar_arrive_expect_tx(bar(bKF + sk), C::kTile);
-          for (int b = 0; b < NB; ++b)
-            tma_load_3d(smem_u32(sK + sk * C::kTile + b * C::kBox), km, bar(bKF + sk), b * 64, g, kr);
-          k_issued = gi + 1;
-          if (gi >= VS && !(ok = wait(bar(bVE + sv), ((gi / VS) - 1) & 1, W, 0x180))) break;
-          mbar_arrive_expect_tx(bar(bVF + sv), C::kTile);
-          for (int b = 0; b < NB; ++b)
-            tma_load_3d(smem_u32(sV + sv * C::kTile + b * C::kBox), vm, bar(bVF + sv), b * 64, g, kr);
-          v_issued = gi + 1;
-        }
-        gk += un.nk;
-        ++lu;
-      }
-      // drain: every copy this thread started has landed before the block exits
-      if (q_issued > 0) wait_drain(bar(bQF), (q_issued - 1) & 1);
-      for (int i = (k_issued > KS ? k_issued - KS : 0); i < k_issued; ++i)
-        wait_drain(bar(bKF + i % KS), (i / KS) & 1);
-      for (int i = (v_issued > VS ? v_issued - VS : 0); i < v_issued; ++i)
-        wait_drain(bar(bVF + i % VS), (i / VS) & 1);
-    }
-  } else if (warp == 1) {
-    // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16(128, kBN, false);
-      constexpr uint32_t idO = idesc_bf16(128, D, true);
-      bool ok = true;
-      if (p.stall) ok = wait(bar(bDR), 0, W, 0x7ff);   // nothing arrives before the drain
-      // S_t = Q_q K^T into the S columns of stream t (q: the Q slot)
-      auto issue_s = [&](int t, int q, int sk) {
-        const uint32_t aQ = smem_u32(sQ + q * C::kTile);
-        const uint32_t aK = smem_u32(sK + sk * C::kTile);
-#pragma unroll
-        for (int b = 0; b < NB; ++b)
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_ss(tmem + colS(t), sdesc_sw128(aQ + b * C::kBox + ks * 32, 16, 1024),
-                   sdesc_sw128(aK + b * C::kBox + ks * 32, 16, 1024), idS, (b | ks) != 0);
-        mma_commit(bar(bSF + t));
-      };
-      auto issue_pv = [&](int t, int sv, bool acc) {
-        const uint32_t aV = smem_u32(sV + sv * C::kTile);
-#pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          // V is MN-major (head dim contiguous): 8-key groups 1024 B apart,
-          // 64-column boxes kBox apart. P_t sits in the first columns of S_t.
-          const uint64_t db = sdesc_sw128(aV + ks * 16 * 128, C::kBox, 1024);
-          mma_ts(tmem + colO(t), tmem + colS(t) + ks * 8, db, idO, (acc || ks != 0) ? 1u : 0u);
-        }
-      };
-      // c0, c1: S products issued so far for each stream (the phase of SF_t / PF_t)
-      int gk = 0, lu = 0, c0 = 0, c1 = 0;
-      for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {
-        const int u = unit_at(kk, total);
-        if (u < 0) continue;
-        const int nk = p.units[u / n_hg].nk;
-        if (!(ok = wait(bar(bQF), lu & 1, W, 0x200))) break;
-        // the first PV of stream t in this unit overwrites O_t: the epilogue of
-        // the previous unit must have read it out of tensor memory. In the
-        // split schedule one barrier covers both accumulators, and stream 0's
-        // first PV always comes first.
-        auto first_pv = [&](int t) -> bool {
-          if (lu == 0 || (split && t == 1)) return true;
-          if (!wait(bar(bOE + t), (lu - 1) & 1, W, 0x280 + t)) return false;
-          tc_fence_after();
-          return true;
-        };
-        // unit-local key tile of stream t at step s
-        const int ns = split ? (nk + 1) / 2 : nk;
-        bool pend1 = false;            // stream 1 owes the PV of the previous step
-        int pend1_g = 0;               // ... on this key tile (global index)
-        bool pend1_acc = false, pend1_first = false;
-        auto flush_pv1 = [&]() -> bool {
-          const int pend1_v = pend1_g % VS;
-          // split: stream 1's V tile is not stream 0's, wait for it here (in
-          // the pair schedule PV_0 of the same tile already waited)
-          if (split && !wait(bar(bVF + pend1_v), (pend1_g / VS) & 1, W, 0x3c0)) return false;
-          if (!wait(bar(bPF + 1), (c1 - 1) & 1, W, 0x400)) return false;
-          tc_fence_after();
-          if (pend1_first && !first_pv(1)) return false;
-          issue_pv(1, pend1_v, pend1_acc);
-          mma_commit(bar(bVE + pend1_v));
-          pend1 = false;
-          return true;
-        };
-        for (int st = 0; ok && st < ns; ++st) {
-          const int g0 = gk + (split ? 2 * st : st);
-          const int sk0 = g0 % KS, sv0 = g0 % VS;
-          if (!(ok = wait(bar(bKF + sk0), (g0 / KS) & 1, W, 0x300))) break;
-          tc_fence_after();
-          issue_s(0, 0, sk0);
-          if (split) mma_commit(bar(bKE + sk0));
-          if (pend1 && !(ok = flush_pv1())) break;
-          const int i1 = split ? 2 * st + 1 : st;
-          if (i1 < nk) {
-            const int g1 = gk + i1, sk1 = g1 % KS;
-            if (split) {
-              if (!(ok = wait(bar(bKF + sk1), (g1 / KS) & 1, W, 0x380))) break;
-              tc_fence_after();
-            }
-            issue_s(1, split ? 0 : 1, sk1);
-            mma_commit(bar(bKE + sk1));
-            ++c1;
-            pend1 = true;
-            pend1_g = g1;
-            pend1_acc = st > 0;
-            pend1_first = st == 0;
+  // register budgets per warpgroup: warps 0..3 control, 4..11 softmax, 12..15
+  // epilogue. The softmax warpgroups' request is the only increase and is met
+  // by the two decreases; no warpgroup hands registers back before it exits
+  // (an idle control warp doing so early could take them from the pool ahead
+  // of the softmax request and stall it).
+  if (warp < 4) {
+    regs_dec<RegSplit<kSplit>::kCtl>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        int gk = 0, lu = 0, q_issued = 0, k_issued = 0, v_issued = 0;
+        bool ok = true;
+        for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {
+          const int u = unit_at(kk, total);
+          if (u < 0) continue;
+          const WorkItem un = p.units[u / n_hg];
+          const int h0 = (u % n_hg) * nh, g = h0 / p.group;
+          // Q of this unit once the previous unit's S products are done with it
+          if (lu > 0 && !(ok = wait<true>(bar(bQE), (lu - 1) & 1, W, 0x80))) break;
+          mbar_arrive_expect_tx(bar(bQF), nh * C::kTile);
+          for (int t = 0; t < nh; ++t)
+            for (int b = 0; b < NB; ++b)
+              tma_load_3d(smem_u32(sQ + t * C::kTile + b * C::kBox), &qmap, bar(bQF), b * 64,
+                          h0 + t, un.q0 - p.qbase);
+          q_issued = lu + 1;
+          for (int it = 0; it < un.nk; ++it) {
+            const int gi = gk + it;
+            const int32_t c0 = (int32_t)(p.klist[un.kofs + it] & ~kNeedMask);
+            // key rows below qbase are cache rows (cached-prefix plans only)
+            const bool from_cache = c0 < p.qbase;
+            const CUtensorMap* km = from_cache ? &kcmap : &kmap;
+            const CUtensorMap* vm = from_cache ? &vcmap : &vmap;
+            const int32_t kr = from_cache ? c0 : c0 - p.qbase;
+            const int sk = gi % KS, sv = gi % VS;
+            if (gi >= KS && !(ok = wait<true>(bar(bKE + sk), ((gi / KS) - 1) & 1, W, 0x100))) break;
+            mbar_arrive_expect_tx(bar(bKF + sk), C::kTile);
+            for (int b = 0; b < NB; ++b)
+              tma_load_3d(smem_u32(sK + sk * C::kTile + b * C::kBox), km, bar(bKF + sk), b * 64,
+                          g, kr);
+            k_issued = gi + 1;
+            if (gi >= VS && !(ok = wait<true>(bar(bVE + sv), ((gi / VS) - 1) & 1, W, 0x180))) break;
+            mbar_arrive_expect_tx(bar(bVF + sv), C::kTile);
+            for (int b = 0; b < NB; ++b)
+              tma_load_3d(smem_u32(sV + sv * C::kTile + b * C::kBox), vm, bar(bVF + sv), b * 64,
+                          g, kr);
+            v_issued = gi + 1;
           }
-          if (st == ns - 1) mma_commit(bar(bQE));        // Q of this unit no longer read
-          if (!(ok = wait(bar(bVF + sv0), (g0 / VS) & 1, W, 0x480))) break;
-          if (!(ok = wait(bar(bPF + 0), c0 & 1, W, 0x500))) break;
-          tc_fence_after();
-          if (st == 0 && !(ok = first_pv(0))) break;
-          issue_pv(0, sv0, st > 0);
-          ++c0;
-          if (split) mma_commit(bar(bVE + sv0));
+          gk += un.nk;
+          ++lu;
         }
-        if (ok && pend1) ok = flush_pv1();
-        if (ok) mma_commit(bar(bOF));                    // every PV of the unit done
-        gk += nk;
-        ++lu;
+        // drain: every copy this thread started has landed before the block exits
+        if (q_issued > 0) wait_drain(bar(bQF), (q_issued - 1) & 1);
+        for (int i = (k_issued > KS ? k_issued - KS : 0); i < k_issued; ++i)
+          wait_drain(bar(bKF + i % KS), (i / KS) & 1);
+        for (int i = (v_issued > VS ? v_issued - VS : 0); i < v_issued; ++i)
+          wait_drain(bar(bVF + i % VS), (i / VS) & 1);
       }
-      // drain: all tensor-core work of this thread completes before dealloc
-      mma_commit(bar(bDR));
-      wait_drain(bar(bDR), 0);
+    } else if (warp == 1) {
+      // ----------------------------------------------------------------- MMA
+      if (lane == 0) {
+        constexpr uint32_t idS = idesc_bf16(128, kBN, false);
+        constexpr uint32_t idO = idesc_bf16(128, D, true);
+        bool ok = true;
+        if (p.stall) ok = wait<true>(bar(bDR), 0, W, 0x7ff);   // nothing arrives before the drain
+        // S_t = Q_q K^T into the S columns of stream t (q: the Q slot)
+        auto issue_s = [&](int t, int q, int sk) {
+          const uint32_t aQ = smem_u32(sQ + q * C::kTile);
+          const uint32_t aK = smem_u32(sK + sk * C::kTile);
+#pragma unroll
+          for (int b = 0; b < NB; ++b)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_ss(tmem + colS(t), sdesc_sw128(aQ + b * C::kBox + ks * 32, 16, 1024),
+                     sdesc_sw128(aK + b * C::kBox + ks * 32, 16, 1024), idS, (b | ks) != 0);
+          mma_commit(bar(bSF + t));
+        };
+        auto issue_pv = [&](int t, int sv, bool acc) {
+          const uint32_t aV = smem_u32(sV + sv * C::kTile);
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks) {
+            // V is MN-major (head dim contiguous): 8-key groups 1024 B apart,
+            // 64-column boxes kBox apart. P_t sits in the first columns of S_t.
+            const uint64_t db = sdesc_sw128(aV + ks * 16 * 128, C::kBox, 1024);
+            mma_ts(tmem + colO(t), tmem + colS(t) + ks * 8, db, idO, (acc || ks != 0) ? 1u : 0u);
+          }
+        };
+        // c0, c1: S products issued so far for each stream (the phase of SF_t / PF_t)
+        int gk = 0, lu = 0, c0 = 0, c1 = 0;
+        for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {
+          const int u = unit_at(kk, total);
+          if (u < 0) continue;
+          const int nk = p.units[u / n_hg].nk;
+          if (!(ok = wait<true>(bar(bQF), lu & 1, W, 0x200))) break;
+          // the first PV of stream t in this unit overwrites O_t: the epilogue of
+          // the previous unit must have read it out of tensor memory. In the
+          // split schedule one barrier covers both accumulators, and stream 0's
+          // first PV always comes first.
+          auto first_pv = [&](int t) -> bool {
+            if (lu == 0 || (split && t == 1)) return true;
+            if (!wait<true>(bar(bOE + t), (lu - 1) & 1, W, 0x280 + t)) return false;
+            tc_fence_after();
+            return true;
+          };
+          // unit-local key tile of stream t at step s
+          const int ns = split ? (nk + 1) / 2 : nk;
+          bool pend1 = false;            // stream 1 owes the PV of the previous step
+          int pend1_g = 0;               // ... on this key tile (global index)
+          bool pend1_acc = false, pend1_first = false;
+          auto flush_pv1 = [&]() -> bool {
+            const int pend1_v = pend1_g % VS;
+            // split: stream 1's V tile is not stream 0's, wait for it here (in
+            // the pair schedule PV_0 of the same tile already waited)
+            if (split && !wait<true>(bar(bVF + pend1_v), (pend1_g / VS) & 1, W, 0x3c0))
+              return false;
+            if (!wait<true>(bar(bPF + 1), (c1 - 1) & 1, W, 0x400)) return false;
+            tc_fence_after();
+            if (pend1_first && !first_pv(1)) return false;
+            issue_pv(1, pend1_v, pend1_acc);
+            mma_commit(bar(bVE + pend1_v));
+            pend1 = false;
+            return true;
+          };
+          for (int st = 0; ok && st < ns; ++st) {
+            const int g0 = gk + (split ? 2 * st : st);
+            const int sk0 = g0 % KS, sv0 = g0 % VS;
+            if (!(ok = wait<true>(bar(bKF + sk0), (g0 / KS) & 1, W, 0x300))) break;
+            tc_fence_after();
+            issue_s(0, 0, sk0);
+            if (split) mma_commit(bar(bKE + sk0));
+            if (pend1 && !(ok = flush_pv1())) break;
+            const int i1 = split ? 2 * st + 1 : st;
+            if (i1 < nk) {
+              const int g1 = gk + i1, sk1 = g1 % KS;
+              if (split) {
+                if (!(ok = wait<true>(bar(bKF + sk1), (g1 / KS) & 1, W, 0x380))) break;
+                tc_fence_after();
+              }
+              issue_s(1, split ? 0 : 1, sk1);
+              mma_commit(bar(bKE + sk1));
+              ++c1;
+              pend1 = true;
+              pend1_g = g1;
+              pend1_acc = st > 0;
+              pend1_first = st == 0;
+            }
+            if (st == ns - 1) mma_commit(bar(bQE));        // Q of this unit no longer read
+            if (!(ok = wait<true>(bar(bVF + sv0), (g0 / VS) & 1, W, 0x480))) break;
+            if (!(ok = wait<true>(bar(bPF + 0), c0 & 1, W, 0x500))) break;
+            tc_fence_after();
+            if (st == 0 && !(ok = first_pv(0))) break;
+            issue_pv(0, sv0, st > 0);
+            ++c0;
+            if (split) mma_commit(bar(bVE + sv0));
+          }
+          if (ok && pend1) ok = flush_pv1();
+          if (ok) mma_commit(bar(bOF));                    // every PV of the unit done
+          gk += nk;
+          ++lu;
+        }
+        // drain: all tensor-core work of this thread completes before dealloc
+        mma_commit(bar(bDR));
+        wait_drain(bar(bDR), 0);
+      }
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------------- softmax and epilogue
+  } else if (warp < 12) {
+    // -------------------------------------------------------------- softmax
+    regs_inc<RegSplit<kSplit>::kSoftmax>();
     const int t = (warp - 4) / 4;                       // stream
     const int sw = warp & 3;
     const int r = sw * 32 + lane;
@@ -348,16 +388,12 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
     const uint32_t tS = tl + colS(t), tO = tl + colO(t);
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = f2_pack(__float_as_uint(sl2), __float_as_uint(sl2));
-    // split schedule: each stream's (max, sum) for the other, in the unused
-    // second Q slot
-    float2* xch = reinterpret_cast<float2*>(sQ + C::kTile);
     int lu = 0, cs = 0;                                 // cs: S tiles of this stream so far
     bool ok = true;
     for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {
       const int u = unit_at(kk, total);
       if (u < 0) continue;
       const WorkItem un = p.units[u / n_hg];
-      const int h = split ? u % n_hg : (u % n_hg) * 2 + t;
       const ReqInfo R = p.req[un.req];
       const int j = un.q0 + r;
       const bool valid = j < R.e0;
@@ -375,7 +411,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
         if (it + 1 < nkt) e_next = p.klist[un.kofs + kfirst + (it + 1) * kstep];   // prefetch
         const int32_t c0 = (int32_t)(e & ~kNeedMask);
         const bool masked = (e & kNeedMask) != 0;
-        ok = wait(bar(bSF + t), gi & 1, W, 0x600);
+        ok = wait<true>(bar(bSF + t), gi & 1, W, 0x600);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
@@ -454,122 +490,185 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
       }
       if (!ok) break;
       cs += nkt;
-      ok = wait(bar(bOF), lu & 1, W, 0x700);
+      // hand the row's (max, sum) to the epilogue and go on to the next unit.
+      // Slot lu & 1 last held unit lu - 2, which the epilogue has read once
+      // SE of the slot completed for it.
+      const int slot = lu & 1;
+      if (lu >= 2) {
+        ok = wait<true>(bar(bSE + slot), ((lu >> 1) - 1) & 1, W, 0x6c0 + t);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      stats[(slot * 2 + t) * kBM + r] = make_float2(m_ref, l);
+      mbar_arrive(bar(bST + slot * 2 + t));
+      ++lu;
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    regs_dec<RegSplit<kSplit>::kEpi>();
+    const int sw = warp & 3;
+    const int r = sw * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(sw * 32) << 16);
+    const uint32_t sOw = smem_u32(sO + sw * C::kOWarp);
+    int lu = 0;
+    bool ok = true;
+    for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {
+      const int u = unit_at(kk, total);
+      if (u < 0) continue;
+      const WorkItem un = p.units[u / n_hg];
+      const ReqInfo R = p.req[un.req];
+      const int j = un.q0 + r;
+      const bool valid = j < R.e0;
+      // both streams' (max, sum) of the row; the slot is free once read
+      const int slot = lu & 1;
+      ok = wait<true>(bar(bST + slot * 2), (lu >> 1) & 1, W, 0x700) &&
+           wait<true>(bar(bST + slot * 2 + 1), (lu >> 1) & 1, W, 0x701);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const float2 s0 = stats[(slot * 2) * kBM + r], s1 = stats[(slot * 2 + 1) * kBM + r];
+      mbar_arrive(bar(bSE + slot));
+      ok = wait<true>(bar(bOF), lu & 1, W, 0x740);          // every PV of the unit done
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      __nv_bfloat16* orow = p.o + (int64_t)(valid ? j - p.qbase : 0) * p.o_stride + (int64_t)h * D;
       // O leaves through a 32-row x 64-column staging buffer per warp and a
       // TMA tensor store (asynchronous, whole rows); a warp whose 32 rows run
       // past the request's end stores its valid rows directly instead, since
       // the rows after them belong to the next request
       const int row0 = un.q0 + sw * 32;
       const bool wfull = row0 + 32 <= R.e0;
-      const uint32_t sOw = smem_u32(sO + (warp - 4) * C::kOWarp);
-      auto store64 = [&](const uint32_t* pk, int col0) {   // 64 bf16 of this row at column col0
-        if (wfull) {
-          if (lane == 0) bulk_wait_read0();               // the previous store read the buffer
-          __syncwarp();
-          const uint32_t ra = sOw + lane * 128;
+      auto stage_begin = [&]() {                        // the previous store has read the buffer
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+      };
+      // 32 columns (16 bf16 pairs) of this row: piece q of the staged 64 columns
+      auto stage16 = [&](const uint32_t* pk, int q) {
+        const uint32_t ra = sOw + lane * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)                     // 128-byte swizzle: chunk c ^ (row & 7)
-            st_shared_v4(ra + ((c ^ (lane & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                         pk[4 * c + 3]);
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&omap, sOw, col0, h, row0 - p.qbase);
-            bulk_commit();
-          }
-        } else if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + col0);
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        for (int c = 0; c < 4; ++c) {                   // 128-byte swizzle: chunk cc ^ (row & 7)
+          const int cc = q * 4 + c;
+          st_shared_v4(ra + ((cc ^ (lane & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                       pk[4 * c + 3]);
         }
       };
-      if (!split) {
-        // normalise O_t and store it as bf16, 64 columns at a time
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-        for (int hh = 0; hh < D / 64; ++hh) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(tO + hh * 64 + c * 32, ov);
-            tmem_ld_wait();
-            reg_fence32(ov);
-            if (hh == D / 64 - 1 && c == 1) {           // O_t fully read: hand it back
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar(bOE + t));
-            }
-#pragma unroll
-            for (int x = 0; x < 16; ++x)
-              pk[c * 16 + x] = pack_bf16(__uint_as_float(ov[2 * x]) * inv,
-                                         __uint_as_float(ov[2 * x + 1]) * inv);
-          }
-          store64(pk, hh * 64);
+      auto stage_end = [&](int col0, int h) {
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&omap, sOw, col0, h, row0 - p.qbase);
+          bulk_commit();
         }
-        if (p.lse && valid) p.lse[(int64_t)h * p.T + (j - p.qbase)] = (m_ref + log2f(l)) * kLn2;
+      };
+      // 16 columns (8 bf16 pairs): piece q of the staged 64 columns
+      auto stage8 = [&](const uint32_t* pk, int q) {
+        const uint32_t ra = sOw + lane * 128;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int cc = q * 2 + c;
+          st_shared_v4(ra + ((cc ^ (lane & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                       pk[4 * c + 3]);
+        }
+      };
+      auto direct8 = [&](const uint32_t* pk, int col0, int h) {
+        if (!valid) return;
+        uint4* dst = reinterpret_cast<uint4*>(p.o + (int64_t)(j - p.qbase) * p.o_stride +
+                                              (int64_t)h * D + col0);
+        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      };
+      auto direct16 = [&](const uint32_t* pk, int col0, int h) {
+        if (!valid) return;
+        uint4* dst = reinterpret_cast<uint4*>(p.o + (int64_t)(j - p.qbase) * p.o_stride +
+                                              (int64_t)h * D + col0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      };
+      if (!split) {
+        // head t of the pair: O_t / l_t, 32 columns at a time; O_t goes back
+        // to the MMA thread as soon as its last columns are read
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const float2 st = t == 0 ? s0 : s1;
+          const int h = (u % n_hg) * 2 + t;
+          const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
+          const uint32_t tO = tl + colO(t);
+#pragma unroll
+          for (int hh = 0; hh < D / 64; ++hh) {
+            if (wfull) stage_begin();
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              uint32_t ov[32];
+              tmem_ld32(tO + hh * 64 + q * 32, ov);
+              tmem_ld_wait();
+              reg_fence32(ov);
+              if (hh == D / 64 - 1 && q == 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(bOE + t));
+              }
+              uint32_t pk[16];
+#pragma unroll
+              for (int x = 0; x < 16; ++x)
+                pk[x] = pack_bf16(__uint_as_float(ov[2 * x]) * inv,
+                                  __uint_as_float(ov[2 * x + 1]) * inv);
+              if (wfull) stage16(pk, q);
+              else direct16(pk, hh * 64 + q * 32, h);
+            }
+            if (wfull) stage_end(hh * 64, h);
+          }
+          if (p.lse && valid) p.lse[(int64_t)h * p.T + (j - p.qbase)] = (st.x + log2f(st.y)) * kLn2;
+        }
       } else {
         // merge the two streams' partial results of this row:
         //   m = max(m_0, m_1), a_s = 2^(m_s - m), L = a_0 l_0 + a_1 l_1,
         //   O = (a_0 O_0 + a_1 O_1) / L.
-        // Stream t writes the head-dim half [t D/2, (t+1) D/2).
-        xch[t * kBM + r] = make_float2(m_ref, l);
-        mbar_arrive(bar(bXC));
-        ok = wait(bar(bXC), lu & 1, W, 0x780);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        const float2 other = xch[(1 - t) * kBM + r];
-        const float m = fmaxf(m_ref, other.x);
-        const float a_me = (m == -INFINITY) ? 0.f : ex2(m_ref - m);
-        const float a_ot = (m == -INFINITY) ? 0.f : ex2(other.x - m);
-        const float L = l * a_me + other.y * a_ot;
+        const int h = u % n_hg;
+        const float m = fmaxf(s0.x, s1.x);
+        const float a0 = (m == -INFINITY) ? 0.f : ex2(s0.x - m);
+        const float a1 = (m == -INFINITY) ? 0.f : ex2(s1.x - m);
+        const float L = s0.y * a0 + s1.y * a1;
         const float inv = L > 0.f ? 1.f / L : 0.f;
-        const float w0 = (t == 0 ? a_me : a_ot) * inv, w1 = (t == 0 ? a_ot : a_me) * inv;
-        const bool has1 = nk > 1;                       // stream 1 wrote O_1 in this unit
+        const float w0 = a0 * inv, w1 = a1 * inv;
+        const bool has1 = un.nk > 1;                    // stream 1 wrote O_1 in this unit
         const uint32_t tO0 = tl + colO(0), tO1 = tl + colO(1);
-        constexpr int NH = D / 64;                      // 32-column chunks per half
-        uint32_t pk[16 * NH];
 #pragma unroll
-        for (int c2 = 0; c2 < NH; ++c2) {
-          const int c = t * NH + c2;
-          // O_1 is read even when stream 1 had no tile (then it holds an older
-          // unit's values, or nothing ever written) and dropped by a select
-          uint32_t o0[32], o1[32];
-          tmem_ld32(tO0 + c * 32, o0);
-          tmem_ld32(tO1 + c * 32, o1);
-          tmem_ld_wait();
-          reg_fence32(o0);
-          reg_fence32(o1);
-          if (c2 == NH - 1) {                           // both halves read: hand O back
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(bOE + 0));
-          }
+        for (int hh = 0; hh < D / 64; ++hh) {
+          if (wfull) stage_begin();
 #pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            float v2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float a = __uint_as_float(o0[2 * x + e]) * w0;
-              v2[e] = has1 ? fmaf(__uint_as_float(o1[2 * x + e]), w1, a) : a;
+          for (int q = 0; q < 4; ++q) {                 // 16 columns of each accumulator at a time
+            const int c = hh * 64 + q * 16;
+            // O_1 is read even when stream 1 had no tile (then it holds an
+            // older unit's values, or nothing ever written) and dropped by a
+            // select
+            uint32_t o0[16], o1[16];
+            tmem_ld16(tO0 + c, o0);
+            tmem_ld16(tO1 + c, o1);
+            tmem_ld_wait();
+            reg_fence16(o0);
+            reg_fence16(o1);
+            if (hh == D / 64 - 1 && q == 3) {           // both accumulators read: hand them back
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar(bOE + 0));
             }
-            pk[c2 * 16 + x] = pack_bf16(v2[0], v2[1]);
-          }
-        }
-        if constexpr (D == 128) {
-          store64(pk, t * 64);
-        } else if (valid) {                             // 32 columns: direct stores
-          uint4* dst = reinterpret_cast<uint4*>(orow + t * 32);
+            uint32_t pk[8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            for (int x = 0; x < 8; ++x) {
+              float v2[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float a = __uint_as_float(o0[2 * x + e]) * w0;
+                v2[e] = has1 ? fmaf(__uint_as_float(o1[2 * x + e]), w1, a) : a;
+              }
+              pk[x] = pack_bf16(v2[0], v2[1]);
+            }
+            if (wfull) stage8(pk, q);
+            else direct8(pk, c, h);
+          }
+          if (wfull) stage_end(hh * 64, h);
         }
-        if (p.lse && valid && t == 0) p.lse[(int64_t)h * p.T + (j - p.qbase)] = (m + log2f(L)) * kLn2;
+        if (p.lse && valid) p.lse[(int64_t)h * p.T + (j - p.qbase)] = (m + log2f(L)) * kLn2;
       }
       ++lu;
     }

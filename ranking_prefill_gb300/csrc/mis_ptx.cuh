@@ -65,8 +65,8 @@ __device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bit, uin
   if ((atomicOr(status, bit) & bit) == 0) status[1] = where;
 }
 
-static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Waiter& w,
-                                       uint32_t where) {
+__device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity, const Waiter& w,
+                                          uint32_t where) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -82,10 +82,20 @@ static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, con
   }
 }
 
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Waiter& w,
+                                              uint32_t where) {
+  return wait_spin(bar, parity, w, where);
+}
+
+// kInline: the slow path is inlined too. Kernels that rebalance registers per
+// warpgroup (setmaxnreg) need it: ptxas cannot give a called function the
+// budgets of several warpgroups.
+template <bool kInline = false>
 __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, const Waiter& w,
                                      uint32_t where) {
   if (mbar_try_wait(bar, parity)) return true;
-  return wait_slow(bar, parity, w, where);
+  if constexpr (kInline) return wait_spin(bar, parity, w, where);
+  else return wait_slow(bar, parity, w, where);
 }
 
 // Wait used while draining after an abort: fixed 20 ms bound, no status.
@@ -236,6 +246,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// 32 lanes x 32 bit, 16 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
 __device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
   uint32_t r;
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
@@ -254,6 +274,12 @@ __device__ __forceinline__ void reg_fence32(uint32_t* r) {
                  "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
                  "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
                  "+r"(r[30]), "+r"(r[31]));
+}
+__device__ __forceinline__ void reg_fence16(uint32_t* r) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
 }
 __device__ __forceinline__ void reg_fence1(uint32_t& r) { asm volatile("" : "+r"(r)); }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
