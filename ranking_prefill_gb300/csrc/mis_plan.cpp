@@ -27,13 +27,15 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Cost of a unit in softmax-step units (one step: two 128x128 S tiles, one
 // per stream, with their PV products); a masked tile costs 5/4 of a full one.
-// kUnitCost covers a unit's Q load, epilogue and pipeline turn-around. Fitted
-// on GB300 to kernel times of both schedules on four packed batches (one
-// request of 3.5K rows, one of 18.5K, 16 requests with 201K rows in all, 256
-// requests with 174K) as time = fixed + step * makespan: a unit costs 1.5
-// steps, and the split schedule's doubled K/V tile loads show up in that
-// per-unit cost rather than in a per-step factor.
-constexpr double kUnitCost = 1.5;
+// kUnitCost covers a unit's Q load, the turn-around of its first and last
+// tiles and the hand-over of O to the epilogue warps. Fitted on GB300 as
+// time = fixed + step * makespan to kernel times of both schedules on eleven
+// packed batches (single requests of 3.5K to 19.5K rows, 16 to 640 requests
+// of up to 555K rows in all): a unit costs one step; every unit cost between
+// 0.5 and 1.5 steps picks the faster schedule on all of them. The split
+// schedule's doubled K/V tile loads show up in that per-unit cost rather than
+// in a per-step factor.
+constexpr double kUnitCost = 1.0;
 
 // Largest per-block total of unit costs when `units` (in list order, each
 // repeated `reps` times for its heads) are dealt to min(total, n_blocks)
