@@ -74,6 +74,21 @@ def test_single_item_and_empty_items(schedule):
     check_attention(s, 4, 2, 128, 8)
 
 
+def test_many_one_tile_units(schedule):
+    # 600 requests of at most 113 rows: every unit has a single key tile, so
+    # in the split schedule stream 1 has no tile at all and hands its row
+    # statistics to the epilogue unit after unit, about 32 units per block
+    rng = np.random.default_rng(77)
+    B = 600
+    p = rng.integers(0, 100, B)
+    n = rng.integers(0, 3, B)
+    lens = rng.integers(0, 10, int(n.sum()))
+    err, st = check_attention(synth.custom_shapes(p, n, lens), 16, 8, 128, 77)
+    assert st["n_qtiles"] == B
+    assert st["n_full"] + st["n_partial"] == B          # one key tile per query tile
+    _expect_schedule(st, schedule, 16, 8)
+
+
 def test_strided_rows_and_no_lse():
     s = synth.custom_shapes([250, 60], [7, 3], [20, 1, 33, 64, 0, 5, 90, 17, 8, 41])
     check_attention(s, 4, 2, 128, 9, stride_pad=8, with_lse=False)
