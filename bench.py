@@ -2,7 +2,9 @@
 """Benchmark of the MIS prefill hot path on one GB300 (or N replicas).
 
 One step = the whole hot path over one batch of synthetic requests:
-layout packing, mask-aware tile planning (host) and its upload, MIS attention
+layout packing, mask-aware tile planning (host) and its upload (step i+1's
+plan travels on a copy stream during step i, which ends only once it has
+landed), MIS attention
 (one layer's worth: Q/K/V -> O), delimiter-row gather, LM-head contraction
 with fused full-vocabulary logsumexp, and the label read-out. The metric is
 scored items per second; attention is also reported as useful (unmasked)
@@ -210,53 +212,87 @@ def run_ours(args, rank, world, dist):
     out = torch.empty(M, K, dtype=torch.float32, device=dev)
     lay0 = HostLayout(w, shapes)
     plan0 = lib.Plan(*lay0.plan_args(), w.hq, w.hkv, w.head_dim)
-    # plan workspace, followed by the batch's readout rows (and, with --rope,
-    # its position ids), uploaded together
+    # two plan workspaces, each followed by its batch's readout rows (and, with
+    # --rope, its position ids), uploaded together: the plan of step i+1
+    # travels on a copy stream while step i computes, as in a serving loop
     wsz = plan0.workspace_size()
     n_extra = M + (T if args.rope else 0)
-    ws_plan = torch.zeros(wsz + 4 * n_extra, dtype=torch.uint8, device=dev)
-    delim_dev = ws_plan[wsz:wsz + 4 * M].view(torch.int32)
-    pos_dev = ws_plan[wsz + 4 * M:wsz + 4 * n_extra].view(torch.int32)
+    ws_plans = [torch.zeros(wsz + 4 * n_extra, dtype=torch.uint8, device=dev) for _ in range(2)]
+    delim_devs = [wp[wsz:wsz + 4 * M].view(torch.int32) for wp in ws_plans]
+    pos_devs = [wp[wsz + 4 * M:wsz + 4 * n_extra].view(torch.int32) for wp in ws_plans]
     qr, kr = (torch.empty_like(q), torch.empty_like(k)) if args.rope else (q, k)
     ws_score = torch.zeros(lib.mis_label_scores_workspace_size(M, w.d_model, w.vocab, K),
                            dtype=torch.uint8, device=dev)
     flush = L2Flush(dev)
-    plan0.create(ws_plan, sp)
+    plan0.create(ws_plans[0], sp)
     stats = plan0.stats()
     plan0.destroy()
     planner = lib.Planner()
+    copy_stream = torch.cuda.Stream(dev)
+    uploaded = [torch.cuda.Event(), torch.cuda.Event()]
+    used = [None, None]            # the step that last read each plan workspace
+    plans = {}
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
-    def step(times=None):
-        # a1: layout (host)
+    def enqueue_plan(i, after=None):
+        """a1 + a2 of step i on the host (layout, plan), then one asynchronous
+        upload of the plan and the readout rows into workspace i % 2 on the
+        copy stream; `after`: an event of the step during which it travels."""
+        s = i % 2
         lay = HostLayout(w, shapes, with_positions=args.rope)
-        # a2: plan (host); one asynchronous upload of the plan and the readout rows
         extra = np.concatenate([lay.readout, lay.position_ids]) if args.rope else lay.readout
-        plan = planner.plan(*lay.plan_args(), w.hq, w.hkv, w.head_dim, ws_plan, stream=sp,
-                            extra=extra)
-        if times is not None:
-            times["a0"].record(stream)
+        with torch.cuda.stream(copy_stream):
+            if after is not None:
+                copy_stream.wait_event(after)
+            if used[s] is not None:
+                copy_stream.wait_event(used[s])
+            plans[i] = planner.plan(*lay.plan_args(), w.hq, w.hkv, w.head_dim, ws_plans[s],
+                                    stream=copy_stream.cuda_stream, extra=extra)
+            uploaded[s].record(copy_stream)
+
+    def step(i, t):
+        """Step i between the events t["st"] (recorded by the caller) and
+        t["s1"]. Its plan arrived during step i-1; the plan of step i+1 is
+        uploaded during this one, and the step ends only once that upload has
+        landed, so every copy lies inside a timed step."""
+        s = i % 2
+        plan = plans.pop(i)
+        stream.wait_event(uploaded[s])
+        if "a0" in t:
+            t["a0"].record(stream)
         # (with --rope) rotary embedding of Q and K at the reused position ids
         if args.rope:
-            lib.mis_rope_qk(q, k, qr, kr, pos_dev, stream=sp)
-            if times is not None:
-                times["r1"].record(stream)
+            lib.mis_rope_qk(q, k, qr, kr, pos_devs[s], stream=sp)
+            if "r1" in t:
+                t["r1"].record(stream)
         # a3: MIS attention
         lib.mis_attention_fwd_plan(plan, qr, kr, v, o, None, sp)
-        if times is not None:
-            times["a1"].record(stream)
+        if "a1" in t:
+            t["a1"].record(stream)
         # a4-a6: gather + LM head + full-vocab LSE + label read-out
-        lib.mis_label_scores(hidden, w_lm, delim_dev, labels, out, None, ws_score, stream=sp)
-        if times is not None:
-            times["s1"].record(stream)
+        lib.mis_label_scores(hidden, w_lm, delim_devs[s], labels, out, None, ws_score, stream=sp)
+        done = torch.cuda.Event()
+        done.record(stream)
+        used[s] = done
+        if "s1" in t and "a0" in t:
+            t["s0"].record(stream)             # end of this step's kernels
+        enqueue_plan(i + 1, after=t["st"])
+        stream.wait_event(uploaded[(i + 1) % 2])
+        t["s1"].record(stream)
         plan.destroy()
 
     with torch.cuda.stream(stream):
+        n = 0
+        enqueue_plan(0)
         for _ in range(args.warmup):
             flush()
-            step()
+            t = {"st": ev(), "s1": ev()}
+            t["st"].record(stream)
+            step(n, t)
+            n += 1
         torch.cuda.synchronize()
-        if lib.mis_get_device_status(ws_plan, sp) or lib.mis_get_device_status(ws_score, sp):
+        if any(lib.mis_get_device_status(wp, sp) for wp in ws_plans) or \
+                lib.mis_get_device_status(ws_score, sp):
             raise RuntimeError("device status not ok after warm-up")
 
         recs, split_recs = [], []
@@ -271,8 +307,8 @@ def run_ours(args, rank, world, dist):
                 flush()                              # L2 eviction between timed steps (untimed)
                 t = {"st": ev(), "s1": ev()}
                 t["st"].record(stream)
-                step()
-                t["s1"].record(stream)
+                step(n, t)
+                n += 1
                 recs.append(t)
             torch.cuda.synchronize()
             if dist is not None:
@@ -281,17 +317,20 @@ def run_ours(args, rank, world, dist):
             # with events between the calls
             for _ in range(args.steps):
                 flush()
-                t = {"st": ev(), "a0": ev(), "r1": ev(), "a1": ev(), "s1": ev()}
+                t = {"st": ev(), "a0": ev(), "r1": ev(), "a1": ev(), "s0": ev(), "s1": ev()}
                 t["st"].record(stream)
-                step(t)
+                step(n, t)
+                n += 1
                 split_recs.append(t)
             torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
+    for pl in plans.values():
+        pl.destroy()
     step_ms = [r["st"].elapsed_time(r["s1"]) for r in recs]
     attn_ms = [r["r1" if args.rope else "a0"].elapsed_time(r["a1"]) for r in split_recs]
     rope_ms = [r["a0"].elapsed_time(r["r1"]) for r in split_recs] if args.rope else []
-    score_ms = [r["a1"].elapsed_time(r["s1"]) for r in split_recs]
+    score_ms = [r["a1"].elapsed_time(r["s0"]) for r in split_recs]
     split_ms = [r["st"].elapsed_time(r["s1"]) for r in split_recs]
     total_ms = float(sum(step_ms))
     total_ms = max_over_ranks(total_ms, dist, dev)
@@ -300,7 +339,8 @@ def run_ours(args, rank, world, dist):
 
     # correctness guard: the timed outputs are finite and the device status clean
     torch.cuda.synchronize()
-    assert lib.mis_get_device_status(ws_plan, sp) == 0 and lib.mis_get_device_status(ws_score, sp) == 0
+    assert all(lib.mis_get_device_status(wp, sp) == 0 for wp in ws_plans)
+    assert lib.mis_get_device_status(ws_score, sp) == 0
     assert bool(torch.isfinite(out).all())
 
     peaks, peak_src = load_peaks()
@@ -343,6 +383,8 @@ def run_ours(args, rank, world, dist):
                    "items": M, "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim,
                    "d_model": w.d_model, "vocab": w.vocab, "labels": K,
                    "l2": "evicted between timed steps (256 MB write, then 256 MB read; untimed)",
+                   "plan": "host layout and plan every step; the upload of step i+1's plan and "
+                           "readout rows overlaps step i, which ends only once it has landed",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "attention": {"ms": round(t_attn * 1e3, 4), "useful_tflops": round(attn_tflops, 1),

@@ -153,7 +153,22 @@ mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
     fence_mbar_init();
     fence_proxy_async();
   }
-  if (warp == 0 && lane == 0) { tma_prefetch_desc(&amap); tma_prefetch_desc(&wmap); }
+  const int total_steps = nt * nkb;
+  // W_lm is not written by the gather kernel this grid depends on, and every
+  // grid before the gather had completed when the gather let this launch
+  // start: the first stages' W_lm tiles load while the gather finishes. Only
+  // the readout-row tiles wait for it.
+  const int pre = min(kStages, total_steps);
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&amap);
+    tma_prefetch_desc(&wmap);
+    for (int step = 0; step < pre; ++step) {
+      const int t = v_first + step / nkb, kb = step % nkb;
+      mbar_expect_tx(bar(bF + step), kBBytes);
+      tma_load_2d(smem_u32(smem + step * kStageBytes + kABytes), &wmap, bar(bF + step),
+                  kb * kKStep, t * kVocabTile);
+    }
+  }
   if (warp == 1 && nt > 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
@@ -166,11 +181,15 @@ mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
   if (nt <= 0) return;
   const uint32_t tmem = *tmem_slot;
   if (*skip_flag) {                       // another block already gave up
+    if (threadIdx.x == 0)                 // the early W_lm copies land before the block exits
+      for (int step = 0; step < pre; ++step) {
+        mbar_arrive(bar(bF + step));
+        wait_drain(bar(bF + step), 0);
+      }
     if (warp == 1) tmem_dealloc(tmem, 512);
     return;
   }
   const Waiter W{abort_flag, p.status, p.wait_ns};
-  const int total_steps = nt * nkb;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -181,9 +200,14 @@ mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
         const int t = v_first + step / nkb, kb = step % nkb;
         uint8_t* sA = smem + st * kStageBytes;
         uint8_t* sB = sA + kABytes;
-        mbar_arrive_expect_tx(bar(bF + st), kStageBytes);
-        tma_load_2d(smem_u32(sA), &amap, bar(bF + st), kb * kKStep, mt * kItemTile);
-        tma_load_2d(smem_u32(sB), &wmap, bar(bF + st), kb * kKStep, t * kVocabTile);
+        if (step < pre) {                 // W_lm tile already on its way
+          mbar_arrive_expect_tx(bar(bF + st), kABytes);
+          tma_load_2d(smem_u32(sA), &amap, bar(bF + st), kb * kKStep, mt * kItemTile);
+        } else {
+          mbar_arrive_expect_tx(bar(bF + st), kStageBytes);
+          tma_load_2d(smem_u32(sA), &amap, bar(bF + st), kb * kKStep, mt * kItemTile);
+          tma_load_2d(smem_u32(sB), &wmap, bar(bF + st), kb * kKStep, t * kVocabTile);
+        }
         issued = step + 1;
       }
       for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
