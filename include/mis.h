@@ -332,6 +332,11 @@ mis_status_t mis_rope_qk(const void* q, const void* k, void* q_out, void* k_out,
  * Workspace: device, 256-byte aligned, >= mis_label_scores_workspace_size().
  * A readout row outside [0, T) sets MIS_ERR_DEVICE_INDEX in the workspace
  * status and scores a zero hidden row instead.
+ * W_lm is treated as a weight: the LM-head kernel starts reading it (into
+ * shared memory and L2) while the work enqueued on the stream before this
+ * call is still finishing, so that work must not write W_lm (write it in
+ * an earlier, completed step, or synchronise before the call). `hidden` and
+ * `delim_positions` are read only after all earlier stream work completed.
  * ------------------------------------------------------------------------ */
 size_t mis_label_scores_workspace_size(int32_t M, int32_t d, int32_t V, int32_t K);
 

@@ -79,6 +79,10 @@ ScoreLayout score_layout(int32_t M, int32_t d, int32_t V, int32_t K) {
 
 struct ScoreParams {
   int32_t M, V, K, n_vtiles, tiles_per_chunk, n_chunks, n_kb;
+  int32_t dynamic;         // one item tile: blocks take vocabulary tiles from a counter
+  uint32_t* ctr;           // that counter (a status word, cleared by the gather kernel)
+  const uint8_t* w_lm;     // W_lm rows, for the L2 prefetch
+  uint32_t pf_bytes;       // W_lm bytes of its range each block prefetches into L2 before its wait
   int32_t labels[16];
   float* part;        // [m_pad][n_chunks][2] = (max in log2 units, sum of 2^(z*log2e - max))
   float* zlab;        // [m_pad][K] label logits
@@ -92,17 +96,21 @@ struct ScoreParams {
 // Also starts the call's device status: block 0 clears the status words (no
 // other block of this launch writes them; an out-of-range row is recorded in
 // bad[] and raised by the combine kernel, which runs after every block here).
+// It lets the LM-head kernel launch at once, before its own wait: the LM-head
+// kernel reads only W_lm before its griddepcontrol.wait, which waits for this
+// grid and so for everything before it.
 __global__ void __launch_bounds__(128)
 mis_gather_rows_kernel(const __nv_bfloat16* __restrict__ hidden, int64_t stride, int32_t T,
                        const int32_t* __restrict__ rows, int32_t M, int32_t d,
                        __nv_bfloat16* __restrict__ out, int32_t* __restrict__ bad,
                        uint32_t* status) {
-  griddep_wait();
   griddep_launch_dependents();
+  griddep_wait();
   const int i = blockIdx.x;
   if (i == 0 && threadIdx.x == 0) {
     status[0] = 0u;
     status[1] = 0u;
+    status[2] = 0u;                                   // the LM head's vocabulary-tile counter
   }
   int32_t r = -1;
   if (i < M) {
@@ -121,55 +129,85 @@ mis_gather_rows_kernel(const __nv_bfloat16* __restrict__ hidden, int64_t stride,
 }
 
 // ----------------------------------------------------------------- partial
+// Vocabulary tiles per block: a fixed run of tiles_per_chunk tiles (grid
+// (item tiles, chunks)), or, with one item tile, tiles taken from a global
+// counter (grid (1, G), G <= SMs): block b starts with tile b and then takes
+// G + counter++ until the tiles run out, so blocks that stream faster take
+// more tiles and all finish together. The producer hands each tile index to
+// the MMA thread and the epilogue warps through a ring in shared memory
+// (index -1 ends the block's work).
+constexpr int kRing = 4;
+
 __global__ void __launch_bounds__(256, 1)
 mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
                          const __grid_constant__ CUtensorMap wmap, const ScoreParams p) {
   griddep_launch_dependents();
   constexpr int bF = 0, bE = kStages, bAF = 2 * kStages, bAE = bAF + 2, bDR = bAE + 2,
-                nBar = bDR + 1;
+                bTF = bDR + 1, bTE = bTF + kRing, nBar = bTE + kRing;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kData);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + nBar);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile uint32_t* skip_flag = tmem_slot + 2;
+  volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(tmem_slot + 4);   // kRing entries
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x;
   const int chunk = blockIdx.y;
-  const int v_first = chunk * p.tiles_per_chunk;
-  const int v_last = min(v_first + p.tiles_per_chunk, p.n_vtiles);
-  const int nt = v_last - v_first;
+  const bool dyn = p.dynamic != 0;
+  const int G = (int)gridDim.y;
+  const int v_first = dyn ? chunk : chunk * p.tiles_per_chunk;   // the block's first tile
+  const int v_last = dyn ? p.n_vtiles : min(v_first + p.tiles_per_chunk, p.n_vtiles);
+  const bool has_work = v_first < v_last;
   const int nkb = p.n_kb;
 
   // prologue (shared memory and tensor memory only) overlaps the previous
-  // kernel in the stream; global memory is read after griddepcontrol.wait
+  // kernel in the stream; global memory other than W_lm is read after
+  // griddepcontrol.wait
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int s = 0; s < kStages; ++s) { mbar_init(bar(bF + s), 1); mbar_init(bar(bE + s), 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(bar(bAF + s), 1); mbar_init(bar(bAE + s), 128); }
     mbar_init(bar(bDR), 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(bar(bTF + s), 1);
+      mbar_init(bar(bTE + s), 5);                       // the MMA thread and 4 epilogue warps
+    }
     fence_mbar_init();
     fence_proxy_async();
   }
-  const int total_steps = nt * nkb;
-  // W_lm is not written by the gather kernel this grid depends on, and every
-  // grid before the gather had completed when the gather let this launch
-  // start: the first stages' W_lm tiles load while the gather finishes. Only
-  // the readout-row tiles wait for it.
-  const int pre = min(kStages, total_steps);
+  // W_lm is a weight: the stream work before this call does not write it (a
+  // documented rule of mis_label_scores), so it is read before
+  // griddepcontrol.wait. The gather kernel lets this grid launch as soon as
+  // its blocks start, so blocks start here while the kernels before the call
+  // (e.g. the attention layer) drain: the first stages of the block's first
+  // W_lm tile load into shared memory and the next part of that tile into L2
+  // while HBM is otherwise idle. Only the readout-row tiles wait for the
+  // gather.
+  const int pre = has_work ? min(kStages, nkb) : 0;
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&amap);
     tma_prefetch_desc(&wmap);
     for (int step = 0; step < pre; ++step) {
-      const int t = v_first + step / nkb, kb = step % nkb;
       mbar_expect_tx(bar(bF + step), kBBytes);
       tma_load_2d(smem_u32(smem + step * kStageBytes + kABytes), &wmap, bar(bF + step),
-                  kb * kKStep, t * kVocabTile);
+                  step * kKStep, v_first * kVocabTile);
+    }
+    if (p.pf_bytes && has_work && blockIdx.x == 0) {
+      // the rows of a run of tiles are one contiguous range of W_lm
+      const size_t row_bytes = (size_t)nkb * kKStep * 2;
+      const size_t v0 = (size_t)v_first * kVocabTile;
+      const size_t v1 = min((size_t)(dyn ? v_first + 1 : v_last) * kVocabTile, (size_t)p.V);
+      const size_t range = (v1 - v0) * row_bytes;
+      const uint8_t* base = p.w_lm + v0 * row_bytes;
+      const size_t n = min((size_t)p.pf_bytes, range) & ~(size_t)15;
+      for (size_t off = 0; off < n; off += 65536)
+        bulk_prefetch_l2(base + off, (uint32_t)min((size_t)65536, n - off));
     }
   }
-  if (warp == 1 && nt > 0) {
+  if (warp == 1 && has_work) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -178,7 +216,7 @@ mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (nt <= 0) return;
+  if (!has_work) return;
   const uint32_t tmem = *tmem_slot;
   if (*skip_flag) {                       // another block already gave up
     if (threadIdx.x == 0)                 // the early W_lm copies land before the block exits
@@ -193,22 +231,40 @@ mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
 
   if (warp == 0) {
     if (lane == 0) {
-      int issued = 0;
-      for (int step = 0; step < total_steps; ++step) {
-        const int st = step % kStages;
-        if (step >= kStages && !wait(bar(bE + st), ((step / kStages) - 1) & 1, W, 0x100)) break;
-        const int t = v_first + step / nkb, kb = step % nkb;
-        uint8_t* sA = smem + st * kStageBytes;
-        uint8_t* sB = sA + kABytes;
-        if (step < pre) {                 // W_lm tile already on its way
-          mbar_arrive_expect_tx(bar(bF + st), kABytes);
-          tma_load_2d(smem_u32(sA), &amap, bar(bF + st), kb * kKStep, mt * kItemTile);
-        } else {
-          mbar_arrive_expect_tx(bar(bF + st), kStageBytes);
-          tma_load_2d(smem_u32(sA), &amap, bar(bF + st), kb * kKStep, mt * kItemTile);
-          tma_load_2d(smem_u32(sB), &wmap, bar(bF + st), kb * kKStep, t * kVocabTile);
+      int issued = 0, step = 0;
+      int t = v_first;
+      // the tile after the current one, asked for one tile ahead (the
+      // counter's round trip hides behind the current tile's loads)
+      int t_next = dyn ? G + (int)atomicAdd(p.ctr, 1u) : v_first + 1;
+      for (int j = 0;; ++j) {
+        const int slot = j % kRing;
+        if (j >= kRing && !wait(bar(bTE + slot), ((j / kRing) - 1) & 1, W, 0x080)) break;
+        const bool valid = t < v_last;
+        ring[slot] = valid ? t : -1;
+        mbar_arrive(bar(bTF + slot));
+        if (!valid) break;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb, ++step) {
+          const int st = step % kStages;
+          if (step >= kStages && !wait(bar(bE + st), ((step / kStages) - 1) & 1, W, 0x100)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sA = smem + st * kStageBytes;
+          uint8_t* sB = sA + kABytes;
+          if (step < pre) {               // W_lm tile already on its way
+            mbar_arrive_expect_tx(bar(bF + st), kABytes);
+            tma_load_2d(smem_u32(sA), &amap, bar(bF + st), kb * kKStep, mt * kItemTile);
+          } else {
+            mbar_arrive_expect_tx(bar(bF + st), kStageBytes);
+            tma_load_2d(smem_u32(sA), &amap, bar(bF + st), kb * kKStep, mt * kItemTile);
+            tma_load_2d(smem_u32(sB), &wmap, bar(bF + st), kb * kKStep, t * kVocabTile);
+          }
+          issued = step + 1;
         }
-        issued = step + 1;
+        if (!ok) break;
+        t = t_next;
+        if (t < v_last) t_next = dyn ? G + (int)atomicAdd(p.ctr, 1u) : t + 1;
       }
       for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
         wait_drain(bar(bF + i % kStages), (i / kStages) & 1);
@@ -218,13 +274,18 @@ mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
       constexpr uint32_t idesc = idesc_bf16(kItemTile, kVocabTile, false);
       bool ok = true;
       if (p.stall) ok = wait(bar(bDR), 0, W, 0x7ff);   // nothing arrives before the drain
-      for (int ti = 0; ok && ti < nt; ++ti) {
-        const int buf = ti & 1;
-        if (ti >= 2 && !wait(bar(bAE + buf), ((ti >> 1) - 1) & 1, W, 0x200)) break;
+      for (int j = 0; ok; ++j) {
+        const int slot = j % kRing;
+        if (!wait(bar(bTF + slot), (j / kRing) & 1, W, 0x180)) break;
+        const int t = ring[slot];
+        mbar_arrive(bar(bTE + slot));
+        if (t < 0) break;
+        const int buf = j & 1;
+        if (j >= 2 && !wait(bar(bAE + buf), ((j >> 1) - 1) & 1, W, 0x200)) break;
         tc_fence_after();
         const uint32_t dacc = tmem + buf * kVocabTile;
         for (int kb = 0; kb < nkb; ++kb) {
-          const int step = ti * nkb + kb;
+          const int step = j * nkb + kb;
           const int st = step % kStages;
           if (!wait(bar(bF + st), (step / kStages) & 1, W, 0x300)) { ok = false; break; }
           tc_fence_after();
@@ -248,13 +309,21 @@ mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
     const uint32_t tl = tmem + ((uint32_t)(sw * 32) << 16);
     float m2 = -INFINITY, s = 0.f;
     bool ok = true;
-    for (int ti = 0; ti < nt; ++ti) {
-      const int buf = ti & 1;
-      ok = wait(bar(bAF + buf), (ti >> 1) & 1, W, 0x400);
+    for (int j = 0;; ++j) {
+      const int slot = j % kRing;
+      ok = wait(bar(bTF + slot), (j / kRing) & 1, W, 0x380);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const int t = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(bTE + slot));
+      if (t < 0) break;
+      const int buf = j & 1;
+      ok = wait(bar(bAF + buf), (j >> 1) & 1, W, 0x400);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const int v0 = (v_first + ti) * kVocabTile;
+      const int v0 = t * kVocabTile;
       const uint32_t tacc = tl + buf * kVocabTile;
 #pragma unroll 1
       for (int c = 0; c < kVocabTile / 32; ++c) {
@@ -410,12 +479,31 @@ mis_status_t launch_score(const ScoreArgs& a, void* stream) {
   if (!ok) return MIS_ERR_CUDA;
 
   const int n_mtiles = L.m_pad / kItemTile;
+  const int sms = num_sms();
   ScoreParams p;
   p.M = a.M; p.V = a.V; p.K = a.K;
   p.n_vtiles = L.n_vtiles;
-  p.tiles_per_chunk = pick_tiles_per_chunk(n_mtiles, L.n_vtiles, num_sms());
-  p.n_chunks = (L.n_vtiles + p.tiles_per_chunk - 1) / p.tiles_per_chunk;
+  // one item tile and more vocabulary tiles than SMs: HBM-bound on W_lm; the
+  // tiles go out from a counter so that every SM streams until the end.
+  // Otherwise fixed runs of tiles, item tiles side by side in the grid so the
+  // blocks sharing a W_lm tile run together and read it once through L2.
+  p.dynamic = (n_mtiles == 1 && L.n_vtiles > sms) ? 1 : 0;
+  p.ctr = status + 2;
+  p.tiles_per_chunk = p.dynamic ? 0 : pick_tiles_per_chunk(n_mtiles, L.n_vtiles, sms);
+  p.n_chunks = p.dynamic ? sms : (L.n_vtiles + p.tiles_per_chunk - 1) / p.tiles_per_chunk;
   p.n_kb = a.d / kKStep;
+  p.w_lm = static_cast<const uint8_t*>(a.w_lm);
+  // L2 prefetch of W_lm before the wait: only when the whole grid is one wave
+  // (later waves start after the previous kernel anyway, where a prefetch
+  // would only compete with the stream), about 32 MB in all, a quarter of L2
+  {
+    const int64_t blocks = (int64_t)n_mtiles * p.n_chunks;
+    p.pf_bytes = 0;
+    if (blocks <= sms) {
+      const size_t per = ((size_t)32 << 20) / (size_t)p.n_chunks;
+      p.pf_bytes = (uint32_t)std::min<size_t>(per & ~(size_t)65535, (size_t)1 << 30);
+    }
+  }
   for (int l = 0; l < 16; ++l) p.labels[l] = l < a.K ? a.labels[l] : -1;
   p.part = reinterpret_cast<float*>(ws + L.part);
   p.zlab = reinterpret_cast<float*>(ws + L.zlab);

@@ -45,6 +45,11 @@ def test_tiny_workload():
     (128, 512, 2048, [5, 5, 2047, 1000]),
     (129, 128, 777, list(range(16))),
     (300, 1024, 5000, [1234, 4321]),
+    # one item tile and more vocabulary tiles than SMs: tiles go out from a
+    # counter (ragged last tile, labels in the first and last tiles)
+    (1, 64, 60000, [59999, 0]),
+    (128, 128, 50001, [50000, 3, 25000]),
+    (77, 512, 80000, [1, 79999]),
 ])
 def test_random_cases(M, d, V, labels):
     g = torch.Generator().manual_seed(M * 7 + d)
