@@ -209,6 +209,7 @@ mis_status_t create_plan(const Desc* desc, Build build, void* workspace, size_t 
     put(p.off_seg, p.seg_start.data(), p.seg_start.size() * sizeof(int32_t));
     put(p.off_work, p.work.data(), p.work.size() * sizeof(WorkItem));
     put(p.off_klist, p.klist.data(), p.klist.size() * sizeof(uint32_t));
+    put(p.off_order, p.order.data(), p.order.size() * sizeof(int32_t));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     if (cudaMemsetAsync(ws, 0, kStatusBytes, s) != cudaSuccess ||
@@ -336,6 +337,7 @@ mis_status_t mis_planner_plan(mis_planner_t pl, const mis_attn_desc* desc, void*
     put(p.off_seg, p.seg_start.data(), p.seg_start.size() * sizeof(int32_t));
     put(p.off_work, p.work.data(), p.work.size() * sizeof(WorkItem));
     put(p.off_klist, p.klist.data(), p.klist.size() * sizeof(uint32_t));
+    put(p.off_order, p.order.data(), p.order.size() * sizeof(int32_t));
     put(p.total, extra_host, extra_bytes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(workspace, img, n, cudaMemcpyHostToDevice, s) != cudaSuccess ||

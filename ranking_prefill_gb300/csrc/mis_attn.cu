@@ -108,6 +108,8 @@ struct AttnParams {
   const WorkItem* units;  // query tiles, longest first
   const uint32_t* klist;
   int32_t n_units;        // query tiles
+  const int32_t* order;   // or null: the unit at each walk position (-1: none), see unit_at
+  int32_t n_walk;         // walk positions (units in all when there is no order)
   __nv_bfloat16* o;
   float* lse;
   int64_t o_stride;
@@ -121,13 +123,17 @@ struct AttnParams {
   uint32_t stall;         // failure injection: wait on a barrier nothing arrives on
 };
 
-// Unit handled by this block in pass kk over the longest-first unit list:
-// passes alternate direction (snake order), so every block gets a long and a
-// short unit from each pair of passes; -1 past the end.
-__device__ __forceinline__ int unit_at(int kk, int total) {
+// Unit handled by this block in pass kk: walk position kk * G + c, passes
+// alternating direction (snake order), so over the longest-first unit list
+// every block gets a long and a short unit from each pair of passes. A plan
+// may instead give the unit at every walk position (a greedy assignment in
+// list order that balances the blocks better, e.g. over many requests whose
+// units are ordered request by request); -1 = none at that position.
+__device__ __forceinline__ int unit_at(const AttnParams& p, int kk) {
   const int G = gridDim.x, c = blockIdx.x;
-  const int u = kk * G + ((kk & 1) ? (G - 1 - c) : c);
-  return u < total ? u : -1;
+  const int pos = kk * G + ((kk & 1) ? (G - 1 - c) : c);
+  if (pos >= p.n_walk) return -1;
+  return p.order ? p.order[pos] : pos;
 }
 
 template <int D, bool kSplit>
@@ -171,7 +177,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   constexpr bool split = kSplit;
   constexpr int nh = split ? 1 : 2;                    // Q tiles (heads) per unit
   const int n_hg = p.n_head_groups;
-  const int total = p.n_units * n_hg;                  // unit u: p.units[u / n_hg], head group u % n_hg
+  const int total = p.n_walk;                          // walk positions; unit u: p.units[u / n_hg], head group u % n_hg
 
   // prologue (shared memory and tensor memory only) overlaps the previous
   // kernel in the stream; global memory is read after griddepcontrol.wait
@@ -227,7 +233,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
         int gk = 0, lu = 0, q_issued = 0, k_issued = 0, v_issued = 0;
         bool ok = true;
         for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {
-          const int u = unit_at(kk, total);
+          const int u = unit_at(p, kk);
           if (u < 0) continue;
           const WorkItem un = p.units[u / n_hg];
           const int h0 = (u % n_hg) * nh, g = h0 / p.group;
@@ -303,7 +309,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
         // c0, c1: S products issued so far for each stream (the phase of SF_t / PF_t)
         int gk = 0, lu = 0, c0 = 0, c1 = 0;
         for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {
-          const int u = unit_at(kk, total);
+          const int u = unit_at(p, kk);
           if (u < 0) continue;
           const int nk = p.units[u / n_hg].nk;
           if (!(ok = wait<true>(bar(bQF), lu & 1, W, 0x200))) break;
@@ -391,7 +397,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
     int lu = 0, cs = 0;                                 // cs: S tiles of this stream so far
     bool ok = true;
     for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {
-      const int u = unit_at(kk, total);
+      const int u = unit_at(p, kk);
       if (u < 0) continue;
       const WorkItem un = p.units[u / n_hg];
       const ReqInfo R = p.req[un.req];
@@ -513,7 +519,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
     int lu = 0;
     bool ok = true;
     for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {
-      const int u = unit_at(kk, total);
+      const int u = unit_at(p, kk);
       if (u < 0) continue;
       const WorkItem un = p.units[u / n_hg];
       const ReqInfo R = p.req[un.req];
@@ -718,6 +724,7 @@ mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
   prm.units = reinterpret_cast<const WorkItem*>(ws + pl.off_work);
   prm.klist = reinterpret_cast<const uint32_t*>(ws + pl.off_klist);
   prm.n_units = (int32_t)pl.work.size();
+  prm.order = pl.order.empty() ? nullptr : reinterpret_cast<const int32_t*>(ws + pl.off_order);
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
   prm.o_stride = os;
@@ -741,6 +748,7 @@ mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
   if (!kernel_attr_once(reinterpret_cast<const void*>(kern), C::kSmem)) return MIS_ERR_CUDA;
   const int64_t total = (int64_t)pl.work.size() * pl.n_head_groups;
   if (total > 0x7fffffff) return MIS_ERR_UNSUPPORTED;
+  prm.n_walk = pl.order.empty() ? (int32_t)total : (int32_t)pl.order.size();
   dim3 grid((unsigned)std::min<int64_t>(total, num_sms()));
   return launch_pdl(kern, grid, dim3(kThreads), C::kSmem, st, qm, km, vm, om, kcm, vcm, prm) ==
                  cudaSuccess

@@ -54,6 +54,10 @@ struct HostPlan {
   bool split = false;              // split schedule (one head per unit, key tiles alternate
                                    // between the block's two softmax streams)
   int32_t n_head_groups = 1;       // units per query tile: Hq / 2 (pair) or Hq (split)
+  // the unit at each walk position of the kernel's blocks (pass kk, block c
+  // at kk * G + c, odd passes reversed), -1 for none; empty: position = unit
+  std::vector<int32_t> order;
+  size_t off_order = 0;
   void* workspace = nullptr;       // device base, set by mis_plan_create
   bool status_clear = false;       // the upload zeroed the status words; the
                                    // first launch need not clear them again

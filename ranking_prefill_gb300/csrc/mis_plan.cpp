@@ -15,7 +15,9 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <functional>
 #include <limits>
+#include <queue>
 
 #include "mis_internal.h"
 
@@ -204,6 +206,49 @@ mis_status_t finish_plan(HostPlan* p, std::vector<Tmp>& tmp, int32_t B, int32_t 
   p->stats.schedule = split ? MIS_SCHEDULE_SPLIT : MIS_SCHEDULE_PAIR;
   p->stats.n_units = (int64_t)p->work.size() * p->n_head_groups;
 
+  // ---- unit order: the snake walk over the list, or, when the blocks come
+  // out clearly better balanced, a greedy assignment in list order (each unit
+  // to the block with the least work so far, ties to the lower index) laid
+  // out on the same walk positions. Units keep their list order inside every
+  // block, and blocks that run together still work on neighbouring units of
+  // the list, so a request's K/V tiles are still shared through L2.
+  p->order.clear();
+  {
+    const int64_t n_units = p->stats.n_units;
+    const int64_t G = std::min<int64_t>(n_units, num_sms());
+    if (n_units > G && G > 0 && n_units < ((int64_t)1 << 30)) {
+      std::vector<double> cost((size_t)n_units);
+      for (int64_t u = 0; u < n_units; ++u) {
+        const Tmp& w = tmp[(size_t)(u / p->n_head_groups)];
+        cost[(size_t)u] = (split ? std::max(w.cost_even, w.cost_odd) : w.cost) / 4.0 + kUnitCost;
+      }
+      const double snake = snake_makespan(cost, 1, (int)G);
+      using Slot = std::pair<double, int64_t>;
+      std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+      for (int64_t c = 0; c < G; ++c) heap.push({0.0, c});
+      std::vector<std::vector<int32_t>> lists((size_t)G);
+      double greedy = 0.0;
+      for (int64_t u = 0; u < n_units; ++u) {
+        Slot s = heap.top();
+        heap.pop();
+        s.first += cost[(size_t)u];
+        greedy = std::max(greedy, s.first);
+        lists[(size_t)s.second].push_back((int32_t)u);
+        heap.push(s);
+      }
+      if (greedy < 0.99 * snake) {
+        size_t passes = 0;
+        for (const auto& l : lists) passes = std::max(passes, l.size());
+        p->order.assign(passes * (size_t)G, -1);
+        for (int64_t c = 0; c < G; ++c)
+          for (size_t kk = 0; kk < lists[(size_t)c].size(); ++kk) {
+            const int64_t pos = (int64_t)kk * G + ((kk & 1) ? (G - 1 - c) : c);
+            p->order[(size_t)pos] = lists[(size_t)c][kk];
+          }
+      }
+    }
+  }
+
   p->stats.n_qtiles = (int64_t)p->work.size();
   p->stats.n_tiles = p->stats.n_full + p->stats.n_partial;
   p->stats.n_causal_tiles = causal_tiles;
@@ -215,6 +260,7 @@ mis_status_t finish_plan(HostPlan* p, std::vector<Tmp>& tmp, int32_t B, int32_t 
   p->off_seg = off;   off = align_up(off + sizeof(int32_t) * (size_t)T, 256);
   p->off_work = off;  off = align_up(off + sizeof(WorkItem) * p->work.size(), 256);
   p->off_klist = off; off = align_up(off + sizeof(uint32_t) * std::max<size_t>(p->klist.size(), 1), 256);
+  p->off_order = off; off = align_up(off + sizeof(int32_t) * p->order.size(), 256);
   p->total = off;
   p->stats.workspace_bytes = (int64_t)off;
   return MIS_OK;
