@@ -174,3 +174,48 @@ def test_one_workspace_for_calls_of_different_shapes_and_after_a_timeout():
         lib.mis_set_wait_limit_ns(old)
     for c in reversed(cases):
         check(*c)
+
+
+def test_counter_fed_tiles_across_back_to_back_calls():
+    # One item tile and more vocabulary tiles than SMs: blocks take tiles from a
+    # counter in the workspace status words, which the call's first kernel
+    # zeroes. Three calls enqueued back to back on one workspace (no sync in
+    # between), then a call whose waits ran out, then a clean call again: each
+    # clean call scores every vocabulary tile exactly once.
+    g = torch.Generator().manual_seed(21)
+    T, d, V = 400, 256, 60001
+    hidden = torch.randn(T, d, generator=g).to(torch.bfloat16)
+    w = (torch.randn(V, d, generator=g) * 0.05).to(torch.bfloat16)
+    dh, dw = hidden.cuda(), w.cuda()
+    cases = [(np.random.default_rng(s).choice(T, m, replace=False).astype(np.int32), lb)
+             for s, m, lb in [(1, 100, [0, 60000]), (2, 128, [777, 30000, 59999]), (3, 1, [5])]]
+    ws = torch.zeros(max(lib.mis_label_scores_workspace_size(len(r), d, V, len(lb)) for r, lb in cases),
+                     dtype=torch.uint8, device="cuda")
+    outs = []
+    for rows, lb in cases:
+        out = torch.empty(len(rows), len(lb), dtype=torch.float32, device="cuda")
+        lib.mis_label_scores(dh, dw, torch.as_tensor(rows).cuda(), lb, out, None, ws)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert lib.mis_get_device_status(ws) == lib.MIS_OK
+    for (rows, lb), out in zip(cases, outs):
+        lp, _, _ = O.label_scores(f64(hidden), f64(w), rows, lb)
+        assert np.abs(f64(out) - lp).max() <= SCORE_TOL
+    old = lib.mis_set_wait_limit_ns(2_000_000)
+    lib.mis_inject_stall(2)
+    try:
+        rows, lb = cases[0]
+        out = torch.empty(len(rows), len(lb), dtype=torch.float32, device="cuda")
+        lib.mis_label_scores(dh, dw, torch.as_tensor(rows).cuda(), lb, out, None, ws)
+        torch.cuda.synchronize()
+        assert lib.mis_get_device_status(ws) == lib.MIS_ERR_DEVICE_TIMEOUT
+    finally:
+        lib.mis_inject_stall(0)
+        lib.mis_set_wait_limit_ns(old)
+    rows, lb = cases[1]
+    out = torch.empty(len(rows), len(lb), dtype=torch.float32, device="cuda")
+    lib.mis_label_scores(dh, dw, torch.as_tensor(rows).cuda(), lb, out, None, ws)
+    torch.cuda.synchronize()
+    assert lib.mis_get_device_status(ws) == lib.MIS_OK
+    lp, _, _ = O.label_scores(f64(hidden), f64(w), rows, lb)
+    assert np.abs(f64(out) - lp).max() <= SCORE_TOL
