@@ -15,9 +15,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
-#include <functional>
 #include <limits>
-#include <queue>
 
 #include "mis_internal.h"
 
@@ -207,11 +205,11 @@ mis_status_t finish_plan(HostPlan* p, std::vector<Tmp>& tmp, int32_t B, int32_t 
   p->stats.n_units = (int64_t)p->work.size() * p->n_head_groups;
 
   // ---- unit order: the snake walk over the list, or, when the blocks come
-  // out clearly better balanced, a greedy assignment in list order (each unit
-  // to the block with the least work so far, ties to the lower index) laid
-  // out on the same walk positions. Units keep their list order inside every
-  // block, and blocks that run together still work on neighbouring units of
-  // the list, so a request's K/V tiles are still shared through L2.
+  // out clearly better balanced, a wave-by-wave longest-processing-time
+  // assignment: pass k still hands out the list's units kG..kG+G-1 (so blocks
+  // that run together work on neighbouring units and share a request's K/V
+  // tiles through L2), but the longest of them go to the blocks with the
+  // least work so far. Laid out on the kernel's walk positions.
   p->order.clear();
   {
     const int64_t n_units = p->stats.n_units;
@@ -223,29 +221,28 @@ mis_status_t finish_plan(HostPlan* p, std::vector<Tmp>& tmp, int32_t B, int32_t 
         cost[(size_t)u] = (split ? std::max(w.cost_even, w.cost_odd) : w.cost) / 4.0 + kUnitCost;
       }
       const double snake = snake_makespan(cost, 1, (int)G);
-      using Slot = std::pair<double, int64_t>;
-      std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-      for (int64_t c = 0; c < G; ++c) heap.push({0.0, c});
-      std::vector<std::vector<int32_t>> lists((size_t)G);
-      double greedy = 0.0;
-      for (int64_t u = 0; u < n_units; ++u) {
-        Slot s = heap.top();
-        heap.pop();
-        s.first += cost[(size_t)u];
-        greedy = std::max(greedy, s.first);
-        lists[(size_t)s.second].push_back((int32_t)u);
-        heap.push(s);
+      const int64_t passes = (n_units + G - 1) / G;
+      std::vector<int32_t> order((size_t)(passes * G), -1);
+      std::vector<double> load((size_t)G, 0.0);
+      std::vector<int32_t> blk((size_t)G), unt;
+      for (int64_t c = 0; c < G; ++c) blk[(size_t)c] = (int32_t)c;
+      for (int64_t kk = 0; kk < passes; ++kk) {
+        const int64_t u0 = kk * G, u1 = std::min(u0 + G, n_units);
+        unt.resize((size_t)(u1 - u0));
+        for (int64_t u = u0; u < u1; ++u) unt[(size_t)(u - u0)] = (int32_t)u;
+        std::stable_sort(unt.begin(), unt.end(),
+                         [&](int32_t a, int32_t b) { return cost[(size_t)a] > cost[(size_t)b]; });
+        std::sort(blk.begin(), blk.end(), [&](int32_t a, int32_t b) {
+          return load[(size_t)a] < load[(size_t)b] || (load[(size_t)a] == load[(size_t)b] && a < b);
+        });
+        for (size_t i = 0; i < unt.size(); ++i) {
+          const int64_t c = blk[i];
+          load[(size_t)c] += cost[(size_t)unt[i]];
+          order[(size_t)(kk * G + ((kk & 1) ? (G - 1 - c) : c))] = unt[i];
+        }
       }
-      if (greedy < 0.99 * snake) {
-        size_t passes = 0;
-        for (const auto& l : lists) passes = std::max(passes, l.size());
-        p->order.assign(passes * (size_t)G, -1);
-        for (int64_t c = 0; c < G; ++c)
-          for (size_t kk = 0; kk < lists[(size_t)c].size(); ++kk) {
-            const int64_t pos = (int64_t)kk * G + ((kk & 1) ? (G - 1 - c) : c);
-            p->order[(size_t)pos] = lists[(size_t)c][kk];
-          }
-      }
+      const double waves = *std::max_element(load.begin(), load.end());
+      if (waves < 0.99 * snake) p->order.swap(order);
     }
   }
 
