@@ -186,6 +186,15 @@ mis_status_t mis_plan_get_stats(mis_plan_t plan, mis_plan_stats* out);
  * k-tile). Writes min(cap, n) quadruples to host_out (may be NULL when cap is
  * 0); *n_out receives n. */
 mis_status_t mis_plan_tile_map(mis_plan_t plan, int32_t* host_out, size_t cap, size_t* n_out);
+/* The attention kernel's unit walk (for inspection and tests): the unit each
+ * walk position hands out, -1 where a block has none. Position kk * G + c
+ * belongs to block c in pass kk (odd passes reversed), G = min(units, SMs);
+ * the plan's unit u is query tile u / g, head group u % g with g = Hq / 2
+ * (pair schedule) or Hq (split). Every unit appears exactly once. Writes
+ * min(cap, n) entries to host_out (may be NULL when cap is 0); *n_out
+ * receives n and *blocks_out (may be NULL) receives G. */
+mis_status_t mis_plan_unit_walk(mis_plan_t plan, int32_t* host_out, size_t cap, size_t* n_out,
+                                int32_t* blocks_out);
 mis_status_t mis_plan_destroy(mis_plan_t plan);
 
 /* Reusable planner for a stream of batches. mis_plan_create() uploads the

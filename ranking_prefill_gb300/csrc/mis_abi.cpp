@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -369,6 +370,19 @@ mis_status_t mis_plan_tile_map(mis_plan_t plan, int32_t* host_out, size_t cap, s
   *n_out = n;
   const size_t w = cap < n ? cap : n;
   if (w) std::memcpy(host_out, tm.data(), w * 4 * sizeof(int32_t));
+  return MIS_OK;
+}
+
+mis_status_t mis_plan_unit_walk(mis_plan_t plan, int32_t* host_out, size_t cap, size_t* n_out,
+                                int32_t* blocks_out) {
+  if (!plan || !n_out || (cap && !host_out)) return MIS_ERR_INVALID_ARG;
+  const HostPlan& p = plan->p;
+  const int64_t units = p.stats.n_units;
+  const size_t n = p.order.empty() ? (size_t)units : p.order.size();
+  *n_out = n;
+  if (blocks_out) *blocks_out = (int32_t)std::min<int64_t>(units, num_sms());
+  const size_t w = cap < n ? cap : n;
+  for (size_t i = 0; i < w; ++i) host_out[i] = p.order.empty() ? (int32_t)i : p.order[i];
   return MIS_OK;
 }
 

@@ -30,7 +30,7 @@ for _v, _n in STATUS.items():
 # every symbol include/mis.h declares
 EXPORTS = ["mis_status_string", "mis_abi_version", "mis_layout_size", "mis_build_layout",
            "mis_plan_workspace_size", "mis_plan_create", "mis_plan_get_stats",
-           "mis_plan_tile_map", "mis_plan_destroy", "mis_attention_fwd_plan",
+           "mis_plan_tile_map", "mis_plan_unit_walk", "mis_plan_destroy", "mis_attention_fwd_plan",
            "mis_attention_fwd", "mis_label_scores_workspace_size", "mis_label_scores",
            "mis_get_device_status", "mis_set_wait_limit_ns", "mis_label_scores_noalloc",
            "mis_inject_stall", "mis_planner_create", "mis_planner_plan", "mis_planner_destroy",
@@ -93,6 +93,7 @@ def load(path: str = LIB_PATH):
         "mis_plan_create": (C.c_int, [C.POINTER(mis_attn_desc), vp, sz, vp, C.POINTER(vp)]),
         "mis_plan_get_stats": (C.c_int, [vp, C.POINTER(mis_plan_stats)]),
         "mis_plan_tile_map": (C.c_int, [vp, i32p, sz, C.POINTER(sz)]),
+        "mis_plan_unit_walk": (C.c_int, [vp, i32p, sz, C.POINTER(sz), C.POINTER(C.c_int32)]),
         "mis_plan_destroy": (C.c_int, [vp]),
         "mis_attention_fwd_plan": (C.c_int, [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, vp]),
         "mis_attention_fwd": (C.c_int, [vp, vp, vp, vp, vp, i64, i64, i64, i64,
@@ -312,6 +313,18 @@ class Plan:
         s = mis_plan_stats()
         _check(self._L.mis_plan_get_stats(self._h, C.byref(s)), "mis_plan_get_stats")
         return s.as_dict()
+
+    def unit_walk(self):
+        """(walk, G): the unit at each walk position of the attention kernel's
+        blocks (-1: none) and the block count G."""
+        n = C.c_size_t()
+        g = C.c_int32()
+        _check(self._L.mis_plan_unit_walk(self._h, None, 0, C.byref(n), C.byref(g)),
+               "mis_plan_unit_walk")
+        out = np.zeros(max(n.value, 1), np.int32)
+        _check(self._L.mis_plan_unit_walk(self._h, _ptr_i32(out), n.value, C.byref(n), C.byref(g)),
+               "mis_plan_unit_walk")
+        return out[:n.value], int(g.value)
 
     def tile_map(self) -> np.ndarray:
         n = C.c_size_t()

@@ -271,3 +271,31 @@ def test_cached_plan_tile_map_and_pairs_bit_exact(L):
         with pytest.raises(lib.MisError) as e:
             mk(**kw)
         assert e.value.status == want, kw
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3-0.6b-layer", "decision-256", "varlen-16"])
+@pytest.mark.parametrize("mode", [lib.SCHEDULE_AUTO, lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT],
+                         ids=["auto", "pair", "split"])
+def test_unit_walk_hands_out_every_unit_once_pass_by_pass(name, mode):
+    # The attention kernel's blocks take walk position kk * G + c in pass kk.
+    # Whatever the order (the snake over the list, or its wave-by-wave
+    # longest-first assignment), every unit is handed out exactly once, and
+    # pass kk hands out exactly the list's units kk * G .. kk * G + G - 1, so
+    # blocks running together work on neighbouring units of the list.
+    w = synth.WORKLOADS[name]
+    s = synth.draw_shapes(w)
+    lay = lib.mis_build_layout(s.prefix_tokens, s.n_items, s.item_lens, with_positions=False)
+    prev = lib.mis_set_schedule(mode)
+    try:
+        p = lib.Plan.host_only(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets,
+                               w.hq, w.hkv, w.head_dim)
+        walk, G = p.unit_walk()
+        n = p.stats()["n_units"]
+    finally:
+        lib.mis_set_schedule(prev)
+    assert G == min(n, G) and G >= 1
+    got = walk[walk >= 0]
+    assert np.array_equal(np.sort(got), np.arange(n))
+    for kk in range((len(walk) + G - 1) // G):
+        part = walk[kk * G:(kk + 1) * G]
+        assert set(part[part >= 0].tolist()) == set(range(kk * G, min((kk + 1) * G, n)))
