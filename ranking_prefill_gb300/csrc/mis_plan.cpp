@@ -115,6 +115,25 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
   // ---- tiles ----
   std::vector<Tmp> tmp;
   int64_t visible = 0, causal_tiles = 0;
+  {
+    // exact sizes first (the same interval arithmetic as below), so the lists
+    // are filled without reallocation
+    size_t n_tiles = 0, n_qt = 0;
+    for (int b = 0; b < B; ++b) {
+      const ReqInfo& R = p->req[b];
+      const int32_t nqt = (R.e0 - R.s0 + kBM - 1) / kBM;
+      n_qt += (size_t)nqt;
+      for (int32_t t = 0; t < nqt; ++t) {
+        const int32_t r0 = R.s0 + t * kBM, r1 = std::min(r0 + kBM, R.e0);
+        const int32_t qb = (std::min(R.pend, r1) - R.s0 + kBN - 1) / kBN;
+        const int32_t ba = (p->seg_start[r0] - R.s0) / kBN, bb = (r1 - 1 - R.s0) / kBN + 1;
+        n_tiles += (size_t)qb + (size_t)std::max(0, bb - std::max(ba, qb));
+      }
+    }
+    tmp.reserve(n_qt);
+    p->klist.reserve(n_tiles);
+    p->tile_map.reserve(4 * n_tiles);
+  }
   for (int b = 0; b < B; ++b) {
     const ReqInfo& R = p->req[b];
     const int32_t L = R.e0 - R.s0;
