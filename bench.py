@@ -602,9 +602,10 @@ def run_comparators(w, shapes, vals, labels, dev, stream, q, k, v, hidden, w_lm,
 
 
 def _prefix_cache(w, lay, labels, dev, stream, flush, q, k, v, hidden, w_lm, t_attn, t_score, M):
-    """The same requests with their prefixes in a K/V cache ("Turbocharging
-    LinkedIn's recommendation systems with SGLang": the in-batch prefix
-    cache and the knock-knock second request). Times the prefix prefill
+    """The same requests with their prefixes in a K/V cache (the in-batch
+    prefix cache of "Scaling LLM-Based Ranking Systems with Prefill-Only
+    Optimization", Components table, and the knock-knock second request of
+    "Turbocharging LinkedIn's recommendation systems with SGLang"). Times the prefix prefill
     (causal attention over each prefix: the first request, which fills the
     cache), the item request (MIS among the items over the cached prefix,
     then scoring) and single-item scoring with the prefix cache (one request

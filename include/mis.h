@@ -243,10 +243,11 @@ mis_status_t mis_attention_fwd(const void* q, const void* k, const void* v, void
 
 /* ------------------------------------------------------------------------
  * Items over a cached prefix: the prefix K/V of each request was computed
- * earlier and kept in a cache buffer ("Turbocharging LinkedIn's
- * recommendation systems with SGLang": the in-batch prefix cache, which
- * reuses query-prefix KV within one forward pass, and the "knock-knock"
- * second request, which appends the items to a prefix prefilled while
+ * earlier and kept in a cache buffer: the in-batch prefix cache of
+ * "Scaling LLM-Based Ranking Systems with Prefill-Only Optimization"
+ * (Components table), which reuses query-prefix KV within one forward
+ * pass, and the knock-knock second request of "Turbocharging LinkedIn's
+ * recommendation systems with SGLang", which appends the items to a prefix prefilled while
  * retrieval ran). The new sequence holds only item sets; each item row sees
  * its request's cached prefix (all of it: the prefix precedes every item
  * token) and its own item causally, as eq. (4) of "From Generation to

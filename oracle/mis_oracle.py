@@ -34,9 +34,10 @@ What it computes, and where each step comes from:
   Scoring" Section 4.1 ("Positional encoding is also adjusted accordingly",
   "Turbocharging ...", section "SGLang changes").
 * ``cached_layout`` / ``attention_cached`` — items scored over a prefix whose
-  K/V was computed earlier and kept in a cache (the "in-batch prefix cache"
-  and the "knock-knock" second request of "Turbocharging LinkedIn's
-  recommendation systems with SGLang"): each item row sees its request's
+  K/V was computed earlier and kept in a cache (the in-batch prefix cache
+  of "Scaling LLM-Based Ranking Systems with Prefill-Only Optimization",
+  Components table, and the knock-knock second request of "Turbocharging
+  LinkedIn's recommendation systems with SGLang"): each item row sees its request's
   cached prefix and its own item causally, as in eq. (4).
 * ``setwise_layout`` — the anchor-based setwise prompt of "Scaling JEV-like
   Decision Models with SGLang" (section "Benchmark: Fused-Choice vs. Setwise

@@ -1,6 +1,7 @@
-"""GPU parity of attention over a cached prefix ("Turbocharging LinkedIn's
-recommendation systems with SGLang": in-batch prefix cache, knock-knock
-second request) against the fp64 oracle, through the C ABI."""
+"""GPU parity of attention over a cached prefix (the in-batch prefix cache of
+"Scaling LLM-Based Ranking Systems with Prefill-Only Optimization", the
+knock-knock second request of "Turbocharging LinkedIn's recommendation
+systems with SGLang") against the fp64 oracle, through the C ABI."""
 import numpy as np
 import pytest
 import torch
