@@ -31,8 +31,9 @@ What it computes, and where each step comes from:
 * ``cost_ratio`` — eq. (5), the prefill-token reduction factor R(N).
 * ``rope`` — rotary position embedding of Q and K at given position ids, the
   step that consumes the reused position ids of "From Generation to
-  Scoring" Section 4.1 ("Positional encoding is also adjusted accordingly",
-  "Turbocharging ...", section "SGLang changes").
+  Scoring" Section 4.1; the SGLang changes of "Turbocharging ..." also
+  adjust the positional encoding so each item sits at its single-item
+  position.
 * ``cached_layout`` / ``attention_cached`` — items scored over a prefix whose
   K/V was computed earlier and kept in a cache (the in-batch prefix cache
   of "Scaling LLM-Based Ranking Systems with Prefill-Only Optimization",
