@@ -168,8 +168,8 @@ size_t mis_plan_workspace_size(const mis_attn_desc* desc);
 /* Validate the descriptor, build the mask-aware tile schedule on the host
  * (per query tile: the key tiles of the prefix plus the band of its own
  * items, each flagged full or partial; fully masked tiles are never listed —
- * "From Generation to Scoring" Section 4.2, "FlashInfer kernels skip fully
- * masked tiles"; "Turbocharging ...", "Implemented skip tiles"), and upload
+ * "From Generation to Scoring" Section 4.2; "Turbocharging ...", section
+ * "FlashInfer changes"), and upload
  * it into `workspace` (device, 256-byte aligned, >= mis_plan_workspace_size
  * bytes) on `stream`. The workspace must stay untouched while the plan is in
  * use. *out receives a host-side handle, freed by mis_plan_destroy().

@@ -9,9 +9,9 @@
 // where lo(j) is the first row of the set holding j (s0 for rows of Q). The
 // planner walks 128-row query tiles and lists only the key tiles that meet
 // one of those intervals for some row of the tile, so fully masked tiles cost
-// neither FLOPs nor bytes (Section 4.2: "the FlashInfer kernels skip fully
-// masked tiles"; "Turbocharging LinkedIn's recommendation systems with
-// SGLang", "Implemented skip tiles for FA2 and FA3 multi-item scoring").
+// neither FLOPs nor bytes (both pages skip tiles with no visible entry:
+// Section 4.2 of "From Generation to Scoring", and "Turbocharging LinkedIn's
+// recommendation systems with SGLang", section "FlashInfer changes").
 #include <algorithm>
 #include <cmath>
 #include <cstring>
