@@ -7,9 +7,9 @@
 // host planner lists, per 128-row query tile, only the 128-key tiles that hold
 // a visible entry and flags the ones that need the element mask, so masked
 // item x item blocks are never loaded or multiplied ("Turbocharging LinkedIn's
-// recommendation systems with SGLang", section "FlashInfer changes"; Section 4.2
-// of the former: attention work O(Lq^2 + N Lq Lbar) instead of the causal
-// O((Lq + N Lbar)^2)).
+// recommendation systems with SGLang", section "FlashInfer changes"; Section
+// 4.2 of "From Generation to Scoring": attention work O(Lq^2 + N Lq Lbar)
+// instead of the causal O((Lq + N Lbar)^2)).
 //
 // Persistent kernel: one block per SM walks the planner's units in
 // longest-first order, snaking over the blocks. A unit is a query tile with
