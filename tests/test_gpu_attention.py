@@ -1,7 +1,8 @@
 """GPU parity of mis_attention_fwd against the fp64 oracle (through the C ABI).
 
 Element-by-element on small and medium layouts (several tiles, ragged tails,
-empty items, D = 64 and 128, GQA 1/2/4, strided rows, varlen batches), on
+empty items, D = 64 and 128, GQA groups 1 to 5 and a lone head, strided
+rows, varlen batches), on
 the full qwen3-0.6b-layer workload, and on seeded row samples of the large
 workloads (rows are independent, so each sampled row is still an exact
 element-by-element check). Tolerances: max-abs 2e-2 on O, 2e-3 on LSE.
@@ -67,6 +68,15 @@ def test_plain_causal_ragged(D, schedule):
     lens = [1, 127, 128, 129, 300, 513]
     s = synth.custom_shapes([L - 1 for L in lens], [0] * len(lens), [])
     check_attention(s, 4, 2, D, 7, causal=True)
+
+
+@pytest.mark.parametrize("hq,hkv,D", [(6, 2, 128), (3, 1, 64), (1, 1, 128), (10, 2, 64)])
+def test_odd_gqa_groups_and_single_head(hq, hkv, D, schedule):
+    # odd groups (3, 5) and a lone head cannot pair two heads on one kv head:
+    # the split schedule runs them whatever the request
+    s = synth.custom_shapes([90, 260], [3, 5], [12, 0, 140, 7, 64, 1, 33, 129])
+    err, st = check_attention(s, hq, hkv, D, 40 + hq)
+    _expect_schedule(st, schedule, hq, hkv)
 
 
 def test_single_item_and_empty_items(schedule):

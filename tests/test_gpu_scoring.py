@@ -1,8 +1,8 @@
 """GPU parity of mis_label_scores against the fp64 oracle (through the C ABI).
 
 Full element-by-element checks on small and medium cases (ragged vocabulary
-tails, item counts around the 128-item tile, d = 64..1024, K = 1..16,
-repeated and edge label ids), the full qwen3-0.6b-layer workload, and
+tails, item counts around the 128-item tile, d = 64..8192, V = 1..151936,
+K = 1..16, repeated and edge label ids), the full qwen3-0.6b-layer workload, and
 seeded item samples of the large ones. Tolerance: max-abs 1e-2 on log-probs
 and on the label-renormalised scores.
 """
@@ -50,6 +50,10 @@ def test_tiny_workload():
     (1, 64, 60000, [59999, 0]),
     (128, 128, 50001, [50000, 3, 25000]),
     (77, 512, 80000, [1, 79999]),
+    # the largest model width (d = 8192: 128 k-blocks per tile) and a
+    # one-token vocabulary (every log-prob is exactly 0)
+    (3, 8192, 700, [0, 699, 350]),
+    (5, 64, 1, [0, 0]),
 ])
 def test_random_cases(M, d, V, labels):
     g = torch.Generator().manual_seed(M * 7 + d)
