@@ -158,7 +158,7 @@ def test_schedules_agree_on_a_long_unit_mix():
     assert (outs[0][1] - outs[1][1]).abs().max().item() <= 1e-4
 
 
-@pytest.mark.parametrize("name", ["8b-large", "decision-256", "varlen-16"])
+@pytest.mark.parametrize("name", ["8b-large", "decision-256", "varlen-16", "prefix12k-50x150"])
 def test_large_workloads_sampled_rows(name, schedule):
     w = synth.WORKLOADS[name]
     s = synth.draw_shapes(w)

@@ -122,7 +122,7 @@ def test_qwen3_layer_full():
     _check(v["hidden"], v["w_lm"], lay.delim_positions, s.label_sets[0].tolist())
 
 
-@pytest.mark.parametrize("name", ["8b-large", "decision-256", "varlen-16"])
+@pytest.mark.parametrize("name", ["8b-large", "decision-256", "varlen-16", "prefix12k-50x150"])
 def test_large_workloads_sampled_items(name):
     w = synth.WORKLOADS[name]
     s = synth.draw_shapes(w)
