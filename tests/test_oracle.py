@@ -114,6 +114,25 @@ def test_mask_matches_set_enumeration_on_all_tiny_layouts():
     assert count > 500
 
 
+def test_mask_matches_set_enumeration_on_sampled_small_layouts():
+    # beyond the exhaustive sweep: 400 seeded layouts with up to 3 requests,
+    # shared sets of up to 8 rows (prefix <= 7 plus its DELIM), up to 4 items
+    # of up to 4 tokens; the interval form, the set enumeration and the
+    # closed-form pair count agree on every one
+    rng = np.random.default_rng(2024)
+    for _ in range(400):
+        B = int(rng.integers(1, 4))
+        ps = rng.integers(0, 8, B).tolist()
+        ns = rng.integers(0, 5, B).tolist()
+        lens = rng.integers(0, 5, sum(ns)).tolist()
+        lay = O.build_layout(ps, ns, lens)
+        dense = O.mask_bruteforce(lay)
+        for b in range(lay.B):
+            s0, e0 = lay.cu_seqlens[b], lay.cu_seqlens[b + 1]
+            assert (O.mask_rows(lay, b, np.arange(s0, e0)) == dense[s0:e0, s0:e0]).all()
+        assert int(dense.sum()) == O.pair_count(lay) == _pairs_closed_form(ps, ns, lens)
+
+
 def _pairs_closed_form(prefix_tokens, n_items, item_lens):
     # S(S+1)/2 for the causal query block, then per item set of n = L+1
     # tokens: n*S (whole query) + n(n+1)/2 (causal inside the item).
