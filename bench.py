@@ -149,6 +149,23 @@ def make_workload(name: str):
     return w, shapes, vals, T, M
 
 
+def make_workload_oracle(name: str):
+    """make_workload for the reference arm: the sizes come from the oracle's
+    own layout, so that arm runs without the CUDA library."""
+    import oracle as O
+    from ranking_prefill_gb300 import synth
+    w = synth.WORKLOADS[name]
+    shapes = synth.draw_shapes(w)
+    if w.layout == "setwise":
+        sl = O.setwise_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
+        T, M = int(sl.causal.cu_seqlens[-1]), len(sl.marker_positions)
+    else:
+        lay = O.build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
+        T, M = int(lay.cu_seqlens[-1]), len(lay.delim_positions)
+    vals = synth.draw_values(w.seed, T, w.hq, w.hkv, w.head_dim, w.d_model, w.vocab)
+    return w, shapes, vals, T, M
+
+
 class HostLayout:
     """The attention descriptor arrays and readout rows of one batch: MIS
     requests (items isolated, read at their trailing DELIMs) or setwise
@@ -853,7 +870,7 @@ def cpu_baseline(w, shapes, vals, labels, budget_s):
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    w, shapes, vals, T, M = make_workload(args.workload)
+    w, shapes, vals, T, M = make_workload_oracle(args.workload)
     labels = [int(x) for x in shapes.label_sets[0]]
     # every step is a bounded sample: about cpu_budget_s over the whole run,
     # at least a quarter second a step (the default 200 + 5 steps: ~1 min)
