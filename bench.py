@@ -149,19 +149,23 @@ def make_workload(name: str):
     return w, shapes, vals, T, M
 
 
+def oracle_sizes(w, shapes):
+    """(T, M) of a workload from the oracle's own layout."""
+    import oracle as O
+    if w.layout == "setwise":
+        sl = O.setwise_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
+        return int(sl.causal.cu_seqlens[-1]), len(sl.marker_positions)
+    lay = O.build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
+    return int(lay.cu_seqlens[-1]), len(lay.delim_positions)
+
+
 def make_workload_oracle(name: str):
     """make_workload for the reference arm: the sizes come from the oracle's
     own layout, so that arm runs without the CUDA library."""
-    import oracle as O
     from ranking_prefill_gb300 import synth
     w = synth.WORKLOADS[name]
     shapes = synth.draw_shapes(w)
-    if w.layout == "setwise":
-        sl = O.setwise_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
-        T, M = int(sl.causal.cu_seqlens[-1]), len(sl.marker_positions)
-    else:
-        lay = O.build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
-        T, M = int(lay.cu_seqlens[-1]), len(lay.delim_positions)
+    T, M = oracle_sizes(w, shapes)
     vals = synth.draw_values(w.seed, T, w.hq, w.hkv, w.head_dim, w.d_model, w.vocab)
     return w, shapes, vals, T, M
 

@@ -299,3 +299,16 @@ def test_unit_walk_hands_out_every_unit_once_pass_by_pass(name, mode):
     for kk in range((len(walk) + G - 1) // G):
         part = walk[kk * G:(kk + 1) * G]
         assert set(part[part >= 0].tolist()) == set(range(kk * G, min((kk + 1) * G, n)))
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_both_bench_arms_size_every_workload_alike(L, name):
+    # bench.py's own arm sizes a workload through the library, its reference
+    # arm (the oracle) through the oracle's layout: both see the same T and M
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    w = synth.WORKLOADS[name]
+    s = synth.draw_shapes(w)
+    size = lib.mis_setwise_layout_size if w.layout == "setwise" else lib.mis_layout_size
+    assert tuple(size(s.prefix_tokens, s.n_items, s.item_lens)) == bench.oracle_sizes(w, s)
