@@ -159,12 +159,20 @@ def test_workspace_size_and_validation(L):
 
 def test_label_scores_argument_errors(L):
     labels = np.array([1, 2], np.int32)
-    def call(M=4, d=128, V=1000, K=2, lab=labels, ws=None, wsb=0):
-        return L.mis_label_scores(C.c_void_p(0x1000), d, 100, C.c_void_p(0x2000), d, V,
-                                  C.c_void_p(0x3000), M, lab.ctypes.data_as(C.POINTER(C.c_int32)),
+    def call(M=4, d=128, V=1000, K=2, lab=labels, ws=None, wsb=0, hidden=0x1000, stride=None,
+             delim=0x3000):
+        return L.mis_label_scores(C.c_void_p(hidden), d if stride is None else stride, 100,
+                                  C.c_void_p(0x2000), d, V, C.c_void_p(delim), M,
+                                  lab.ctypes.data_as(C.POINTER(C.c_int32)),
                                   K, C.c_void_p(0x4000), None, ws, wsb, None)
     assert call() == lib.MIS_ERR_WORKSPACE
     assert call(d=96) == lib.MIS_ERR_UNSUPPORTED
+    assert call(d=8256) == lib.MIS_ERR_UNSUPPORTED              # above the widest model
+    assert call(K=0) == lib.MIS_ERR_INVALID_ARG
+    assert call(hidden=0x1008) == lib.MIS_ERR_INVALID_ARG      # not 16-byte aligned (TMA)
+    assert call(delim=0x3002) == lib.MIS_ERR_INVALID_ARG
+    assert call(stride=64) == lib.MIS_ERR_SHAPE                # row stride below d
+    assert call(stride=132) == lib.MIS_ERR_SHAPE               # not a multiple of 8 elements
     assert call(K=17, lab=np.arange(17, dtype=np.int32)) == lib.MIS_ERR_UNSUPPORTED
     assert call(lab=np.array([1, 1000], np.int32)) == lib.MIS_ERR_INVALID_ARG
     assert call(lab=np.array([-1, 3], np.int32)) == lib.MIS_ERR_INVALID_ARG
