@@ -320,3 +320,28 @@ def test_both_bench_arms_size_every_workload_alike(L, name):
     s = synth.draw_shapes(w)
     size = lib.mis_setwise_layout_size if w.layout == "setwise" else lib.mis_layout_size
     assert tuple(size(s.prefix_tokens, s.n_items, s.item_lens)) == bench.oracle_sizes(w, s)
+
+
+def test_attention_calls_refuse_the_wrong_plan_kind_before_any_launch(L):
+    # A plan form runs only the plan kind it was made for, and a host-only
+    # plan (no workspace) runs nothing; every refusal comes from the host.
+    lay = lib.mis_build_layout([40], [2], [5, 6], with_positions=False)
+    plain = lib.Plan.host_only(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets,
+                               4, 2, 64)
+    cl = O.cached_layout([0], [10], [2], [3, 4])
+    cached = lib.CachedPlan.host_only(cl.cu_seqlens, cl.item_ptr, cl.item_offsets, [0], [10],
+                                      10, 4, 2, 64)
+    a = C.c_void_p(0x10000)
+    def fwd(plan):
+        return L.mis_attention_fwd_plan(plan, a, a, a, a, None, 256, 128, 128, 256, None)
+    def fwd_cached(plan):
+        return L.mis_attention_fwd_cached(plan, a, a, a, a, a, a, None, 256, 128, 128, 128, 128,
+                                          256, None)
+    assert fwd(None) == lib.MIS_ERR_INVALID_ARG
+    assert fwd(cached._h) == lib.MIS_ERR_INVALID_ARG          # needs the cache buffers
+    assert fwd(plain._h) == lib.MIS_ERR_WORKSPACE             # host-only plan
+    assert fwd_cached(None) == lib.MIS_ERR_INVALID_ARG
+    assert fwd_cached(plain._h) == lib.MIS_ERR_INVALID_ARG    # not a cached-prefix plan
+    assert fwd_cached(cached._h) == lib.MIS_ERR_WORKSPACE
+    plain.destroy()
+    cached.destroy()

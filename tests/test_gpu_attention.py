@@ -197,3 +197,32 @@ def test_planner_plans_match_oracle_across_buffer_reuse():
         ro, _ = O.attention(f64(v["q"]), f64(v["k"]), f64(v["v"]), oracle_layout(s))
         assert np.abs(f64(o) - ro).max() <= ATTN_TOL
     planner.destroy()
+
+
+def test_pointer_and_stride_refusals_launch_nothing():
+    # Each refusal below comes from the host checks of mis_attention_fwd_plan,
+    # before any launch: the output keeps its fill and the status stays clean.
+    s = synth.custom_shapes([130], [3], [10, 20, 30])
+    lay = lib.mis_build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+    dev = torch.device("cuda")
+    T, hq, hkv, D = lay.T, 4, 2, 64
+    q = torch.zeros(T, hq, D, dtype=torch.bfloat16, device=dev)
+    k = torch.zeros(T, hkv, D, dtype=torch.bfloat16, device=dev)
+    o = torch.full((T, hq, D), 7.0, dtype=torch.bfloat16, device=dev)
+    lse = torch.full((hq, T), 7.0, dtype=torch.float32, device=dev)
+    plan = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, hq, hkv, D)
+    ws = torch.zeros(plan.workspace_size(), dtype=torch.uint8, device=dev)
+    plan.create(ws)
+    L = lib.load()
+    qp, kp, op, lp = q.data_ptr(), k.data_ptr(), o.data_ptr(), lse.data_ptr()
+    def call(qa=qp, oa=op, la=None, qs=hq * D, ks=hkv * D, os_=hq * D):
+        return L.mis_attention_fwd_plan(plan._h, qa, kp, kp, oa, la, qs, ks, ks, os_, None)
+    assert call(qa=qp + 2) == lib.MIS_ERR_INVALID_ARG          # Q not 16-byte aligned
+    assert call(oa=op + 8) == lib.MIS_ERR_INVALID_ARG          # O not 16-byte aligned
+    assert call(la=lp + 2) == lib.MIS_ERR_INVALID_ARG          # LSE not 4-byte aligned
+    assert call(qs=hq * D - 8) == lib.MIS_ERR_SHAPE            # Q rows overlap
+    assert call(ks=hkv * D + 4) == lib.MIS_ERR_SHAPE           # not a multiple of 8 elements
+    torch.cuda.synchronize()
+    assert bool((o == 7.0).all()) and bool((lse == 7.0).all())
+    assert lib.mis_get_device_status(ws) == lib.MIS_OK
+    plan.destroy()
