@@ -210,6 +210,17 @@ def useful_flops(pairs: int, hq: int, D: int) -> float:
     return 4.0 * hq * D * pairs
 
 
+L2_NOTE = "evicted between timed steps (256 MB write, then 256 MB read; untimed)"
+
+
+def workload_config(w, shapes, T: int, M: int, K: int, world: int) -> dict:
+    """The `config` object of the JSON line; both arms print the same one."""
+    return {"workload": w.name, "requests": int(len(shapes.prefix_tokens)), "tokens": int(T),
+            "items": int(M), "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim,
+            "d_model": w.d_model, "vocab": w.vocab, "labels": int(K), "l2": L2_NOTE,
+            "parallelism": f"replicas x{world}"}
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, dist):
@@ -220,7 +231,27 @@ def run_ours(args, rank, world, dist):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     lib.load()
-    w, shapes, vals, T, M = make_workload(args.workload)
+    result = measure(args, args.workload, rank, world, dist, dev, local, full=True)
+    # further workloads, timed the same way (throughput, per-call split and
+    # roofline only; no end-to-end leg, comparators or CPU baseline)
+    others = {}
+    for name in [x for x in args.extra_workloads.split(",") if x and x != args.workload]:
+        r = measure(args, name, rank, world, dist, dev, local, full=False)
+        others[name] = {k: r[k] for k in ("value", "unit", "ms_per_step", "roofline", "attention",
+                                          "scoring", "clocks")}
+        others[name]["config"] = r["config"]
+    if others:
+        result["other_workloads"] = others
+    return result
+
+
+def measure(args, name, rank, world, dist, dev, local, full):
+    """The timed steps of one workload; with `full`, also the end-to-end leg,
+    the GPU comparators and the CPU oracle baseline."""
+    import torch
+    from ranking_prefill_gb300 import lib
+
+    w, shapes, vals, T, M = make_workload(name)
     labels = [int(x) for x in shapes.label_sets[0]]
     K = len(labels)
     stream = torch.cuda.Stream(dev)
@@ -400,13 +431,9 @@ def run_ours(args, rank, world, dist):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; shapes of the pages' workloads, random-init LM head)",
-        "config": {"workload": w.name, "requests": int(len(shapes.prefix_tokens)), "tokens": T,
-                   "items": M, "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim,
-                   "d_model": w.d_model, "vocab": w.vocab, "labels": K,
-                   "l2": "evicted between timed steps (256 MB write, then 256 MB read; untimed)",
-                   "plan": "host layout and plan every step; the upload of step i+1's plan and "
-                           "readout rows overlaps step i, which ends only once it has landed",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(w, shapes, T, M, K, world),
+        "plan_upload": "host layout and plan every step; the upload of step i+1's plan and "
+                       "readout rows overlaps step i, which ends only once it has landed",
         "roofline": roof,
         "attention": {"ms": round(t_attn * 1e3, 4), "useful_tflops": round(attn_tflops, 1),
                       "frac_of_bf16_peak": round(attn_tflops / peaks["bf16_tflops"], 4),
@@ -431,13 +458,15 @@ def run_ours(args, rank, world, dist):
                           "note": "rotary embedding of Q and K at the reused position ids, "
                                   "inside the timed step before the attention"}
         result["config"]["rope"] = "base 1e6, rotate-half, reused position ids"
-    if not args.no_e2e:
+    if full and not args.no_e2e:
         result["e2e"] = run_e2e(args, w, shapes, vals, labels, dev, stream, dist, world)
-    if not args.no_comparators:
+    if full and not args.no_comparators:
         result["comparators"] = run_comparators(w, shapes, vals, labels, dev, stream, q, k, v,
                                                 hidden, w_lm, t_attn, t_score, M, pairs)
-    if rank == 0 and not args.no_cpu_baseline:
+    if full and rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, shapes, vals, labels, args.cpu_budget_s)
+    del q, k, v, o, hidden, w_lm, ws_plans, ws_score, flush
+    torch.cuda.empty_cache()
     return result
 
 
@@ -818,6 +847,7 @@ def _oracle_sample(w, shapes, vals, labels, budget_s, seed=0, rates=None):
         lay = O.build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
         readout = lay.delim_positions
     n_read = len(readout)
+    t_call = time.perf_counter()
     x = _as_f64(vals)
     q, k, v, hidden, W = x["q"], x["k"], x["v"], x["hidden"], x["w_lm"]
     rng = np.random.default_rng(seed)
@@ -835,7 +865,7 @@ def _oracle_sample(w, shapes, vals, labels, budget_s, seed=0, rates=None):
     else:
         pilot = np.sort(rng.choice(lay.T, size=min(32, lay.T), replace=False))
         per_row = timed(lambda: O.attention(q, k, v, lay, rows=pilot)) / len(pilot)
-    n_rows = int(min(lay.T, max(min(32, lay.T), (budget_s / 2) / max(per_row, 1e-9))))
+    n_rows = int(min(lay.T, max(min(32, lay.T), 0.7 * budget_s / max(per_row, 1e-9))))
     rows = None if n_rows >= lay.T else np.sort(rng.choice(lay.T, size=n_rows, replace=False))
     t_attn = timed(lambda: O.attention(q, k, v, lay, rows=rows))
     frac_r = 1.0 if rows is None else n_rows / lay.T
@@ -848,7 +878,7 @@ def _oracle_sample(w, shapes, vals, labels, budget_s, seed=0, rates=None):
     pilot_i = np.sort(rng.choice(n_read, size=base, replace=False))
     t_pilot = timed(lambda: O.label_scores(hidden, W, readout, labels, items=pilot_i))
     per_item = t_pilot / base
-    n_items = int(min(n_read, max(base, (budget_s / 2) / max(per_item, 1e-9))))
+    n_items = int(min(n_read, max(base, 0.3 * budget_s / max(per_item, 1e-9))))
     if n_items == base:
         items, t_score = (None if base == n_read else pilot_i), t_pilot
     else:
@@ -862,7 +892,8 @@ def _oracle_sample(w, shapes, vals, labels, budget_s, seed=0, rates=None):
         sample = (f"oracle on {'all' if rows is None else n_rows} of {lay.T} rows x {w.hq} heads and "
                   f"{'all' if items is None else n_items} of {n_read} items; full-workload time "
                   f"extrapolated by rows and items")
-    return t_full, n_read, sample, t_attn + t_score
+    # wall time of this call: the pilots and the timed parts
+    return t_full, n_read, sample, time.perf_counter() - t_call
 
 
 def cpu_baseline(w, shapes, vals, labels, budget_s):
@@ -872,13 +903,17 @@ def cpu_baseline(w, shapes, vals, labels, budget_s):
 
 
 def run_reference(args, rank, world):
+    """The fp64 CPU oracle as the reference arm. Each step runs the oracle on
+    the whole workload when that fits the step's budget (at least 2 s, more
+    when --cpu-budget-s spread over the steps allows), else on a seeded
+    sample of rows and items; `value` is the whole workload's items over its
+    full oracle time (measured, or extrapolated from the sample by rows and
+    items), `ms_per_step` the wall time each executed step actually took."""
     if rank != 0:
         return None
     w, shapes, vals, T, M = make_workload_oracle(args.workload)
     labels = [int(x) for x in shapes.label_sets[0]]
-    # every step is a bounded sample: about cpu_budget_s over the whole run,
-    # at least a quarter second a step (the default 200 + 5 steps: ~1 min)
-    budget = max(0.25, args.cpu_budget_s / max(1, args.steps + args.warmup))
+    budget = max(2.0, args.cpu_budget_s / max(1, args.steps + args.warmup))
     vals = _as_f64(vals)
     rates = {}
     for _ in range(args.warmup):
@@ -891,11 +926,14 @@ def run_reference(args, rank, world):
     v = M * args.steps / tot_est
     return {"metric": METRIC, "value": round(v, 3), "unit": "items/s", "impl": "reference",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(1e3 * tot_est / args.steps, 2), "higher_is_better": True,
+            "ms_per_step": round(1e3 * spent / args.steps, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "tokens": T, "items": M},
+            "config": workload_config(w, shapes, T, M, len(labels), world),
             "cpu_baseline": {"value": round(v, 3), "unit": "items/s", "cores": os.cpu_count(),
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample,
+                             "full_workload_s_estimate": round(tot_est / args.steps, 3),
+                             "note": "ms_per_step: wall time of each executed step; value: the "
+                                     "workload's items over its full oracle time"},
             "e2e": {"value": round(v, 3), "unit": "items/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -906,7 +944,12 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="qwen3-0.6b-layer")
+    ap.add_argument("--workload", default="varlen-16",
+                    help="the headline workload (default: varlen-16, the largest configuration "
+                         "that fits one GPU)")
+    ap.add_argument("--extra-workloads", default="qwen3-0.6b-layer",
+                    help="comma-separated workloads also timed (throughput and roofline only); "
+                         "'' for none")
     ap.add_argument("--sweep", action="store_true",
                     help="request-size sweep N = 1..200 (prints its own JSON table)")
     ap.add_argument("--sweep-members", type=int, default=16)

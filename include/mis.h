@@ -425,7 +425,10 @@ int32_t mis_set_schedule(int32_t mode);
  *   - device_status: optional device uint32[2] that receives this call's
  *     device status words after the kernels ([0] bit 1 = a wait timed out,
  *     bit 2 = a readout row was outside [0, T); [1] = first failing site);
- *     NULL skips the copy.
+ *     NULL skips the copy. There is no workspace to hand to
+ *     mis_get_device_status(), so with NULL a readout row outside [0, T)
+ *     (scored as a zero hidden row) and a timed-out wait go unreported:
+ *     pass a status buffer wherever such errors must be seen.
  * ------------------------------------------------------------------------ */
 #define MIS_NOALLOC_SCRATCH_BYTES (8650752) /* 8.25 MiB */
 

@@ -45,8 +45,7 @@ What it computes, and where each step comes from:
   Scoring"): query, every candidate, then one marker per candidate, as one
   plain causal sequence, scored at each marker.
 
-Readings taken where the pages are silent or garbled (each is also listed in
-the design notes):
+Readings taken where the pages are silent or garbled:
   - the leading DELIM belongs to the shared set Q (so |Q| = S = P + 1); each
     trailing DELIM belongs to its own item's set I_i, and is that item's
     readout row (the row that "reads prefix + item k");

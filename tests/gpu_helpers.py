@@ -74,12 +74,23 @@ def oracle_layout(shapes):
     return O.build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
 
 
-def check_attention(shapes, hq, hkv, D, seed, rows=None, causal=False, **kw):
+_ORACLE_CACHE = {}
+
+
+def check_attention(shapes, hq, hkv, D, seed, rows=None, causal=False, cache_key=None, **kw):
+    """GPU attention vs the oracle on the same seeded inputs. With `cache_key`,
+    the oracle's result is kept for the next call with the same key (the same
+    workload under another schedule)."""
     lay, vals, o, lse, stats, _ = run_attention(shapes, hq, hkv, D, seed, causal=causal, **kw)
     olay = oracle_layout(shapes)
     if causal:
         olay = O.causal_layout(np.diff(olay.cu_seqlens))
-    ro, rl = O.attention(f64(vals["q"]), f64(vals["k"]), f64(vals["v"]), olay, rows=rows)
+    if cache_key is not None and cache_key in _ORACLE_CACHE:
+        ro, rl = _ORACLE_CACHE[cache_key]
+    else:
+        ro, rl = O.attention(f64(vals["q"]), f64(vals["k"]), f64(vals["v"]), olay, rows=rows)
+        if cache_key is not None:
+            _ORACLE_CACHE[cache_key] = (ro, rl)
     got = f64(o) if rows is None else f64(o[torch.as_tensor(np.asarray(rows), device=o.device)])
     err = np.abs(got - ro).max() if got.size else 0.0
     assert np.isfinite(got).all()

@@ -40,10 +40,11 @@ def test_exports_every_declared_symbol(L):
 
 
 def _shapes_cases():
-    yield synth.draw_shapes(synth.WORKLOADS["tiny"])
-    yield synth.draw_shapes(synth.WORKLOADS["qwen3-0.6b-layer"])
-    yield synth.draw_shapes(synth.WORKLOADS["decision-256"])
-    yield synth.draw_shapes(synth.WORKLOADS["8b-large"])
+    # every MIS workload the benchmark and the parity tests run (the five
+    # configurations plus the page's 12k-prefix shape), then random batches
+    for name in ("tiny", "qwen3-0.6b-layer", "varlen-16", "8b-large", "decision-256",
+                 "prefix12k-50x150"):
+        yield synth.draw_shapes(synth.WORKLOADS[name])
     rng = np.random.default_rng(123)
     for _ in range(30):
         B = int(rng.integers(1, 5))
@@ -198,6 +199,8 @@ def test_layout_argument_errors(L):
 def test_setwise_layout_bit_exact(L):
     rng = np.random.default_rng(77)
     cases = [([40], [3], [7, 12, 9]), ([0, 5], [2, 0], [3, 4]), ([1], [0], [])]
+    sw = synth.draw_shapes(synth.WORKLOADS["setwise-256"])      # the benchmark's setwise batch
+    cases.append((sw.prefix_tokens.tolist(), sw.n_items.tolist(), sw.item_lens.tolist()))
     for _ in range(20):
         B = int(rng.integers(1, 6))
         qt = rng.integers(0, 300, B)

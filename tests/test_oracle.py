@@ -580,3 +580,103 @@ def test_cached_layout_rejects_bad_requests():
         O.cached_layout([0], [0], [1], [3])        # no cached prefix
     with pytest.raises(ValueError):
         O.cached_layout([0], [4], [0], [])         # no item
+
+
+# ------------------------------------------------- cached-prefix tile map ----
+
+def _cached_mask_bruteforce(cl, b):
+    """Visibility of request b's keys from its new rows, by set enumeration.
+
+    Keys are numbered on the request's own axis: its S_b cached prefix keys
+    first (cache rows cache_start .. cache_start + S_b - 1), then its new rows
+    in order. Eq. (4) of "From Generation to Scoring", Section 4.1: a key is
+    visible from row j iff it precedes j and lies in the shared set Q (here:
+    the cached prefix, which precedes every new row) or in j's own item set.
+    """
+    s0, e0 = int(cl.cu_seqlens[b]), int(cl.cu_seqlens[b + 1])
+    S = int(cl.cache_len[b])
+    Q = {("cache", int(cl.cache_start[b]) + x) for x in range(S)}
+    items = [set(range(int(cl.item_offsets[i]), int(cl.item_ends[i])))
+             for i in range(int(cl.item_ptr[b]), int(cl.item_ptr[b + 1]))]
+    keys = sorted(Q) + [("new", r) for r in range(s0, e0)]
+    vis = np.zeros((e0 - s0, len(keys)), dtype=bool)
+    for jj, j in enumerate(range(s0, e0)):
+        for kk, key in enumerate(keys):
+            if key in Q:
+                vis[jj, kk] = True                     # the prefix precedes every new row
+            else:
+                k = key[1]
+                vis[jj, kk] = k <= j and any(j in I and k in I for I in items)
+    return vis, S
+
+
+def _cached_tiles_from_dense(cl, BM, BN):
+    out = []
+    for b in range(cl.B):
+        vis, S = _cached_mask_bruteforce(cl, b)
+        L = vis.shape[0]
+        # key tiles: the cached prefix from its first key, then the new rows from the first one
+        kt = [(u * BN, min((u + 1) * BN, S)) for u in range((S + BN - 1) // BN)]
+        kt += [(S + u * BN, S + min((u + 1) * BN, L)) for u in range((L + BN - 1) // BN)]
+        for t in range((L + BM - 1) // BM):
+            rows = vis[t * BM:min((t + 1) * BM, L)]
+            for u, (c0, c1) in enumerate(kt):
+                blk = rows[:, c0:c1]
+                if blk.any():
+                    out.append((b, t, u, O.FULL if blk.all() else O.PARTIAL))
+    return np.asarray(out, np.int32).reshape(-1, 4)
+
+
+def test_tile_map_cached_vs_set_enumeration_exhaustive():
+    # every one-request layout with S in 1..5, 1..3 items of 0..3 tokens, on
+    # tile shapes that split the prefix, the items and the tiles' own edges
+    import itertools
+    n_cases = 0
+    for S in range(1, 6):
+        for n in range(1, 4):
+            for lens in itertools.product(range(4), repeat=n):
+                cl = O.cached_layout([2], [S], [n], list(lens))
+                for BM, BN in [(1, 1), (2, 3), (3, 2), (4, 4)]:
+                    got = O.tile_map_cached(cl, BM, BN)
+                    ref = _cached_tiles_from_dense(cl, BM, BN)
+                    assert got.shape == ref.shape and np.array_equal(got, ref), (S, lens, BM, BN)
+                    n_cases += 1
+    assert n_cases == 5 * (4 + 16 + 64) * 4
+
+
+@pytest.mark.parametrize("BM,BN", [(4, 4), (4, 8), (8, 4), (3, 5), (16, 16)])
+def test_tile_map_cached_vs_set_enumeration_random(BM, BN):
+    rng = np.random.default_rng(700 + BM * 10 + BN)
+    for _ in range(20):
+        B = int(rng.integers(1, 4))
+        S = rng.integers(1, 40, B)
+        n = rng.integers(1, 5, B)
+        lens = rng.integers(0, 12, int(n.sum()))
+        cstart = np.zeros(B, np.int64)
+        t = int(rng.integers(0, 9))
+        for b in rng.permutation(B):             # prefixes anywhere in the cache, in any order
+            cstart[b] = t
+            t += int(S[b]) + int(rng.integers(0, 9))
+        cl = O.cached_layout(cstart, S, n, lens)
+        got = O.tile_map_cached(cl, BM, BN)
+        ref = _cached_tiles_from_dense(cl, BM, BN)
+        assert got.shape == ref.shape and np.array_equal(got, ref)
+
+
+def test_tile_map_cached_counts_on_a_hand_case():
+    # S = 5 cached keys, items of 2 and 1 tokens (+ DELIM): new rows 0-2 are
+    # item 0, rows 3-4 item 1. With BM = BN = 2 the key tiles are
+    # cache [0,2) [2,4) [4,5) and new rows [0,2) [2,4) [4,5).
+    cl = O.cached_layout([0], [5], [2], [2, 1])
+    got = O.tile_map_cached(cl, 2, 2)
+    want = [
+        # q-tile 0 (rows 0, 1: item 0): every cached tile, then new tile 0 (causal corner)
+        (0, 0, 0, O.FULL), (0, 0, 1, O.FULL), (0, 0, 2, O.FULL), (0, 0, 3, O.PARTIAL),
+        # q-tile 1 (row 2: item 0; row 3: item 1)
+        (0, 1, 0, O.FULL), (0, 1, 1, O.FULL), (0, 1, 2, O.FULL), (0, 1, 3, O.PARTIAL),
+        (0, 1, 4, O.PARTIAL),
+        # q-tile 2 (row 4: item 1): its own item's keys 3 and 4
+        (0, 2, 0, O.FULL), (0, 2, 1, O.FULL), (0, 2, 2, O.FULL), (0, 2, 4, O.PARTIAL),
+        (0, 2, 5, O.FULL),
+    ]
+    assert [tuple(int(x) for x in r) for r in got] == want
