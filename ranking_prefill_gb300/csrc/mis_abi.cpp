@@ -411,6 +411,34 @@ mis_status_t mis_attention_fwd_plan(mis_plan_t plan, const void* q, const void* 
   }
 }
 
+mis_status_t mis_attention_fwd_plan_rope(mis_plan_t plan, const void* q, const void* k,
+                                         const void* v, void* o, float* lse, int64_t qs,
+                                         int64_t ks, int64_t vs, int64_t os,
+                                         const int32_t* position_ids, const float* rope_table,
+                                         int32_t n_positions, void* stream) {
+  if (!plan) return MIS_ERR_INVALID_ARG;
+  HostPlan& p = plan->p;
+  if (p.cached) return MIS_ERR_INVALID_ARG;       // needs the cache buffers
+  if (!p.workspace) return MIS_ERR_WORKSPACE;
+  if (!q || !k || !v || !o || !position_ids || !rope_table) return MIS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(rope_table))
+    return MIS_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(position_ids) & 3u) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return MIS_ERR_INVALID_ARG;
+  if (n_positions < 1) return MIS_ERR_INVALID_ARG;
+  const int64_t wq = (int64_t)p.Hq * p.D, wk = (int64_t)p.Hkv * p.D;
+  if (qs < wq || os < wq || ks < wk || vs < wk) return MIS_ERR_SHAPE;
+  if ((qs | ks | vs | os) & 7) return MIS_ERR_SHAPE;
+  const RopeQ rope{position_ids, rope_table, n_positions};
+  try {
+    return launch_attention(p, q, k, v, nullptr, nullptr, o, lse, qs, ks, vs, 0, 0, os, stream,
+                            &rope);
+  } catch (...) {
+    return MIS_ERR_CUDA;
+  }
+}
+
 mis_status_t mis_attention_fwd_cached(mis_plan_t plan, const void* q, const void* k,
                                       const void* v, const void* k_cache, const void* v_cache,
                                       void* o, float* lse, int64_t qs, int64_t ks, int64_t vs,

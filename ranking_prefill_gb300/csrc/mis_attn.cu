@@ -121,7 +121,47 @@ struct AttnParams {
   uint32_t* status;
   uint64_t wait_ns;
   uint32_t stall;         // failure injection: wait on a barrier nothing arrives on
+  // rotary embedding of Q on load (null rope_tab: Q arrives rotated)
+  const int32_t* rope_pos;  // [T] position of every (new) row
+  const float4* rope_tab;   // [rope_n][D/2] (cos, sin) pairs, two frequencies per float4
+  int32_t rope_n;
 };
+
+// Rotary embedding of row r of a Q tile in shared memory, in place: NB boxes
+// of 128 rows x 64 bf16 columns with the 128-byte swizzle (16-byte chunk c of
+// row r at chunk c ^ (r & 7)). Rotate-half form: the pair (x[i], x[i + D/2])
+// turns by the angle of frequency i, whose (cos, sin) are tab[i]. Chunk pairs
+// g (frequencies 8g .. 8g+7) from g0 in steps of GS.
+template <int D, int GS>
+__device__ __forceinline__ void rope_row_smem(uint32_t sq, int r, const float4* __restrict__ tab,
+                                              int g0) {
+  constexpr int HALF = D / 2, BOX = kBN * 64 * 2;
+  const uint32_t row = sq + (uint32_t)r * 128u;
+  const int sw = r & 7;
+#pragma unroll
+  for (int gi = 0; gi < D / 16 / GS; ++gi) {
+    const int g = g0 + gi * GS;
+    const int c1 = 8 * g, c2 = 8 * g + HALF;
+    const uint32_t a1 = row + (uint32_t)((c1 >> 6) * BOX) + ((((c1 & 63) >> 3) ^ sw) << 4);
+    const uint32_t a2 = row + (uint32_t)((c2 >> 6) * BOX) + ((((c2 & 63) >> 3) ^ sw) << 4);
+    uint32_t x[4], y[4];
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]) : "r"(a1) : "memory");
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(y[0]), "=r"(y[1]), "=r"(y[2]), "=r"(y[3]) : "r"(a2) : "memory");
+    uint32_t ox[4], oy[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float4 cs = __ldg(tab + 4 * g + w);        // frequencies 8g + 2w, 8g + 2w + 1
+      const float x0 = __uint_as_float(x[w] << 16), x1 = __uint_as_float(x[w] & 0xffff0000u);
+      const float y0 = __uint_as_float(y[w] << 16), y1 = __uint_as_float(y[w] & 0xffff0000u);
+      ox[w] = pack_bf16(fmaf(x0, cs.x, -y0 * cs.y), fmaf(x1, cs.z, -y1 * cs.w));
+      oy[w] = pack_bf16(fmaf(y0, cs.x, x0 * cs.y), fmaf(y1, cs.z, x1 * cs.w));
+    }
+    st_shared_v4(a1, ox[0], ox[1], ox[2], ox[3]);
+    st_shared_v4(a2, oy[0], oy[1], oy[2], oy[3]);
+  }
+}
 
 // Unit handled by this block in pass kk: walk position kk * G + c, passes
 // alternating direction (snake order), so over the longest-first unit list
@@ -155,7 +195,8 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   //   SE_s: the epilogue has read slot s
   constexpr int bQF = 0, bQE = 1, bKF = 2, bKE = bKF + KS, bVF = bKE + KS, bVE = bVF + VS,
                 bSF = bVE + VS, bPF = bSF + 2, bOF = bPF + 2, bOE = bOF + 1, bDR = bOE + 2,
-                bST = bDR + 1, bSE = bST + 4, nBar = bSE + 2;
+                bST = bDR + 1, bSE = bST + 4, bQR = bSE + 2, nBar = bQR + 1;
+  // bQR: the unit's Q tiles rotated in place (rotary embedding on load)
 
   griddep_launch_dependents();
 
@@ -197,6 +238,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
     }
     mbar_init(bar(bOF), 1);
     mbar_init(bar(bDR), 1);
+    mbar_init(bar(bQR), 8);                            // one arrival per softmax warp
     fence_mbar_init();
     fence_proxy_async();
   }
@@ -312,7 +354,8 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
           const int u = unit_at(p, kk);
           if (u < 0) continue;
           const int nk = p.units[u / n_hg].nk;
-          if (!(ok = wait<true>(bar(bQF), lu & 1, W, 0x200))) break;
+          // the unit's Q: landed, or landed and rotated by the softmax warps
+          if (!(ok = wait<true>(bar(p.rope_tab ? bQR : bQF), lu & 1, W, 0x200))) break;
           // the first PV of stream t in this unit overwrites O_t: the epilogue of
           // the previous unit must have read it out of tensor memory. In the
           // split schedule one barrier covers both accumulators, and stream 0's
@@ -406,6 +449,26 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
       const int jj = valid ? j : -1;                    // invalid rows see nothing
       const int lo = valid ? p.seg_start[j - p.qbase] : 0x7fffffff;
       const int nk = un.nk;
+      if (p.rope_tab) {
+        // rotary embedding of this unit's Q on load: each thread turns its
+        // row (pair schedule: of its stream's head; split schedule: half the
+        // frequencies of the one head), then the MMA thread may read it
+        int pos = -1;
+        if (valid) pos = p.rope_pos[j - p.qbase];
+        ok = wait<true>(bar(bQF), lu & 1, W, 0x5c0 + t);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        if (valid) {
+          if (pos >= 0 && pos < p.rope_n)
+            rope_row_smem<D, split ? 2 : 1>(smem_u32(sQ + (split ? 0 : t) * C::kTile), r,
+                                            p.rope_tab + (size_t)pos * (D / 4), split ? t : 0);
+          else
+            raise_status(p.status, kDevIndex, 0x5e0);
+        }
+        fence_proxy_async();            // the tensor core reads what this thread wrote
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(bQR));
+      }
       // key tiles of this stream: all (pair) or t, t+2, ... (split)
       const int kstep = split ? 2 : 1, kfirst = split ? t : 0;
       const int nkt = split ? (nk - t + 1) / 2 : nk;
@@ -692,7 +755,8 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
 template <int D>
 mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
                       const void* kc, const void* vc, void* o, float* lse, int64_t qs, int64_t ks,
-                      int64_t vs, int64_t kcs, int64_t vcs, int64_t os, void* stream) {
+                      int64_t vs, int64_t kcs, int64_t vcs, int64_t os, const RopeQ* rope,
+                      void* stream) {
   using C = AttnCfg<D>;
   bool ok = true;
   const uint32_t box[3] = {64, 1, (uint32_t)kBM};
@@ -736,6 +800,9 @@ mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
   prm.status = reinterpret_cast<uint32_t*>(ws);
   prm.wait_ns = wait_limit_ns();
   prm.stall = inject_stall_mask() & 1u;
+  prm.rope_pos = rope ? rope->pos : nullptr;
+  prm.rope_tab = rope ? reinterpret_cast<const float4*>(rope->tab) : nullptr;
+  prm.rope_n = rope ? rope->n : 0;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (pl.status_clear) {
@@ -761,11 +828,13 @@ mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
 mis_status_t launch_attention(HostPlan& p, const void* q, const void* k, const void* v,
                               const void* k_cache, const void* v_cache, void* o, float* lse,
                               int64_t qs, int64_t ks, int64_t vs, int64_t kcs, int64_t vcs,
-                              int64_t os, void* stream) {
+                              int64_t os, void* stream, const RopeQ* rope) {
   if (p.D == 128)
-    return launch_d<128>(p, q, k, v, k_cache, v_cache, o, lse, qs, ks, vs, kcs, vcs, os, stream);
+    return launch_d<128>(p, q, k, v, k_cache, v_cache, o, lse, qs, ks, vs, kcs, vcs, os, rope,
+                         stream);
   if (p.D == 64)
-    return launch_d<64>(p, q, k, v, k_cache, v_cache, o, lse, qs, ks, vs, kcs, vcs, os, stream);
+    return launch_d<64>(p, q, k, v, k_cache, v_cache, o, lse, qs, ks, vs, kcs, vcs, os, rope,
+                        stream);
   return MIS_ERR_UNSUPPORTED;
 }
 

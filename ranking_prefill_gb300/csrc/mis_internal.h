@@ -108,13 +108,22 @@ uint32_t inject_stall_mask();
 // Process-wide attention schedule override (MIS_SCHEDULE_*).
 int32_t schedule_override();
 
+// Rotary embedding of Q on load: the position of every (new) row and the
+// (cos, sin) table they index (device pointers, already validated).
+struct RopeQ {
+  const int32_t* pos;
+  const float* tab;
+  int32_t n;
+};
+
 // Kernel launchers (defined in the .cu files). Return MIS_ERR_CUDA on launch
 // failure. Pointers are already validated.
-// k_cache / v_cache (and their strides) are used by cached plans only.
+// k_cache / v_cache (and their strides) are used by cached plans only; rope
+// (or null) rotates Q on load.
 mis_status_t launch_attention(HostPlan& p, const void* q, const void* k, const void* v,
                               const void* k_cache, const void* v_cache, void* o, float* lse,
                               int64_t qs, int64_t ks, int64_t vs, int64_t kcs, int64_t vcs,
-                              int64_t os, void* stream);
+                              int64_t os, void* stream, const RopeQ* rope = nullptr);
 
 struct ScoreArgs {
   const void* hidden; int64_t hidden_stride; int32_t T;

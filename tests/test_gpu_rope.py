@@ -112,3 +112,138 @@ def test_rotary_mis_equals_single_item_prompts_on_gpu():
     os_, ss = run(sis, rows)
     assert (om - os_).abs().max().item() <= 1e-2
     assert (sm - ss).abs().max().item() <= SCORE_TOL
+
+
+# ------------------------------------------------ Q rotated on load (fused) ----
+
+@pytest.fixture(params=[lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT], ids=["pair", "split"])
+def schedule(request):
+    from gpu_helpers import forced_schedule
+    with forced_schedule(request.param):
+        yield request.param
+
+
+def _fused_case(shapes, hq, hkv, D, seed, base=1.0e6, n_extra=7, stride_pad=0):
+    """Q unrotated through mis_attention_fwd_plan_rope, K rotated by the K-only
+    mis_rope_qk; returns (oracle layout, O, LSE, oracle O, oracle LSE, status)."""
+    lay = lib.mis_build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
+    v = synth.draw_values(seed, lay.T, hq, hkv, D, want=("q", "k", "v"))
+    dev = torch.device("cuda")
+    T = lay.T
+
+    def place(t, h):
+        buf = torch.zeros(T, h * D + stride_pad, dtype=torch.bfloat16, device=dev)
+        view = buf.as_strided((T, h, D), (h * D + stride_pad, D, 1))
+        view.copy_(t.to(dev))
+        return view
+    q, k, vv = place(v["q"], hq), place(v["k"], hkv), place(v["v"], hkv)
+    q_before = q.clone()
+    pos = torch.as_tensor(lay.position_ids, device=dev)
+    n_pos = int(lay.position_ids.max()) + 1 + n_extra
+    tab = torch.empty(n_pos, D // 2, 2, dtype=torch.float32, device=dev)
+    lib.mis_rope_table(tab, D, base)
+    kr = place(torch.zeros_like(v["k"]), hkv)
+    lib.mis_rope_qk(None, k, None, kr, pos, base, Hq=hq)
+    o = torch.full((T, hq, D), 7.0, dtype=torch.bfloat16, device=dev)
+    lse = torch.full((hq, T), 7.0, dtype=torch.float32, device=dev)
+    plan = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, hq, hkv, D)
+    ws = torch.zeros(plan.workspace_size(), dtype=torch.uint8, device=dev)
+    plan.create(ws)
+    lib.mis_attention_fwd_plan_rope(plan, q, kr, vv, o, lse, pos, tab)
+    torch.cuda.synchronize()
+    status = lib.mis_get_device_status(ws)
+    assert torch.equal(q, q_before)                     # Q is rotated in shared memory only
+    olay = O.build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
+    ro, rl = O.attention(O.rope(f64(v["q"]), olay.position_ids, base),
+                         O.rope(f64(v["k"]), olay.position_ids, base), f64(v["v"]), olay)
+    return olay, o, lse, ro, rl, status, plan.stats()
+
+
+@pytest.mark.parametrize("hq,hkv,D,seed", [(8, 2, 128, 61), (4, 2, 64, 62), (6, 2, 128, 63),
+                                           (16, 8, 128, 64)])
+def test_q_rotated_on_load_matches_oracle(hq, hkv, D, seed, schedule):
+    # several tiles, ragged tails, empty items, long items straddling tiles
+    s = synth.custom_shapes([300, 40, 700], [6, 3, 9],
+                            [12, 0, 40, 7, 130, 2, 25, 1, 60, 3, 3, 200, 64, 0, 9, 77, 5, 31])
+    olay, o, lse, ro, rl, status, st = _fused_case(s, hq, hkv, D, seed)
+    assert status == lib.MIS_OK
+    assert np.abs(f64(o) - ro).max() <= ATTN_TOL
+    assert np.abs(f64(lse).T - rl).max() <= 2e-3
+    want = schedule if (hq // hkv) % 2 == 0 else lib.SCHEDULE_SPLIT
+    assert st["schedule"] == want
+
+
+def test_q_rotated_on_load_strided_and_qwen3_layer(schedule):
+    w = synth.WORKLOADS["qwen3-0.6b-layer"]
+    olay, o, lse, ro, rl, status, _ = _fused_case(synth.draw_shapes(w), w.hq, w.hkv, w.head_dim,
+                                                  w.seed, stride_pad=8)
+    assert status == lib.MIS_OK
+    assert np.abs(f64(o) - ro).max() <= ATTN_TOL
+
+
+def test_q_rotated_on_load_equals_rotating_first():
+    # the fused form and the two-pass form (mis_rope_qk on Q and K, then the
+    # plain attention call) agree to bf16 rounding of the rotated Q
+    s = synth.custom_shapes([500, 90], [20, 4], list(range(3, 63, 3)) + [1, 2, 100, 0])
+    hq, hkv, D = 16, 8, 128
+    lay = lib.mis_build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+    v = synth.draw_values(65, lay.T, hq, hkv, D, want=("q", "k", "v"))
+    dev = torch.device("cuda")
+    q, k, vv = (v[x].to(dev) for x in ("q", "k", "v"))
+    pos = torch.as_tensor(lay.position_ids, device=dev)
+    tab = torch.empty(int(lay.position_ids.max()) + 1, D // 2, 2, dtype=torch.float32, device=dev)
+    lib.mis_rope_table(tab, D)
+    qr, kr = torch.empty_like(q), torch.empty_like(k)
+    lib.mis_rope_qk(q, k, qr, kr, pos)
+    kr2 = torch.empty_like(k)
+    lib.mis_rope_qk(None, k, None, kr2, pos, Hq=hq)
+    assert torch.equal(kr, kr2)                      # the K-only pass gives the same K bits
+    plan = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, hq, hkv, D)
+    ws = torch.zeros(plan.workspace_size(), dtype=torch.uint8, device=dev)
+    plan.create(ws)
+    o1, o2 = torch.empty_like(q), torch.empty_like(q)
+    lib.mis_attention_fwd_plan(plan, qr, kr, vv, o1, None)
+    lib.mis_attention_fwd_plan_rope(plan, q, kr, vv, o2, None, pos, tab)
+    torch.cuda.synchronize()
+    assert lib.mis_get_device_status(ws) == lib.MIS_OK
+    assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
+
+
+def test_rope_table_values():
+    D, n, base = 128, 5000, 1.0e6
+    tab = torch.empty(n, D // 2, 2, dtype=torch.float32, device="cuda")
+    lib.mis_rope_table(tab, D, base)
+    torch.cuda.synchronize()
+    p = np.arange(n, dtype=np.float64)[:, None]
+    f = base ** (-2.0 * np.arange(D // 2, dtype=np.float64) / D)
+    got = f64(tab)
+    # fp64 angle and sine/cosine, rounded once to fp32
+    assert np.abs(got[..., 0] - np.cos(p * f)).max() <= 1e-7
+    assert np.abs(got[..., 1] - np.sin(p * f)).max() <= 1e-7
+
+
+def test_position_outside_the_table_is_reported():
+    # every position must index the table; one beyond it is flagged in the
+    # plan's device status (the row is left unrotated), the launch completes
+    s = synth.custom_shapes([200], [3], [10, 20, 30])
+    lay = lib.mis_build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+    hq, hkv, D = 4, 2, 64
+    dev = torch.device("cuda")
+    v = synth.draw_values(66, lay.T, hq, hkv, D, want=("q", "k", "v"))
+    q, k, vv = (v[x].to(dev) for x in ("q", "k", "v"))
+    pos = torch.as_tensor(lay.position_ids, device=dev)
+    tab = torch.empty(int(lay.position_ids.max()), D // 2, 2, dtype=torch.float32, device=dev)
+    lib.mis_rope_table(tab, D)                       # one row short of the largest position
+    plan = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, hq, hkv, D)
+    ws = torch.zeros(plan.workspace_size(), dtype=torch.uint8, device=dev)
+    plan.create(ws)
+    o = torch.empty_like(q)
+    lib.mis_attention_fwd_plan_rope(plan, q, k, vv, o, None, pos, tab)
+    torch.cuda.synchronize()
+    assert lib.mis_get_device_status(ws) == lib.MIS_ERR_DEVICE_INDEX
+    # the next launch on the same plan starts from a clean status
+    tab2 = torch.empty(int(lay.position_ids.max()) + 1, D // 2, 2, dtype=torch.float32, device=dev)
+    lib.mis_rope_table(tab2, D)
+    lib.mis_attention_fwd_plan_rope(plan, q, k, vv, o, None, pos, tab2)
+    torch.cuda.synchronize()
+    assert lib.mis_get_device_status(ws) == lib.MIS_OK
