@@ -127,41 +127,65 @@ struct AttnParams {
   int32_t rope_n;
 };
 
-// Rotary embedding of row r of a Q tile in shared memory, in place: NB boxes
-// of 128 rows x 64 bf16 columns with the 128-byte swizzle (16-byte chunk c of
-// row r at chunk c ^ (r & 7)). Rotate-half form: the pair (x[i], x[i + D/2])
-// turns by the angle of frequency i, whose (cos, sin) are tab[i]. Chunk pairs
-// g (frequencies 8g .. 8g+7) from g0 in steps of GS.
+// Rotary embedding of one warp's 32 rows of a Q tile in shared memory, in
+// place. The tile is NB boxes of 128 rows x 64 bf16 columns with the 128-byte
+// swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)). Rotate-half form:
+// the pair (x[i], x[i + D/2]) turns by the angle of frequency i. A "chunk
+// pair" g holds frequencies 8g .. 8g+7 (one 16-byte chunk of each half); this
+// warp turns the chunk pairs g0, g0 + GS, ... of rows r0 .. r0 + 31. Lanes
+// are laid out (row, chunk pair) so that a warp's table reads cover whole
+// table rows (coalesced) and its shared-memory accesses whole tile rows.
 template <int D, int GS>
-__device__ __forceinline__ void rope_row_smem(uint32_t sq, int r, const float4* __restrict__ tab,
-                                              int g0) {
-  constexpr int HALF = D / 2, BOX = kBN * 64 * 2;
-  const uint32_t row = sq + (uint32_t)r * 128u;
-  const int sw = r & 7;
+struct RopeWarp {
+  static constexpr int kCpr = D / 16 / GS;   // chunk pairs of a row this warp turns
+  static constexpr int kRpp = 32 / kCpr;     // rows per pass
+  static constexpr int kPasses = kCpr;       // 32 rows
+  float4 cs[kPasses][4];                     // (cos, sin) of the lane's 8 frequencies, per pass
+
+  // Table loads, issued before the tile lands. pos: the position of row
+  // r0 + lane, or -1 (row outside the request: turned by the identity).
+  __device__ __forceinline__ void load(const float4* __restrict__ tab, int pos, int g0) {
+    const int g = g0 + (threadIdx.x & 31) % kCpr * GS;
 #pragma unroll
-  for (int gi = 0; gi < D / 16 / GS; ++gi) {
-    const int g = g0 + gi * GS;
-    const int c1 = 8 * g, c2 = 8 * g + HALF;
-    const uint32_t a1 = row + (uint32_t)((c1 >> 6) * BOX) + ((((c1 & 63) >> 3) ^ sw) << 4);
-    const uint32_t a2 = row + (uint32_t)((c2 >> 6) * BOX) + ((((c2 & 63) >> 3) ^ sw) << 4);
-    uint32_t x[4], y[4];
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]) : "r"(a1) : "memory");
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(y[0]), "=r"(y[1]), "=r"(y[2]), "=r"(y[3]) : "r"(a2) : "memory");
-    uint32_t ox[4], oy[4];
+    for (int k = 0; k < kPasses; ++k) {
+      const int pk = __shfl_sync(0xffffffffu, pos, k * kRpp + (threadIdx.x & 31) / kCpr);
+      const float4* tr = tab + (size_t)max(pk, 0) * (D / 4) + 4 * g;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float4 cs = __ldg(tab + 4 * g + w);        // frequencies 8g + 2w, 8g + 2w + 1
-      const float x0 = __uint_as_float(x[w] << 16), x1 = __uint_as_float(x[w] & 0xffff0000u);
-      const float y0 = __uint_as_float(y[w] << 16), y1 = __uint_as_float(y[w] & 0xffff0000u);
-      ox[w] = pack_bf16(fmaf(x0, cs.x, -y0 * cs.y), fmaf(x1, cs.z, -y1 * cs.w));
-      oy[w] = pack_bf16(fmaf(y0, cs.x, x0 * cs.y), fmaf(y1, cs.z, x1 * cs.w));
+      for (int w = 0; w < 4; ++w) cs[k][w] = pk >= 0 ? __ldg(tr + w) : make_float4(1.f, 0.f, 1.f, 0.f);
     }
-    st_shared_v4(a1, ox[0], ox[1], ox[2], ox[3]);
-    st_shared_v4(a2, oy[0], oy[1], oy[2], oy[3]);
   }
-}
+
+  __device__ __forceinline__ void turn(uint32_t sq, int r0, int g0) const {
+    constexpr int HALF = D / 2, BOX = kBN * 64 * 2;
+    const int lane = threadIdx.x & 31;
+    const int g = g0 + lane % kCpr * GS;
+    const int c1 = 8 * g, c2 = 8 * g + HALF;
+#pragma unroll
+    for (int k = 0; k < kPasses; ++k) {
+      const int r = r0 + k * kRpp + lane / kCpr;
+      const uint32_t row = sq + (uint32_t)r * 128u;
+      const int sw = r & 7;
+      const uint32_t a1 = row + (uint32_t)((c1 >> 6) * BOX) + ((((c1 & 63) >> 3) ^ sw) << 4);
+      const uint32_t a2 = row + (uint32_t)((c2 >> 6) * BOX) + ((((c2 & 63) >> 3) ^ sw) << 4);
+      uint32_t x[4], y[4];
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]) : "r"(a1) : "memory");
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(y[0]), "=r"(y[1]), "=r"(y[2]), "=r"(y[3]) : "r"(a2) : "memory");
+      uint32_t ox[4], oy[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float4 c = cs[k][w];                   // frequencies 8g + 2w, 8g + 2w + 1
+        const float x0 = __uint_as_float(x[w] << 16), x1 = __uint_as_float(x[w] & 0xffff0000u);
+        const float y0 = __uint_as_float(y[w] << 16), y1 = __uint_as_float(y[w] & 0xffff0000u);
+        ox[w] = pack_bf16(fmaf(x0, c.x, -y0 * c.y), fmaf(x1, c.z, -y1 * c.w));
+        oy[w] = pack_bf16(fmaf(y0, c.x, x0 * c.y), fmaf(y1, c.z, x1 * c.w));
+      }
+      st_shared_v4(a1, ox[0], ox[1], ox[2], ox[3]);
+      st_shared_v4(a2, oy[0], oy[1], oy[2], oy[3]);
+    }
+  }
+};
 
 // Unit handled by this block in pass kk: walk position kk * G + c, passes
 // alternating direction (snake order), so over the longest-first unit list
@@ -450,22 +474,25 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
       const int lo = valid ? p.seg_start[j - p.qbase] : 0x7fffffff;
       const int nk = un.nk;
       if (p.rope_tab) {
-        // rotary embedding of this unit's Q on load: each thread turns its
-        // row (pair schedule: of its stream's head; split schedule: half the
-        // frequencies of the one head), then the MMA thread may read it
+        // rotary embedding of this unit's Q on load: each warp turns its 32
+        // rows (pair schedule: of its stream's head; split schedule: half the
+        // frequencies of the one head), then the MMA thread may read them.
+        // The positions and the table entries load while the tile lands.
         int pos = -1;
-        if (valid) pos = p.rope_pos[j - p.qbase];
+        if (valid) {
+          pos = p.rope_pos[j - p.qbase];
+          if (pos < 0 || pos >= p.rope_n) {
+            raise_status(p.status, kDevIndex, 0x5e0);
+            pos = -1;                   // left unrotated
+          }
+        }
+        RopeWarp<D, split ? 2 : 1> rw;
+        rw.load(p.rope_tab, pos, split ? t : 0);
         ok = wait<true>(bar(bQF), lu & 1, W, 0x5c0 + t);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        if (valid) {
-          if (pos >= 0 && pos < p.rope_n)
-            rope_row_smem<D, split ? 2 : 1>(smem_u32(sQ + (split ? 0 : t) * C::kTile), r,
-                                            p.rope_tab + (size_t)pos * (D / 4), split ? t : 0);
-          else
-            raise_status(p.status, kDevIndex, 0x5e0);
-        }
-        fence_proxy_async();            // the tensor core reads what this thread wrote
+        rw.turn(smem_u32(sQ + (split ? 0 : t) * C::kTile), sw * 32, split ? t : 0);
+        fence_proxy_async();            // the tensor core reads what this warp wrote
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(bQR));
       }

@@ -154,8 +154,16 @@ def _fused_case(shapes, hq, hkv, D, seed, base=1.0e6, n_extra=7, stride_pad=0):
     status = lib.mis_get_device_status(ws)
     assert torch.equal(q, q_before)                     # Q is rotated in shared memory only
     olay = O.build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
-    ro, rl = O.attention(O.rope(f64(v["q"]), olay.position_ids, base),
-                         O.rope(f64(v["k"]), olay.position_ids, base), f64(v["v"]), olay)
+    # the rotated Q and K are held in bf16 on the GPU (Q in shared memory, K
+    # in HBM): the oracle attends over the fp64 rotation rounded to bf16
+    # (nearest even) once, the storage precision the kernel decides in
+    bf = lambda x: torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    qr = O.rope(f64(v["q"]), olay.position_ids, base)
+    kr64 = O.rope(f64(v["k"]), olay.position_ids, base)
+    ro, rl = O.attention(bf(qr), bf(kr64), f64(v["v"]), olay)
+    # and over the exact rotation, for the output tolerance of the method
+    ro_exact, _ = O.attention(qr, kr64, f64(v["v"]), olay)
+    assert np.abs(f64(o) - ro_exact).max() <= ATTN_TOL
     return olay, o, lse, ro, rl, status, plan.stats()
 
 
