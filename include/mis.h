@@ -312,8 +312,9 @@ mis_status_t mis_attention_fwd_cached(mis_plan_t plan, const void* q, const void
  *   q_out, k_out  — device bf16 outputs in the same shapes; q_out == q and
  *                   k_out == k (same strides) rotate in place; other overlaps
  *                   are not allowed. q and q_out both NULL rotate K only (for
- *                   mis_attention_fwd_plan_rope, which rotates Q on load);
- *                   one of them NULL alone is MIS_ERR_INVALID_ARG
+ *                   mis_attention_fwd_plan_rope, which rotates Q on load;
+ *                   Hq is then only checked, >= 1); one of them NULL alone
+ *                   is MIS_ERR_INVALID_ARG
  *   position_ids  — device int32 [T]
  * fp32 arithmetic (angles from inverse frequencies computed in fp64 on the
  * host), bf16 results rounded to nearest even. One kernel launch, stream
@@ -325,42 +326,29 @@ mis_status_t mis_rope_qk(const void* q, const void* k, void* q_out, void* k_out,
                          const int32_t* position_ids, double base, void* stream);
 
 /* ------------------------------------------------------------------------
- * The rotary (cos, sin) table that mis_attention_fwd_plan_rope reads: for
- * every position p < n_positions and frequency i < D/2, the pair
- * (cos(p * base^(-2i/D)), sin(p * base^(-2i/D))), angle and sine/cosine in
- * fp64, stored as fp32. It depends on the model only (D, base) and the
- * largest position, so a caller builds it once and keeps it.
- *   table — device float [n_positions][D/2][2], 16-byte aligned, caller
- *           owned (n_positions * D * 4 bytes)
- * One kernel launch, stream ordered.
- * ------------------------------------------------------------------------ */
-mis_status_t mis_rope_table(float* table, int32_t D, int32_t n_positions, double base,
-                            void* stream);
-
-/* ------------------------------------------------------------------------
  * mis_attention_fwd_plan with the rotary embedding of Q fused in: Q arrives
  * unrotated and each unit's Q tile is turned in shared memory right after it
- * loads, at the row's position id ("From Generation to Scoring" Section 4.1:
- * the reused ids, query 0..S-1 and offset d of every item -> S + d, as
- * mis_build_layout emits them; "Turbocharging ...", section "SGLang
- * changes": positional encoding adjusted so each item aligns with its
- * single-item position). Same rotate-half form as mis_rope_qk. K must arrive
- * rotated already (mis_rope_qk with q = q_out = NULL); V is not rotated.
- *   position_ids — device int32 [T], 4-byte aligned
- *   rope_table   — the mis_rope_table() of this D and base, n_positions rows
- *   n_positions  — rows of the table; a position outside [0, n_positions)
- *                  leaves that row unrotated and raises MIS_ERR_DEVICE_INDEX
- *                  in the plan's device status
- * Everything else as mis_attention_fwd_plan (packed plans only; a cached
- * plan returns MIS_ERR_INVALID_ARG). Q is read once per unit and not
- * modified in global memory.
+ * loads, at the row's reused position id ("From Generation to Scoring"
+ * Section 4.1: rows of the shared set at 0..S-1, row d of every item set at
+ * S + d; exactly the ids mis_build_layout emits), derived from the plan, so
+ * every item is rotated as in its own single-item prompt ("Turbocharging
+ * ...", section "SGLang changes"). Same rotate-half form as mis_rope_qk:
+ * the pair (x[i], x[i + D/2]) turns by p * rope_base^(-2i/D), the angle in
+ * fp32 (frequencies computed in fp64 on the host), its sine and cosine
+ * evaluated on the device after an exact reduction to [-pi, pi]; the turned
+ * tile is rounded to bf16 (nearest even) before the products, as a rotated
+ * Q in memory would be. K must arrive rotated already (mis_rope_qk with
+ * q = q_out = NULL and the layout's position ids); V is not rotated.
+ *   rope_base — > 1 (1e6 for the Qwen3 family)
+ * Requests longer than 2^17 rows return MIS_ERR_UNSUPPORTED. Everything
+ * else as mis_attention_fwd_plan (packed plans only; a cached plan returns
+ * MIS_ERR_INVALID_ARG). Q in global memory is read, never written.
  * ------------------------------------------------------------------------ */
 mis_status_t mis_attention_fwd_plan_rope(mis_plan_t plan, const void* q, const void* k,
                                          const void* v, void* o, float* lse,
                                          int64_t q_row_stride, int64_t k_row_stride,
                                          int64_t v_row_stride, int64_t o_row_stride,
-                                         const int32_t* position_ids, const float* rope_table,
-                                         int32_t n_positions, void* stream);
+                                         double rope_base, void* stream);
 
 /* ------------------------------------------------------------------------
  * Label scoring at the readout rows ("From Generation to Scoring", Section

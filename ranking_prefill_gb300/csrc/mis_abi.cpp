@@ -6,6 +6,7 @@
 
 #include <atomic>
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -413,24 +414,25 @@ mis_status_t mis_attention_fwd_plan(mis_plan_t plan, const void* q, const void* 
 
 mis_status_t mis_attention_fwd_plan_rope(mis_plan_t plan, const void* q, const void* k,
                                          const void* v, void* o, float* lse, int64_t qs,
-                                         int64_t ks, int64_t vs, int64_t os,
-                                         const int32_t* position_ids, const float* rope_table,
-                                         int32_t n_positions, void* stream) {
+                                         int64_t ks, int64_t vs, int64_t os, double rope_base,
+                                         void* stream) {
   if (!plan) return MIS_ERR_INVALID_ARG;
   HostPlan& p = plan->p;
   if (p.cached) return MIS_ERR_INVALID_ARG;       // needs the cache buffers
   if (!p.workspace) return MIS_ERR_WORKSPACE;
-  if (!q || !k || !v || !o || !position_ids || !rope_table) return MIS_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(rope_table))
-    return MIS_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(position_ids) & 3u) ||
-      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
-    return MIS_ERR_INVALID_ARG;
-  if (n_positions < 1) return MIS_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o) return MIS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return MIS_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return MIS_ERR_INVALID_ARG;
+  if (!(rope_base > 1.0) || !std::isfinite(rope_base)) return MIS_ERR_INVALID_ARG;
+  // positions stay below the longest request's length, at most 2^17: the
+  // range reduction of the fp32 angle p * base^(-2i/D) is then exact
+  int64_t longest = 0;
+  for (const ReqInfo& r : p.req) longest = std::max<int64_t>(longest, r.e0 - r.s0);
+  if (longest > (1 << 17)) return MIS_ERR_UNSUPPORTED;
   const int64_t wq = (int64_t)p.Hq * p.D, wk = (int64_t)p.Hkv * p.D;
   if (qs < wq || os < wq || ks < wk || vs < wk) return MIS_ERR_SHAPE;
   if ((qs | ks | vs | os) & 7) return MIS_ERR_SHAPE;
-  const RopeQ rope{position_ids, rope_table, n_positions};
+  const RopeQ rope{rope_base};
   try {
     return launch_attention(p, q, k, v, nullptr, nullptr, o, lse, qs, ks, vs, 0, 0, os, stream,
                             &rope);

@@ -121,11 +121,24 @@ struct AttnParams {
   uint32_t* status;
   uint64_t wait_ns;
   uint32_t stall;         // failure injection: wait on a barrier nothing arrives on
-  // rotary embedding of Q on load (null rope_tab: Q arrives rotated)
-  const int32_t* rope_pos;  // [T] position of every (new) row
-  const float4* rope_tab;   // [rope_n][D/2] (cos, sin) pairs, two frequencies per float4
-  int32_t rope_n;
+  // rotary embedding of Q on load (rope == 0: Q arrives rotated)
+  int32_t rope;
+  float rope_freq[64];      // base^(-2i/D), i < D/2 (fp64 on the host, rounded to fp32)
 };
+
+// sin and cos of x (|x| < 2^16 * pi): x is reduced to r in [-pi, pi] by the
+// Cody-Waite method (2 pi split into a high part exact in 8 bits, so k * high
+// is exact for k < 2^16, and the fp32 remainder), then the SFU's sin/cos
+// approximations, whose absolute error on [-pi, pi] is about 2^-21.
+__device__ __forceinline__ void sincos_reduced(float x, float& sn, float& cs) {
+  constexpr float kInv2Pi = 0.15915494309189535f;
+  constexpr float k2PiHi = 6.28125f;                          // 201 / 32
+  constexpr float k2PiLo = 0.0019353071795864769f;            // 2 pi - 6.28125
+  const float k = rintf(x * kInv2Pi);
+  const float r = fmaf(-k, k2PiLo, fmaf(-k, k2PiHi, x));
+  asm("sin.approx.f32 %0, %1;" : "=f"(sn) : "f"(r));
+  asm("cos.approx.f32 %0, %1;" : "=f"(cs) : "f"(r));
+}
 
 // Rotary embedding of one warp's 32 rows of a Q tile in shared memory, in
 // place. The tile is NB boxes of 128 rows x 64 bf16 columns with the 128-byte
@@ -140,18 +153,26 @@ struct RopeWarp {
   static constexpr int kCpr = D / 16 / GS;   // chunk pairs of a row this warp turns
   static constexpr int kRpp = 32 / kCpr;     // rows per pass
   static constexpr int kPasses = kCpr;       // 32 rows
-  float4 cs[kPasses][4];                     // (cos, sin) of the lane's 8 frequencies, per pass
+  float4 cs[kPasses][4];   // (cos, sin, cos, sin) of the lane's 8 frequencies, per pass
 
-  // Table loads, issued before the tile lands. pos: the position of row
-  // r0 + lane, or -1 (row outside the request: turned by the identity).
-  __device__ __forceinline__ void load(const float4* __restrict__ tab, int pos, int g0) {
+  // The angles of every pass, computed while the tile lands. pos: the
+  // position of row r0 + lane, or -1 (row outside the request: identity).
+  __device__ __forceinline__ void angles(const float* freq, int pos, int g0) {
     const int g = g0 + (threadIdx.x & 31) % kCpr * GS;
+    float f[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = freq[8 * g + e];
 #pragma unroll
     for (int k = 0; k < kPasses; ++k) {
       const int pk = __shfl_sync(0xffffffffu, pos, k * kRpp + (threadIdx.x & 31) / kCpr);
-      const float4* tr = tab + (size_t)max(pk, 0) * (D / 4) + 4 * g;
+      const float fp = (float)max(pk, 0);
 #pragma unroll
-      for (int w = 0; w < 4; ++w) cs[k][w] = pk >= 0 ? __ldg(tr + w) : make_float4(1.f, 0.f, 1.f, 0.f);
+      for (int w = 0; w < 4; ++w) {
+        float s0, c0, s1, c1;
+        sincos_reduced(fp * f[2 * w], s0, c0);
+        sincos_reduced(fp * f[2 * w + 1], s1, c1);
+        cs[k][w] = make_float4(c0, s0, c1, s1);
+      }
     }
   }
 
@@ -379,7 +400,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
           if (u < 0) continue;
           const int nk = p.units[u / n_hg].nk;
           // the unit's Q: landed, or landed and rotated by the softmax warps
-          if (!(ok = wait<true>(bar(p.rope_tab ? bQR : bQF), lu & 1, W, 0x200))) break;
+          if (!(ok = wait<true>(bar(p.rope ? bQR : bQF), lu & 1, W, 0x200))) break;
           // the first PV of stream t in this unit overwrites O_t: the epilogue of
           // the previous unit must have read it out of tensor memory. In the
           // split schedule one barrier covers both accumulators, and stream 0's
@@ -473,21 +494,17 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
       const int jj = valid ? j : -1;                    // invalid rows see nothing
       const int lo = valid ? p.seg_start[j - p.qbase] : 0x7fffffff;
       const int nk = un.nk;
-      if (p.rope_tab) {
+      if (p.rope) {
         // rotary embedding of this unit's Q on load: each warp turns its 32
         // rows (pair schedule: of its stream's head; split schedule: half the
         // frequencies of the one head), then the MMA thread may read them.
-        // The positions and the table entries load while the tile lands.
-        int pos = -1;
-        if (valid) {
-          pos = p.rope_pos[j - p.qbase];
-          if (pos < 0 || pos >= p.rope_n) {
-            raise_status(p.status, kDevIndex, 0x5e0);
-            pos = -1;                   // left unrotated
-          }
-        }
+        // Positions are the reused ids of Section 4.1 of "From Generation to
+        // Scoring": rows of the shared set count from 0 at the request's
+        // first row, row d of an item set sits at S + d. Their sines and
+        // cosines are computed while the tile lands.
+        const int pos = !valid ? -1 : (j < R.pend ? j - R.s0 : (R.pend - R.s0) + (j - lo));
         RopeWarp<D, split ? 2 : 1> rw;
-        rw.load(p.rope_tab, pos, split ? t : 0);
+        rw.angles(p.rope_freq, pos, split ? t : 0);
         ok = wait<true>(bar(bQF), lu & 1, W, 0x5c0 + t);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -827,9 +844,9 @@ mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
   prm.status = reinterpret_cast<uint32_t*>(ws);
   prm.wait_ns = wait_limit_ns();
   prm.stall = inject_stall_mask() & 1u;
-  prm.rope_pos = rope ? rope->pos : nullptr;
-  prm.rope_tab = rope ? reinterpret_cast<const float4*>(rope->tab) : nullptr;
-  prm.rope_n = rope ? rope->n : 0;
+  prm.rope = rope ? 1 : 0;
+  for (int i = 0; i < 64; ++i)
+    prm.rope_freq[i] = (rope && i < D / 2) ? (float)std::pow(rope->base, -2.0 * i / D) : 0.f;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (pl.status_clear) {

@@ -108,12 +108,10 @@ uint32_t inject_stall_mask();
 // Process-wide attention schedule override (MIS_SCHEDULE_*).
 int32_t schedule_override();
 
-// Rotary embedding of Q on load: the position of every (new) row and the
-// (cos, sin) table they index (device pointers, already validated).
+// Rotary embedding of Q on load at the reused position ids (the base of the
+// rotate-half frequencies base^(-2i/D)).
 struct RopeQ {
-  const int32_t* pos;
-  const float* tab;
-  int32_t n;
+  double base;
 };
 
 // Kernel launchers (defined in the .cu files). Return MIS_ERR_CUDA on launch

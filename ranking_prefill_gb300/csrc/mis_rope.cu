@@ -100,22 +100,6 @@ mis_rope_kernel(const RopeParams p) {
     rotate(p.k + t * p.ks + (int64_t)(h - p.Hq) * D, p.ko + t * p.kos + (int64_t)(h - p.Hq) * D);
 }
 
-// (cos, sin) of p * base^(-2i/D) for every position p < n and frequency
-// i < D/2, angles and their sine and cosine in fp64, stored as fp32 pairs.
-__global__ void __launch_bounds__(kRopeThreads)
-mis_rope_table_kernel(float2* __restrict__ tab, int32_t n, int32_t half, double log2_base) {
-  griddep_wait();
-  griddep_launch_dependents();
-  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (gid >= (int64_t)n * half) return;
-  const int i = (int)(gid % half);
-  const int64_t pos = gid / half;
-  const double f = exp2(-log2_base * (double)i / (double)half);
-  double sn, cs;
-  sincos((double)pos * f, &sn, &cs);
-  tab[gid] = make_float2((float)cs, (float)sn);
-}
-
 template <int D>
 mis_status_t launch_rope_d(RopeParams& p, double base, cudaStream_t st) {
   for (int i = 0; i < D / 2; ++i) p.inv_freq[i] = (float)std::pow(base, -2.0 * i / D);
@@ -178,23 +162,3 @@ extern "C" mis_status_t mis_rope_qk(const void* q, const void* k, void* q_out, v
   }
 }
 
-extern "C" mis_status_t mis_rope_table(float* table, int32_t D, int32_t n_positions, double base,
-                                       void* stream) {
-  using namespace mis;
-  if (D != 64 && D != 128) return MIS_ERR_UNSUPPORTED;
-  if (n_positions < 1 || !table) return MIS_ERR_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(table) & 15u) return MIS_ERR_INVALID_ARG;
-  if (!(base > 1.0) || !std::isfinite(base)) return MIS_ERR_INVALID_ARG;
-  const int64_t cells = (int64_t)n_positions * (D / 2);
-  const int64_t blocks = (cells + kRopeThreads - 1) / kRopeThreads;
-  if (blocks > 0x7fffffff) return MIS_ERR_UNSUPPORTED;
-  try {
-    return launch_pdl(mis_rope_table_kernel, dim3((unsigned)blocks), dim3(kRopeThreads), 0,
-                      static_cast<cudaStream_t>(stream), reinterpret_cast<float2*>(table),
-                      n_positions, D / 2, std::log2(base)) == cudaSuccess
-               ? MIS_OK
-               : MIS_ERR_CUDA;
-  } catch (...) {
-    return MIS_ERR_CUDA;
-  }
-}

@@ -36,7 +36,7 @@ EXPORTS = ["mis_status_string", "mis_abi_version", "mis_layout_size", "mis_build
            "mis_inject_stall", "mis_planner_create", "mis_planner_plan", "mis_planner_destroy",
            "mis_set_schedule", "mis_setwise_layout_size", "mis_build_setwise_layout",
            "mis_rope_qk", "mis_cached_plan_workspace_size", "mis_cached_plan_create",
-           "mis_attention_fwd_cached", "mis_rope_table", "mis_attention_fwd_plan_rope"]
+           "mis_attention_fwd_cached", "mis_attention_fwd_plan_rope"]
 
 
 class MisError(RuntimeError):
@@ -111,9 +111,8 @@ def load(path: str = LIB_PATH):
                                                i64, i64, vp]),
         "mis_rope_qk": (C.c_int, [vp, vp, vp, vp, i64, i64, i64, i64, C.c_int32, C.c_int32,
                                   C.c_int32, C.c_int32, vp, C.c_double, vp]),
-        "mis_rope_table": (C.c_int, [vp, C.c_int32, C.c_int32, C.c_double, vp]),
         "mis_attention_fwd_plan_rope": (C.c_int, [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64,
-                                                  vp, vp, C.c_int32, vp]),
+                                                  C.c_double, vp]),
         "mis_setwise_layout_size": (C.c_int, [C.c_int32, i32p, i32p, i32p, C.POINTER(i64),
                                               C.POINTER(i64)]),
         "mis_build_setwise_layout": (C.c_int, [C.c_int32, i32p, i32p, i32p, i32p, i32p, i32p,
@@ -484,23 +483,14 @@ def mis_rope_qk(q, k, q_out, k_out, position_ids, base: float = 1.0e6, stream=No
                          float(base), _stream(stream)), "mis_rope_qk")
 
 
-def mis_rope_table(table, D: int, base: float = 1.0e6, stream=None):
-    """Fill `table` (device float32 [n_positions, D/2, 2]) with the rotary
-    (cos, sin) pairs of every position and frequency."""
-    L = load()
-    n = int(table.shape[0])
-    _check(L.mis_rope_table(_dptr(table), D, n, float(base), _stream(stream)), "mis_rope_table")
-
-
-def mis_attention_fwd_plan_rope(plan: "Plan", q, k, v, o, lse, position_ids, rope_table,
+def mis_attention_fwd_plan_rope(plan: "Plan", q, k, v, o, lse=None, base: float = 1.0e6,
                                 stream=None):
-    """mis_attention_fwd_plan with Q rotated on load at `position_ids` (device
-    int32 [T]) from `rope_table` (mis_rope_table); K arrives rotated."""
+    """mis_attention_fwd_plan with Q rotated on load at the reused position
+    ids (derived from the plan); K arrives rotated."""
     L = load()
     _check(L.mis_attention_fwd_plan_rope(plan._h, _dptr(q), _dptr(k), _dptr(v), _dptr(o),
                                          _dptr(lse), q.stride(0), k.stride(0), v.stride(0),
-                                         o.stride(0), _dptr(position_ids), _dptr(rope_table),
-                                         int(rope_table.shape[0]), _stream(stream)),
+                                         o.stride(0), float(base), _stream(stream)),
            "mis_attention_fwd_plan_rope")
 
 

@@ -250,20 +250,15 @@ def test_rope_argument_checks(L):
     assert call(q=None, qo=None, ks=8 * 128 - 8) == lib.MIS_ERR_SHAPE
 
 
-def test_rope_table_and_fused_attention_argument_checks(L):
+def test_fused_rope_attention_argument_checks(L):
     fake = C.c_void_p(1 << 20)
-    assert L.mis_rope_table(fake, 96, 10, 1e6, None) == lib.MIS_ERR_UNSUPPORTED
-    assert L.mis_rope_table(fake, 128, 0, 1e6, None) == lib.MIS_ERR_INVALID_ARG
-    assert L.mis_rope_table(None, 128, 10, 1e6, None) == lib.MIS_ERR_INVALID_ARG
-    assert L.mis_rope_table(C.c_void_p((1 << 20) + 4), 128, 10, 1e6, None) == lib.MIS_ERR_INVALID_ARG
-    assert L.mis_rope_table(fake, 128, 10, 0.5, None) == lib.MIS_ERR_INVALID_ARG
     s = synth.custom_shapes([130], [3], [10, 20, 30])
     lay = lib.mis_build_layout(s.prefix_tokens, s.n_items, s.item_lens)
     args = (lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, 4, 2, 64)
     host = lib.Plan.host_only(*args)
     strides = (4 * 64, 2 * 64, 2 * 64, 4 * 64)
-    call = lambda h, pos=fake, tab=fake, n=10: L.mis_attention_fwd_plan_rope(
-        h, fake, fake, fake, fake, None, *strides, pos, tab, n, None)
+    call = lambda h, base=1e6: L.mis_attention_fwd_plan_rope(h, fake, fake, fake, fake, None,
+                                                             *strides, base, None)
     assert call(None) == lib.MIS_ERR_INVALID_ARG
     assert call(host._h) == lib.MIS_ERR_WORKSPACE                 # no device workspace
     cl = O.cached_layout([0], [10], [2], [3, 4])

@@ -123,9 +123,10 @@ def schedule(request):
         yield request.param
 
 
-def _fused_case(shapes, hq, hkv, D, seed, base=1.0e6, n_extra=7, stride_pad=0):
+def _fused_case(shapes, hq, hkv, D, seed, base=1.0e6, stride_pad=0):
     """Q unrotated through mis_attention_fwd_plan_rope, K rotated by the K-only
-    mis_rope_qk; returns (oracle layout, O, LSE, oracle O, oracle LSE, status)."""
+    mis_rope_qk at the layout's position ids; returns (oracle layout, O, LSE,
+    oracle O, oracle LSE, status, plan stats)."""
     lay = lib.mis_build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
     v = synth.draw_values(seed, lay.T, hq, hkv, D, want=("q", "k", "v"))
     dev = torch.device("cuda")
@@ -139,9 +140,6 @@ def _fused_case(shapes, hq, hkv, D, seed, base=1.0e6, n_extra=7, stride_pad=0):
     q, k, vv = place(v["q"], hq), place(v["k"], hkv), place(v["v"], hkv)
     q_before = q.clone()
     pos = torch.as_tensor(lay.position_ids, device=dev)
-    n_pos = int(lay.position_ids.max()) + 1 + n_extra
-    tab = torch.empty(n_pos, D // 2, 2, dtype=torch.float32, device=dev)
-    lib.mis_rope_table(tab, D, base)
     kr = place(torch.zeros_like(v["k"]), hkv)
     lib.mis_rope_qk(None, k, None, kr, pos, base, Hq=hq)
     o = torch.full((T, hq, D), 7.0, dtype=torch.bfloat16, device=dev)
@@ -149,7 +147,7 @@ def _fused_case(shapes, hq, hkv, D, seed, base=1.0e6, n_extra=7, stride_pad=0):
     plan = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, hq, hkv, D)
     ws = torch.zeros(plan.workspace_size(), dtype=torch.uint8, device=dev)
     plan.create(ws)
-    lib.mis_attention_fwd_plan_rope(plan, q, kr, vv, o, lse, pos, tab)
+    lib.mis_attention_fwd_plan_rope(plan, q, kr, vv, o, lse, base)
     torch.cuda.synchronize()
     status = lib.mis_get_device_status(ws)
     assert torch.equal(q, q_before)                     # Q is rotated in shared memory only
@@ -167,13 +165,13 @@ def _fused_case(shapes, hq, hkv, D, seed, base=1.0e6, n_extra=7, stride_pad=0):
     return olay, o, lse, ro, rl, status, plan.stats()
 
 
-@pytest.mark.parametrize("hq,hkv,D,seed", [(8, 2, 128, 61), (4, 2, 64, 62), (6, 2, 128, 63),
-                                           (16, 8, 128, 64)])
-def test_q_rotated_on_load_matches_oracle(hq, hkv, D, seed, schedule):
+@pytest.mark.parametrize("hq,hkv,D,seed,base", [(8, 2, 128, 61, 1e6), (4, 2, 64, 62, 1e4),
+                                                (6, 2, 128, 63, 5e5), (16, 8, 128, 64, 1e6)])
+def test_q_rotated_on_load_matches_oracle(hq, hkv, D, seed, base, schedule):
     # several tiles, ragged tails, empty items, long items straddling tiles
     s = synth.custom_shapes([300, 40, 700], [6, 3, 9],
                             [12, 0, 40, 7, 130, 2, 25, 1, 60, 3, 3, 200, 64, 0, 9, 77, 5, 31])
-    olay, o, lse, ro, rl, status, st = _fused_case(s, hq, hkv, D, seed)
+    olay, o, lse, ro, rl, status, st = _fused_case(s, hq, hkv, D, seed, base)
     assert status == lib.MIS_OK
     assert np.abs(f64(o) - ro).max() <= ATTN_TOL
     assert np.abs(f64(lse).T - rl).max() <= 2e-3
@@ -187,6 +185,16 @@ def test_q_rotated_on_load_strided_and_qwen3_layer(schedule):
                                                   w.seed, stride_pad=8)
     assert status == lib.MIS_OK
     assert np.abs(f64(o) - ro).max() <= ATTN_TOL
+    assert np.abs(f64(lse).T - rl).max() <= 2e-3
+
+
+def test_q_rotated_on_load_long_positions(schedule):
+    # a 12k-token shared set: angles up to 12,000 rad, reduced on the device
+    s = synth.custom_shapes([12000], [5], [150, 3, 0, 64, 100])
+    olay, o, lse, ro, rl, status, _ = _fused_case(s, 4, 2, 128, 67)
+    assert status == lib.MIS_OK
+    assert np.abs(f64(o) - ro).max() <= ATTN_TOL
+    assert np.abs(f64(lse).T - rl).max() <= 2e-3
 
 
 def test_q_rotated_on_load_equals_rotating_first():
@@ -199,8 +207,6 @@ def test_q_rotated_on_load_equals_rotating_first():
     dev = torch.device("cuda")
     q, k, vv = (v[x].to(dev) for x in ("q", "k", "v"))
     pos = torch.as_tensor(lay.position_ids, device=dev)
-    tab = torch.empty(int(lay.position_ids.max()) + 1, D // 2, 2, dtype=torch.float32, device=dev)
-    lib.mis_rope_table(tab, D)
     qr, kr = torch.empty_like(q), torch.empty_like(k)
     lib.mis_rope_qk(q, k, qr, kr, pos)
     kr2 = torch.empty_like(k)
@@ -211,47 +217,23 @@ def test_q_rotated_on_load_equals_rotating_first():
     plan.create(ws)
     o1, o2 = torch.empty_like(q), torch.empty_like(q)
     lib.mis_attention_fwd_plan(plan, qr, kr, vv, o1, None)
-    lib.mis_attention_fwd_plan_rope(plan, q, kr, vv, o2, None, pos, tab)
+    lib.mis_attention_fwd_plan_rope(plan, q, kr, vv, o2, None)
     torch.cuda.synchronize()
     assert lib.mis_get_device_status(ws) == lib.MIS_OK
     assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
 
 
-def test_rope_table_values():
-    D, n, base = 128, 5000, 1.0e6
-    tab = torch.empty(n, D // 2, 2, dtype=torch.float32, device="cuda")
-    lib.mis_rope_table(tab, D, base)
-    torch.cuda.synchronize()
-    p = np.arange(n, dtype=np.float64)[:, None]
-    f = base ** (-2.0 * np.arange(D // 2, dtype=np.float64) / D)
-    got = f64(tab)
-    # fp64 angle and sine/cosine, rounded once to fp32
-    assert np.abs(got[..., 0] - np.cos(p * f)).max() <= 1e-7
-    assert np.abs(got[..., 1] - np.sin(p * f)).max() <= 1e-7
-
-
-def test_position_outside_the_table_is_reported():
-    # every position must index the table; one beyond it is flagged in the
-    # plan's device status (the row is left unrotated), the launch completes
-    s = synth.custom_shapes([200], [3], [10, 20, 30])
-    lay = lib.mis_build_layout(s.prefix_tokens, s.n_items, s.item_lens)
-    hq, hkv, D = 4, 2, 64
+def test_fused_rope_refuses_requests_beyond_its_position_range():
+    s = synth.custom_shapes([(1 << 17)], [0], [])
+    lay = lib.mis_build_layout(s.prefix_tokens, s.n_items, s.item_lens, with_positions=False)
     dev = torch.device("cuda")
-    v = synth.draw_values(66, lay.T, hq, hkv, D, want=("q", "k", "v"))
-    q, k, vv = (v[x].to(dev) for x in ("q", "k", "v"))
-    pos = torch.as_tensor(lay.position_ids, device=dev)
-    tab = torch.empty(int(lay.position_ids.max()), D // 2, 2, dtype=torch.float32, device=dev)
-    lib.mis_rope_table(tab, D)                       # one row short of the largest position
-    plan = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, hq, hkv, D)
+    plan = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, 2, 2, 64)
     ws = torch.zeros(plan.workspace_size(), dtype=torch.uint8, device=dev)
     plan.create(ws)
-    o = torch.empty_like(q)
-    lib.mis_attention_fwd_plan_rope(plan, q, k, vv, o, None, pos, tab)
+    q = torch.zeros(lay.T, 2, 64, dtype=torch.bfloat16, device=dev)
+    o = torch.full_like(q, 7.0)
+    with pytest.raises(lib.MisError) as e:
+        lib.mis_attention_fwd_plan_rope(plan, q, q, q, o, None)
+    assert e.value.status == lib.MIS_ERR_UNSUPPORTED
     torch.cuda.synchronize()
-    assert lib.mis_get_device_status(ws) == lib.MIS_ERR_DEVICE_INDEX
-    # the next launch on the same plan starts from a clean status
-    tab2 = torch.empty(int(lay.position_ids.max()) + 1, D // 2, 2, dtype=torch.float32, device=dev)
-    lib.mis_rope_table(tab2, D)
-    lib.mis_attention_fwd_plan_rope(plan, q, k, vv, o, None, pos, tab2)
-    torch.cuda.synchronize()
-    assert lib.mis_get_device_status(ws) == lib.MIS_OK
+    assert bool((o == 7.0).all())                    # nothing was launched
