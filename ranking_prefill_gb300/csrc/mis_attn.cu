@@ -140,38 +140,43 @@ __device__ __forceinline__ void sincos_reduced(float x, float& sn, float& cs) {
   asm("cos.approx.f32 %0, %1;" : "=f"(cs) : "f"(r));
 }
 
-// Rotary embedding of one warp's 32 rows of a Q tile in shared memory, in
-// place. The tile is NB boxes of 128 rows x 64 bf16 columns with the 128-byte
-// swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)). Rotate-half form:
+// Rotary embedding of ROWS rows of NH Q tiles (heads at the same rows) in
+// shared memory, in place, by one warp. A tile is NB boxes of 128 rows x 64
+// bf16 columns with the 128-byte swizzle (16-byte chunk c of row r at chunk
+// c ^ (r & 7)); tile h starts kTileBytes after tile h - 1. Rotate-half form:
 // the pair (x[i], x[i + D/2]) turns by the angle of frequency i. A "chunk
-// pair" g holds frequencies 8g .. 8g+7 (one 16-byte chunk of each half); this
-// warp turns the chunk pairs g0, g0 + GS, ... of rows r0 .. r0 + 31. Lanes
-// are laid out (row, chunk pair) so that a warp's table reads cover whole
-// table rows (coalesced) and its shared-memory accesses whole tile rows.
-template <int D, int GS>
+// pair" g holds frequencies 8g .. 8g+7 (one 16-byte chunk of each half);
+// this warp turns the chunk pairs g0, g0 + GS, ... of rows r0 .. r0+ROWS-1.
+// Lanes are laid out (row, chunk pair), so a warp's shared-memory accesses
+// cover whole tile rows, and each angle is computed once for the NH heads.
+template <int D, int GS, int NH, int ROWS>
 struct RopeWarp {
   static constexpr int kCpr = D / 16 / GS;   // chunk pairs of a row this warp turns
   static constexpr int kRpp = 32 / kCpr;     // rows per pass
-  static constexpr int kPasses = kCpr;       // 32 rows
+  static constexpr int kPasses = ROWS / kRpp;
+  static constexpr int kTileBytes = kBM * D * 2;
+  static_assert(ROWS % kRpp == 0, "rows per warp");
   float4 cs[kPasses][4];   // (cos, sin, cos, sin) of the lane's 8 frequencies, per pass
 
-  // The angles of every pass, computed while the tile lands. pos: the
-  // position of row r0 + lane, or -1 (row outside the request: identity).
+  // The angles of every pass, computed while the tiles land. pos: the
+  // position of row r0 + lane % ROWS, or -1 (row outside the request: the
+  // identity).
   __device__ __forceinline__ void angles(const float* freq, int pos, int g0) {
-    const int g = g0 + (threadIdx.x & 31) % kCpr * GS;
+    const int lane = threadIdx.x & 31;
+    const int g = g0 + lane % kCpr * GS;
     float f[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) f[e] = freq[8 * g + e];
 #pragma unroll
     for (int k = 0; k < kPasses; ++k) {
-      const int pk = __shfl_sync(0xffffffffu, pos, k * kRpp + (threadIdx.x & 31) / kCpr);
+      const int pk = __shfl_sync(0xffffffffu, pos, k * kRpp + lane / kCpr);
       const float fp = (float)max(pk, 0);
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         float s0, c0, s1, c1;
         sincos_reduced(fp * f[2 * w], s0, c0);
         sincos_reduced(fp * f[2 * w + 1], s1, c1);
-        cs[k][w] = make_float4(c0, s0, c1, s1);
+        cs[k][w] = pk >= 0 ? make_float4(c0, s0, c1, s1) : make_float4(1.f, 0.f, 1.f, 0.f);
       }
     }
   }
@@ -186,24 +191,29 @@ struct RopeWarp {
       const int r = r0 + k * kRpp + lane / kCpr;
       const uint32_t row = sq + (uint32_t)r * 128u;
       const int sw = r & 7;
-      const uint32_t a1 = row + (uint32_t)((c1 >> 6) * BOX) + ((((c1 & 63) >> 3) ^ sw) << 4);
-      const uint32_t a2 = row + (uint32_t)((c2 >> 6) * BOX) + ((((c2 & 63) >> 3) ^ sw) << 4);
-      uint32_t x[4], y[4];
-      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]) : "r"(a1) : "memory");
-      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(y[0]), "=r"(y[1]), "=r"(y[2]), "=r"(y[3]) : "r"(a2) : "memory");
-      uint32_t ox[4], oy[4];
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float4 c = cs[k][w];                   // frequencies 8g + 2w, 8g + 2w + 1
-        const float x0 = __uint_as_float(x[w] << 16), x1 = __uint_as_float(x[w] & 0xffff0000u);
-        const float y0 = __uint_as_float(y[w] << 16), y1 = __uint_as_float(y[w] & 0xffff0000u);
-        ox[w] = pack_bf16(fmaf(x0, c.x, -y0 * c.y), fmaf(x1, c.z, -y1 * c.w));
-        oy[w] = pack_bf16(fmaf(y0, c.x, x0 * c.y), fmaf(y1, c.z, x1 * c.w));
+      for (int h = 0; h < NH; ++h) {
+        const uint32_t a1 = row + (uint32_t)(h * kTileBytes + (c1 >> 6) * BOX) +
+                            ((((c1 & 63) >> 3) ^ sw) << 4);
+        const uint32_t a2 = row + (uint32_t)(h * kTileBytes + (c2 >> 6) * BOX) +
+                            ((((c2 & 63) >> 3) ^ sw) << 4);
+        uint32_t x[4], y[4];
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]) : "r"(a1) : "memory");
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(y[0]), "=r"(y[1]), "=r"(y[2]), "=r"(y[3]) : "r"(a2) : "memory");
+        uint32_t ox[4], oy[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float4 c = cs[k][w];                 // frequencies 8g + 2w, 8g + 2w + 1
+          const float x0 = __uint_as_float(x[w] << 16), x1 = __uint_as_float(x[w] & 0xffff0000u);
+          const float y0 = __uint_as_float(y[w] << 16), y1 = __uint_as_float(y[w] & 0xffff0000u);
+          ox[w] = pack_bf16(fmaf(x0, c.x, -y0 * c.y), fmaf(x1, c.z, -y1 * c.w));
+          oy[w] = pack_bf16(fmaf(y0, c.x, x0 * c.y), fmaf(y1, c.z, x1 * c.w));
+        }
+        st_shared_v4(a1, ox[0], ox[1], ox[2], ox[3]);
+        st_shared_v4(a2, oy[0], oy[1], oy[2], oy[3]);
       }
-      st_shared_v4(a1, ox[0], ox[1], ox[2], ox[3]);
-      st_shared_v4(a2, oy[0], oy[1], oy[2], oy[3]);
     }
   }
 };
@@ -495,20 +505,28 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
       const int lo = valid ? p.seg_start[j - p.qbase] : 0x7fffffff;
       const int nk = un.nk;
       if (p.rope) {
-        // rotary embedding of this unit's Q on load: each warp turns its 32
-        // rows (pair schedule: of its stream's head; split schedule: half the
-        // frequencies of the one head), then the MMA thread may read them.
-        // Positions are the reused ids of Section 4.1 of "From Generation to
-        // Scoring": rows of the shared set count from 0 at the request's
-        // first row, row d of an item set sits at S + d. Their sines and
-        // cosines are computed while the tile lands.
-        const int pos = !valid ? -1 : (j < R.pend ? j - R.s0 : (R.pend - R.s0) + (j - lo));
-        RopeWarp<D, split ? 2 : 1> rw;
+        // rotary embedding of this unit's Q on load, then the MMA thread may
+        // read it. Pair schedule: stream t's warps turn rows [64t, 64t + 64)
+        // of both heads (16 rows a warp); split schedule: stream t's warps
+        // turn half the frequencies of all 128 rows of the one head. Either
+        // way every angle is computed once. Positions are the reused ids of
+        // Section 4.1 of "From Generation to Scoring": rows of the shared set
+        // count from 0 at the request's first row, row d of an item set sits
+        // at S + d. Their sines and cosines are computed while the tiles land.
+        constexpr int ROWS = split ? 32 : 16;
+        const int rr0 = split ? sw * 32 : 64 * t + 16 * sw;
+        const int jr = un.q0 + rr0 + lane % ROWS;
+        int pos = -1;
+        if (jr < R.e0) {
+          const int lor = split ? lo : p.seg_start[jr - p.qbase];
+          pos = jr < R.pend ? jr - R.s0 : (R.pend - R.s0) + (jr - lor);
+        }
+        RopeWarp<D, split ? 2 : 1, split ? 1 : 2, ROWS> rw;
         rw.angles(p.rope_freq, pos, split ? t : 0);
         ok = wait<true>(bar(bQF), lu & 1, W, 0x5c0 + t);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        rw.turn(smem_u32(sQ + (split ? 0 : t) * C::kTile), sw * 32, split ? t : 0);
+        rw.turn(smem_u32(sQ), rr0, split ? t : 0);
         fence_proxy_async();            // the tensor core reads what this warp wrote
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(bQR));
