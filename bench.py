@@ -264,14 +264,14 @@ def measure(args, name, rank, world, dist, dev, local, full):
     out = torch.empty(M, K, dtype=torch.float32, device=dev)
     lay0 = HostLayout(w, shapes)
     plan0 = lib.Plan(*lay0.plan_args(), w.hq, w.hkv, w.head_dim)
-    # two plan workspaces, each followed by its batch's readout rows (and, with
-    # --rope, its position ids), uploaded together: the plan of step i+1
-    # travels on a copy stream while step i computes, as in a serving loop
+    # two plan workspaces, each followed by its batch's readout rows, uploaded
+    # together: the plan of step i+1 travels on a copy stream while step i
+    # computes, as in a serving loop (with --rope the position ids come from
+    # the plan itself)
     wsz = plan0.workspace_size()
-    n_extra = M + (T if args.rope else 0)
+    n_extra = M
     ws_plans = [torch.zeros(wsz + 4 * n_extra, dtype=torch.uint8, device=dev) for _ in range(2)]
     delim_devs = [wp[wsz:wsz + 4 * M].view(torch.int32) for wp in ws_plans]
-    pos_devs = [wp[wsz + 4 * M:wsz + 4 * n_extra].view(torch.int32) for wp in ws_plans]
     kr = torch.empty_like(k) if args.rope else k
     ws_score = torch.zeros(lib.mis_label_scores_workspace_size(M, w.d_model, w.vocab, K),
                            dtype=torch.uint8, device=dev)
@@ -291,8 +291,8 @@ def measure(args, name, rank, world, dist, dev, local, full):
         upload of the plan and the readout rows into workspace i % 2 on the
         copy stream; `after`: an event of the step during which it travels."""
         s = i % 2
-        lay = HostLayout(w, shapes, with_positions=args.rope)
-        extra = np.concatenate([lay.readout, lay.position_ids]) if args.rope else lay.readout
+        lay = HostLayout(w, shapes)
+        extra = lay.readout
         with torch.cuda.stream(copy_stream):
             if after is not None:
                 copy_stream.wait_event(after)
@@ -312,10 +312,11 @@ def measure(args, name, rank, world, dist, dev, local, full):
         stream.wait_event(uploaded[s])
         if "a0" in t:
             t["a0"].record(stream)
-        # (with --rope) rotary embedding at the reused position ids: K in its
-        # own pass, Q inside the attention kernel as each tile loads
+        # (with --rope) rotary embedding at the reused position ids, which
+        # both kernels derive from the plan: K in its own pass, Q inside the
+        # attention kernel as each tile loads
         if args.rope:
-            lib.mis_rope_qk(None, k, None, kr, pos_devs[s], stream=sp, Hq=w.hq)
+            lib.mis_rope_k_plan(plan, k, kr, 1.0e6, stream=sp)
             if "r1" in t:
                 t["r1"].record(stream)
             # a3: MIS attention, Q rotated on load
@@ -455,7 +456,7 @@ def measure(args, name, rank, world, dist, dev, local, full):
     }
     if args.rope:
         t_rope = statistics.mean(rope_ms) / 1e3
-        rope_bytes = T * w.hkv * w.head_dim * 2 * 2 + T * 4
+        rope_bytes = T * w.hkv * w.head_dim * 2 * 2
         result["rope"] = {"ms": round(t_rope * 1e3, 4), "bytes": rope_bytes,
                           "hbm_gbs": round(rope_bytes / t_rope / 1e9, 1),
                           "frac_of_hbm_peak": round(rope_bytes / t_rope / 1e9 / peaks["hbm_gbs"], 4),

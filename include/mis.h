@@ -326,6 +326,23 @@ mis_status_t mis_rope_qk(const void* q, const void* k, void* q_out, void* k_out,
                          const int32_t* position_ids, double base, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Rotary embedding of K alone at a plan's reused position ids (the same ids
+ * mis_build_layout emits, derived on the device from the plan: rows of the
+ * shared set at 0..S-1, row d of every item set at S + d), the companion of
+ * mis_attention_fwd_plan_rope: no position ids travel to the device.
+ * Rotate-half form and precision as mis_rope_qk.
+ *   plan          — a plan with its device workspace (mis_plan_create or the
+ *                   planner); packed or cached (K of the new rows)
+ *   k, k_out      — device bf16 [T, Hkv, D], row strides in elements (>=
+ *                   Hkv*D, multiples of 8), 16-byte aligned; k_out == k with
+ *                   equal strides rotates in place
+ * One kernel launch (one block per 128-row query tile), stream ordered after
+ * the plan upload.
+ * ------------------------------------------------------------------------ */
+mis_status_t mis_rope_k_plan(mis_plan_t plan, const void* k, void* k_out, int64_t k_row_stride,
+                             int64_t k_out_row_stride, double base, void* stream);
+
+/* ------------------------------------------------------------------------
  * mis_attention_fwd_plan with the rotary embedding of Q fused in: Q arrives
  * unrotated and each unit's Q tile is turned in shared memory right after it
  * loads, at the row's reused position id ("From Generation to Scoring"
@@ -337,8 +354,9 @@ mis_status_t mis_rope_qk(const void* q, const void* k, void* q_out, void* k_out,
  * fp32 (frequencies computed in fp64 on the host), its sine and cosine
  * evaluated on the device after an exact reduction to [-pi, pi]; the turned
  * tile is rounded to bf16 (nearest even) before the products, as a rotated
- * Q in memory would be. K must arrive rotated already (mis_rope_qk with
- * q = q_out = NULL and the layout's position ids); V is not rotated.
+ * Q in memory would be. K must arrive rotated already (mis_rope_k_plan on
+ * the same plan, or mis_rope_qk with q = q_out = NULL and the layout's
+ * position ids); V is not rotated.
  *   rope_base — > 1 (1e6 for the Qwen3 family)
  * Requests longer than 2^17 rows return MIS_ERR_UNSUPPORTED. Everything
  * else as mis_attention_fwd_plan (packed plans only; a cached plan returns

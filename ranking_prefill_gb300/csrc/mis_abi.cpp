@@ -139,6 +139,8 @@ struct mis_plan_s {
   mis::HostPlan p;
 };
 
+const mis::HostPlan& mis::plan_of(mis_plan_t plan) { return plan->p; }
+
 using namespace mis;
 
 extern "C" {

@@ -70,6 +70,9 @@ struct HostPlan {
   int32_t qbase = 0;
 };
 
+// The host plan behind a C-ABI plan handle.
+const HostPlan& plan_of(mis_plan_t plan);
+
 // Validates a cached-prefix descriptor and fills the plan (cached = true).
 mis_status_t build_plan_cached(const mis_cached_desc* d, HostPlan* p);
 

@@ -100,6 +100,60 @@ mis_rope_kernel(const RopeParams p) {
     rotate(p.k + t * p.ks + (int64_t)(h - p.Hq) * D, p.ko + t * p.kos + (int64_t)(h - p.Hq) * D);
 }
 
+// K at the reused position ids of a plan: one block per query tile of the
+// plan's work list (the tiles partition every request's rows), so a row's
+// request and set start come from the plan: rows of the shared set sit at
+// j - s0, row j of an item set starting at a at S + (j - a).
+struct RopePlanParams {
+  const ReqInfo* req;
+  const int32_t* seg_start;
+  const WorkItem* units;
+  int32_t qbase;
+  const __nv_bfloat16* k;
+  __nv_bfloat16* ko;
+  int64_t ks, kos;
+  int32_t Hkv;
+  float inv_freq[64];
+};
+
+template <int D>
+__global__ void __launch_bounds__(kRopeThreads)
+mis_rope_k_plan_kernel(const RopePlanParams p) {
+  griddep_wait();
+  griddep_launch_dependents();
+  constexpr int HALF = D / 2, NC = HALF / 8;          // 8-pair chunks per head
+  const WorkItem un = p.units[blockIdx.x];
+  const ReqInfo R = p.req[un.req];
+  for (int cell = threadIdx.x; cell < kBM * NC; cell += blockDim.x) {
+    const int c = cell % NC, j = un.q0 + cell / NC;
+    if (j >= R.e0) break;                             // cells run row by row
+    const int jn = j - p.qbase;
+    const int pos = j < R.pend ? j - R.s0 : (R.pend - R.s0) + (j - p.seg_start[jn]);
+    const float fp = (float)pos;
+    float cs[8], sn[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sincosf(fp * p.inv_freq[c * 8 + e], &sn[e], &cs[e]);
+    for (int h = 0; h < p.Hkv; ++h) {
+      const __nv_bfloat16* src = p.k + jn * p.ks + (int64_t)h * D;
+      __nv_bfloat16* dst = p.ko + jn * p.kos + (int64_t)h * D;
+      const uint4 a = *reinterpret_cast<const uint4*>(src + c * 8);
+      const uint4 b = *reinterpret_cast<const uint4*>(src + HALF + c * 8);
+      float x1[8], x2[8];
+      unpack8(a, x1);
+      unpack8(b, x2);
+      uint32_t y1[4], y2[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e0 = 2 * i, e1 = 2 * i + 1;
+        y1[i] = pack_bf16(x1[e0] * cs[e0] - x2[e0] * sn[e0], x1[e1] * cs[e1] - x2[e1] * sn[e1]);
+        y2[i] = pack_bf16(x2[e0] * cs[e0] + x1[e0] * sn[e0], x2[e1] * cs[e1] + x1[e1] * sn[e1]);
+      }
+      *reinterpret_cast<uint4*>(dst + c * 8) = make_uint4(y1[0], y1[1], y1[2], y1[3]);
+      *reinterpret_cast<uint4*>(dst + HALF + c * 8) = make_uint4(y2[0], y2[1], y2[2], y2[3]);
+    }
+  }
+}
+
 template <int D>
 mis_status_t launch_rope_d(RopeParams& p, double base, cudaStream_t st) {
   for (int i = 0; i < D / 2; ++i) p.inv_freq[i] = (float)std::pow(base, -2.0 * i / D);
@@ -162,3 +216,43 @@ extern "C" mis_status_t mis_rope_qk(const void* q, const void* k, void* q_out, v
   }
 }
 
+
+extern "C" mis_status_t mis_rope_k_plan(mis_plan_t plan, const void* k, void* k_out,
+                                        int64_t k_row_stride, int64_t k_out_row_stride,
+                                        double base, void* stream) {
+  using namespace mis;
+  if (!plan) return MIS_ERR_INVALID_ARG;
+  const HostPlan& pl = plan_of(plan);
+  if (!pl.workspace) return MIS_ERR_WORKSPACE;
+  if (!k || !k_out) return MIS_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(k_out)) & 15u)
+    return MIS_ERR_INVALID_ARG;
+  if (!(base > 1.0) || !std::isfinite(base)) return MIS_ERR_INVALID_ARG;
+  const int64_t wk = (int64_t)pl.Hkv * pl.D;
+  if (k_row_stride < wk || k_out_row_stride < wk || ((k_row_stride | k_out_row_stride) & 7))
+    return MIS_ERR_SHAPE;
+  if (pl.work.empty()) return MIS_OK;
+  if (pl.work.size() > 0x7fffffff) return MIS_ERR_UNSUPPORTED;
+  const uint8_t* ws = static_cast<const uint8_t*>(pl.workspace);
+  RopePlanParams p;
+  p.req = reinterpret_cast<const ReqInfo*>(ws + pl.off_req);
+  p.seg_start = reinterpret_cast<const int32_t*>(ws + pl.off_seg);
+  p.units = reinterpret_cast<const WorkItem*>(ws + pl.off_work);
+  p.qbase = pl.cached ? pl.qbase : 0;
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.ko = static_cast<__nv_bfloat16*>(k_out);
+  p.ks = k_row_stride; p.kos = k_out_row_stride;
+  p.Hkv = pl.Hkv;
+  for (int i = 0; i < 64; ++i)
+    p.inv_freq[i] = i < pl.D / 2 ? (float)std::pow(base, -2.0 * i / pl.D) : 0.f;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const dim3 grid((unsigned)pl.work.size());
+  try {
+    const cudaError_t e = pl.D == 128
+        ? launch_pdl(mis_rope_k_plan_kernel<128>, grid, dim3(kRopeThreads), 0, st, p)
+        : launch_pdl(mis_rope_k_plan_kernel<64>, grid, dim3(kRopeThreads), 0, st, p);
+    return e == cudaSuccess ? MIS_OK : MIS_ERR_CUDA;
+  } catch (...) {
+    return MIS_ERR_CUDA;
+  }
+}

@@ -36,7 +36,7 @@ EXPORTS = ["mis_status_string", "mis_abi_version", "mis_layout_size", "mis_build
            "mis_inject_stall", "mis_planner_create", "mis_planner_plan", "mis_planner_destroy",
            "mis_set_schedule", "mis_setwise_layout_size", "mis_build_setwise_layout",
            "mis_rope_qk", "mis_cached_plan_workspace_size", "mis_cached_plan_create",
-           "mis_attention_fwd_cached", "mis_attention_fwd_plan_rope"]
+           "mis_attention_fwd_cached", "mis_attention_fwd_plan_rope", "mis_rope_k_plan"]
 
 
 class MisError(RuntimeError):
@@ -113,6 +113,7 @@ def load(path: str = LIB_PATH):
                                   C.c_int32, C.c_int32, vp, C.c_double, vp]),
         "mis_attention_fwd_plan_rope": (C.c_int, [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64,
                                                   C.c_double, vp]),
+        "mis_rope_k_plan": (C.c_int, [vp, vp, vp, i64, i64, C.c_double, vp]),
         "mis_setwise_layout_size": (C.c_int, [C.c_int32, i32p, i32p, i32p, C.POINTER(i64),
                                               C.POINTER(i64)]),
         "mis_build_setwise_layout": (C.c_int, [C.c_int32, i32p, i32p, i32p, i32p, i32p, i32p,
@@ -481,6 +482,13 @@ def mis_rope_qk(q, k, q_out, k_out, position_ids, base: float = 1.0e6, stream=No
     _check(L.mis_rope_qk(_dptr(q), _dptr(k), _dptr(q_out), _dptr(k_out), qs, k.stride(0),
                          qos, k_out.stride(0), T, Hq, Hkv, D, _dptr(position_ids),
                          float(base), _stream(stream)), "mis_rope_qk")
+
+
+def mis_rope_k_plan(plan, k, k_out, base: float = 1.0e6, stream=None):
+    """Rotary embedding of k [T, Hkv, D] at the plan's reused position ids."""
+    L = load()
+    _check(L.mis_rope_k_plan(plan._h, _dptr(k), _dptr(k_out), k.stride(0), k_out.stride(0),
+                             float(base), _stream(stream)), "mis_rope_k_plan")
 
 
 def mis_attention_fwd_plan_rope(plan: "Plan", q, k, v, o, lse=None, base: float = 1.0e6,

@@ -265,6 +265,10 @@ def test_fused_rope_attention_argument_checks(L):
     cached = lib.CachedPlan.host_only(cl.cu_seqlens, cl.item_ptr, cl.item_offsets, [0], [10], 10,
                                       4, 2, 64)
     assert call(cached._h) == lib.MIS_ERR_INVALID_ARG             # cached plans: not this call
+    kcall = lambda h, k=fake, ko=fake, ks=2 * 64, base=1e6: L.mis_rope_k_plan(h, k, ko, ks, ks, base,
+                                                                            None)
+    assert kcall(None) == lib.MIS_ERR_INVALID_ARG
+    assert kcall(host._h) == lib.MIS_ERR_WORKSPACE
 
 
 def _cached_random(rng):

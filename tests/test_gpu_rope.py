@@ -237,3 +237,33 @@ def test_fused_rope_refuses_requests_beyond_its_position_range():
     assert e.value.status == lib.MIS_ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert bool((o == 7.0).all())                    # nothing was launched
+
+
+@pytest.mark.parametrize("cached", [False, True], ids=["packed", "cached"])
+def test_k_rotated_at_the_plans_positions(cached):
+    # mis_rope_k_plan derives the reused position ids from the plan: bit for
+    # bit the K of mis_rope_qk at the layout's position ids
+    s = synth.custom_shapes([300, 0, 700], [6, 2, 9],
+                            [12, 0, 40, 7, 130, 2, 25, 1, 60, 3, 3, 200, 64, 0, 9, 77, 5])
+    hkv, D = 4, 128
+    dev = torch.device("cuda")
+    if cached:
+        lay = O.cached_layout([0, 400, 100], [301, 1, 10], s.n_items, s.item_lens)
+        pos = lay.position_ids
+        plan = lib.CachedPlan(lay.cu_seqlens, lay.item_ptr, lay.item_offsets, [0, 400, 100],
+                              [301, 1, 10], 500, 8, hkv, D)
+    else:
+        lay = lib.mis_build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+        pos = lay.position_ids
+        plan = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, 8, hkv, D)
+    T = int(lay.cu_seqlens[-1])
+    v = synth.draw_values(68, T, 8, hkv, D, want=("k",))
+    k = v["k"].to(dev)
+    ws = torch.zeros(plan.workspace_size(), dtype=torch.uint8, device=dev)
+    plan.create(ws)
+    k1, k2 = torch.empty_like(k), torch.empty_like(k)
+    lib.mis_rope_qk(None, k, None, k1, torch.as_tensor(pos, device=dev), Hq=8)
+    lib.mis_rope_k_plan(plan, k, k2)
+    torch.cuda.synchronize()
+    assert torch.equal(k1, k2)
+    assert _rope_err(k2, O.rope(f64(v["k"]), pos)) <= ROPE_TOL
