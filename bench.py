@@ -286,10 +286,13 @@ def measure(args, name, rank, world, dist, dev, local, full):
     plans = {}
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
+    host_s = []                    # host time of each step's layout + plan + upload call
+
     def enqueue_plan(i, after=None):
         """a1 + a2 of step i on the host (layout, plan), then one asynchronous
         upload of the plan and the readout rows into workspace i % 2 on the
         copy stream; `after`: an event of the step during which it travels."""
+        h0 = time.perf_counter()
         s = i % 2
         lay = HostLayout(w, shapes)
         extra = lay.readout
@@ -301,6 +304,7 @@ def measure(args, name, rank, world, dist, dev, local, full):
             plans[i] = planner.plan(*lay.plan_args(), w.hq, w.hkv, w.head_dim, ws_plans[s],
                                     stream=copy_stream.cuda_stream, extra=extra)
             uploaded[s].record(copy_stream)
+        host_s.append(time.perf_counter() - h0)
 
     def step(i, t):
         """Step i between the events t["st"] (recorded by the caller) and
@@ -449,6 +453,7 @@ def measure(args, name, rank, world, dist, dev, local, full):
                     "tflops": round(score_tflops, 1)},
         "gpu_launches": (5 if args.rope else 4) * args.steps,
         "clocks": clk.summary(),
+        "host_plan_ms": round(1e3 * statistics.median(host_s[-args.steps:]), 4),
         "per_call_split": {"steps": args.steps, "ms_per_step": round(statistics.mean(split_ms), 4),
                            "note": "attention, scoring and roofline times from as many further "
                                    "steps with CUDA events between the calls; value and "

@@ -124,7 +124,9 @@ mis_rope_k_plan_kernel(const RopePlanParams p) {
   constexpr int HALF = D / 2, NC = HALF / 8;          // 8-pair chunks per head
   const WorkItem un = p.units[blockIdx.x];
   const ReqInfo R = p.req[un.req];
-  for (int cell = threadIdx.x; cell < kBM * NC; cell += blockDim.x) {
+  // gridDim.y blocks share a tile (few tiles: more blocks than tiles)
+  const int stride = blockDim.x * gridDim.y;
+  for (int cell = threadIdx.x + blockDim.x * blockIdx.y; cell < kBM * NC; cell += stride) {
     const int c = cell % NC, j = un.q0 + cell / NC;
     if (j >= R.e0) break;                             // cells run row by row
     const int jn = j - p.qbase;
@@ -246,7 +248,10 @@ extern "C" mis_status_t mis_rope_k_plan(mis_plan_t plan, const void* k, void* k_
   for (int i = 0; i < 64; ++i)
     p.inv_freq[i] = i < pl.D / 2 ? (float)std::pow(base, -2.0 * i / pl.D) : 0.f;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const dim3 grid((unsigned)pl.work.size());
+  // at least about four blocks per SM: a tile's 128 rows split over up to 4 blocks
+  const int64_t tiles = (int64_t)pl.work.size();
+  const int64_t ysplit = std::min<int64_t>(4, std::max<int64_t>(1, (4 * num_sms() + tiles - 1) / tiles));
+  const dim3 grid((unsigned)tiles, (unsigned)ysplit);
   try {
     const cudaError_t e = pl.D == 128
         ? launch_pdl(mis_rope_k_plan_kernel<128>, grid, dim3(kRopeThreads), 0, st, p)
