@@ -141,6 +141,42 @@ struct mis_plan_s {
 
 const mis::HostPlan& mis::plan_of(mis_plan_t plan) { return plan->p; }
 
+namespace {
+
+// Destroyed plans are kept (a few) and handed out again: a serving loop that
+// plans every batch then reuses the same host buffers instead of faulting in
+// fresh pages for every plan.
+constexpr size_t kPlanPoolMax = 4;
+std::mutex g_plan_pool_mu;
+std::vector<mis_plan_s*> g_plan_pool;
+
+mis_plan_s* new_plan() {
+  {
+    std::lock_guard<std::mutex> lock(g_plan_pool_mu);
+    if (!g_plan_pool.empty()) {
+      mis_plan_s* h = g_plan_pool.back();
+      g_plan_pool.pop_back();
+      h->p.reset();
+      return h;
+    }
+  }
+  return new mis_plan_s();
+}
+
+void free_plan(mis_plan_s* h) {
+  if (!h) return;
+  {
+    std::lock_guard<std::mutex> lock(g_plan_pool_mu);
+    if (g_plan_pool.size() < kPlanPoolMax) {
+      g_plan_pool.push_back(h);
+      return;
+    }
+  }
+  free_plan(h);
+}
+
+}  // namespace
+
 using namespace mis;
 
 extern "C" {
@@ -194,15 +230,15 @@ mis_status_t create_plan(const Desc* desc, Build build, void* workspace, size_t 
   *out = nullptr;
   mis_plan_s* h = nullptr;
   try {
-    h = new mis_plan_s();
+    h = new_plan();
     mis_status_t st = build(desc, &h->p);
-    if (st != MIS_OK) { delete h; return st; }
+    if (st != MIS_OK) { free_plan(h); return st; }
     HostPlan& p = h->p;
     if (!workspace && ws_bytes == 0) {   // host-only plan: inspection, no launches
       *out = h;
       return MIS_OK;
     }
-    if (!workspace || !aligned256(workspace) || ws_bytes < p.total) { delete h; return MIS_ERR_WORKSPACE; }
+    if (!workspace || !aligned256(workspace) || ws_bytes < p.total) { free_plan(h); return MIS_ERR_WORKSPACE; }
     p.workspace = workspace;
     // one host image of the workspace after the status words, one copy
     std::vector<uint8_t> img(p.total - kStatusBytes, 0);
@@ -219,7 +255,7 @@ mis_status_t create_plan(const Desc* desc, Build build, void* workspace, size_t 
     if (cudaMemsetAsync(ws, 0, kStatusBytes, s) != cudaSuccess ||
         cudaMemcpyAsync(ws + kStatusBytes, img.data(), img.size(), cudaMemcpyHostToDevice, s) !=
             cudaSuccess) {
-      delete h;
+      free_plan(h);
       return MIS_ERR_CUDA;
     }
     // A copy from pageable memory returns once the source has been staged, so
@@ -227,7 +263,7 @@ mis_status_t create_plan(const Desc* desc, Build build, void* workspace, size_t 
     *out = h;
     return MIS_OK;
   } catch (...) {
-    delete h;
+    free_plan(h);
     return MIS_ERR_INVALID_ARG;
   }
 }
@@ -306,12 +342,12 @@ mis_status_t mis_planner_plan(mis_planner_t pl, const mis_attn_desc* desc, void*
   *out = nullptr;
   mis_plan_s* h = nullptr;
   try {
-    h = new mis_plan_s();
+    h = new_plan();
     mis_status_t st = build_plan(desc, &h->p);
-    if (st != MIS_OK) { delete h; return st; }
+    if (st != MIS_OK) { free_plan(h); return st; }
     HostPlan& p = h->p;
     if (!workspace || !aligned256(workspace) || ws_bytes < p.total + extra_bytes) {
-      delete h;
+      free_plan(h);
       return MIS_ERR_WORKSPACE;
     }
     p.workspace = workspace;
@@ -319,7 +355,7 @@ mis_status_t mis_planner_plan(mis_planner_t pl, const mis_attn_desc* desc, void*
     // one image from offset 0: zeroed status words, the plan, the side payload
     const size_t n = p.total + extra_bytes;
     // the buffer's previous upload (two calls ago) must have been read
-    if (pl->used[b] && cudaEventSynchronize(pl->done[b]) != cudaSuccess) { delete h; return MIS_ERR_CUDA; }
+    if (pl->used[b] && cudaEventSynchronize(pl->done[b]) != cudaSuccess) { free_plan(h); return MIS_ERR_CUDA; }
     if (pl->cap[b] < n) {
       if (pl->staging[b]) cudaFreeHost(pl->staging[b]);
       pl->staging[b] = nullptr;
@@ -327,13 +363,13 @@ mis_status_t mis_planner_plan(mis_planner_t pl, const mis_attn_desc* desc, void*
       const size_t want = n + n / 2 + 4096;
       if (cudaHostAlloc(&pl->staging[b], want, cudaHostAllocDefault) != cudaSuccess) {
         pl->staging[b] = nullptr;
-        delete h;
+        free_plan(h);
         return MIS_ERR_CUDA;
       }
       pl->cap[b] = want;
     }
     uint8_t* img = static_cast<uint8_t*>(pl->staging[b]);
-    std::memset(img, 0, p.total);
+    std::memset(img, 0, kStatusBytes);   // the status words; every region is written below
     auto put = [&](size_t off, const void* src, size_t len) {
       if (len) std::memcpy(img + off, src, len);
     };
@@ -346,7 +382,7 @@ mis_status_t mis_planner_plan(mis_planner_t pl, const mis_attn_desc* desc, void*
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(workspace, img, n, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaEventRecord(pl->done[b], s) != cudaSuccess) {
-      delete h;
+      free_plan(h);
       return MIS_ERR_CUDA;
     }
     p.status_clear = true;
@@ -355,7 +391,7 @@ mis_status_t mis_planner_plan(mis_planner_t pl, const mis_attn_desc* desc, void*
     *out = h;
     return MIS_OK;
   } catch (...) {
-    delete h;
+    free_plan(h);
     return MIS_ERR_INVALID_ARG;
   }
 }
@@ -390,7 +426,7 @@ mis_status_t mis_plan_unit_walk(mis_plan_t plan, int32_t* host_out, size_t cap, 
 }
 
 mis_status_t mis_plan_destroy(mis_plan_t plan) {
-  delete plan;
+  free_plan(plan);
   return MIS_OK;
 }
 

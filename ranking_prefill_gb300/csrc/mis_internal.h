@@ -68,6 +68,23 @@ struct HostPlan {
   bool cached = false;
   int32_t cache_T = 0;
   int32_t qbase = 0;
+
+  // Back to the state of a fresh plan; the vectors keep their capacity, so a
+  // recycled plan of similar size touches no fresh pages.
+  void reset() {
+    B = T = Hq = Hkv = D = 0;
+    scale = 0.f;
+    req.clear(); seg_start.clear(); work.clear(); klist.clear(); tile_map.clear(); order.clear();
+    stats = mis_plan_stats{};
+    off_req = off_seg = off_work = off_klist = off_order = total = 0;
+    split = false;
+    n_head_groups = 1;
+    workspace = nullptr;
+    status_clear = false;
+    cached = false;
+    cache_T = 0;
+    qbase = 0;
+  }
 };
 
 // The host plan behind a C-ABI plan handle.

@@ -44,11 +44,16 @@ double snake_makespan(const std::vector<double>& cost, int reps, int n_blocks) {
   const int64_t total = (int64_t)cost.size() * reps;
   if (total == 0) return 0.0;
   const int64_t G = std::min<int64_t>(total, n_blocks);
-  std::vector<double> load((size_t)G, 0.0);
+  thread_local std::vector<double> load;
+  load.assign((size_t)G, 0.0);
+  // walk position u = kk * G + i runs through the units in list order; unit u
+  // is list entry u / reps, tracked without a division
+  int64_t q = 0, r = 0;
   for (int64_t kk = 0; kk * G < total; ++kk)
-    for (int64_t c = 0; c < G; ++c) {
-      const int64_t u = kk * G + ((kk & 1) ? (G - 1 - c) : c);
-      if (u < total) load[(size_t)c] += cost[(size_t)(u / reps)];
+    for (int64_t i = 0; i < G && kk * G + i < total; ++i) {
+      const int64_t c = (kk & 1) ? (G - 1 - i) : i;
+      load[(size_t)c] += cost[(size_t)q];
+      if (++r == reps) { r = 0; ++q; }
     }
   return *std::max_element(load.begin(), load.end());
 }
@@ -92,13 +97,16 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
     if (S < 1 || S > e0 - s0) return MIS_ERR_SHAPE;
     const int32_t pend = s0 + S;
     p->req[b] = ReqInfo{s0, e0, pend, 0};
-    for (int32_t j = s0; j < pend; ++j) p->seg_start[j] = s0;
+    std::fill(p->seg_start.begin() + s0, p->seg_start.begin() + pend, s0);
     int32_t i0 = 0, i1 = 0;
     if (d->item_ptr) {
       i0 = d->item_ptr[b]; i1 = d->item_ptr[b + 1];
       if (i0 < 0 || i1 < i0 || (b == 0 && i0 != 0)) return MIS_ERR_SHAPE;
       if (i1 > i0 && !d->item_offsets) return MIS_ERR_INVALID_ARG;
     }
+    // visible pairs: row j of Q sees [s0, j]; row d of an item set of n rows
+    // sees the S rows of Q and d + 1 rows of its own set
+    p->stats.visible_pairs += (int64_t)S * (S + 1) / 2;
     if (i1 == i0) {
       if (pend != e0) return MIS_ERR_SHAPE;      // rows after Q would belong to no set
       continue;
@@ -108,12 +116,16 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
       const int32_t a = d->item_offsets[i];
       const int32_t e = (i + 1 < i1) ? d->item_offsets[i + 1] : e0;
       if (a < pend || e <= a || e > e0) return MIS_ERR_SHAPE;
-      for (int32_t j = a; j < e; ++j) p->seg_start[j] = a;
+      std::fill(p->seg_start.begin() + a, p->seg_start.begin() + e, a);
+      const int64_t n = e - a;
+      p->stats.visible_pairs += n * S + n * (n + 1) / 2;
     }
   }
 
   // ---- tiles ----
-  std::vector<Tmp> tmp;
+  // per-thread scratch: keeps its capacity from plan to plan
+  thread_local std::vector<Tmp> tmp;
+  tmp.clear();
   int64_t visible = 0, causal_tiles = 0;
   {
     // exact sizes first (the same interval arithmetic as below), so the lists
@@ -131,17 +143,16 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
       }
     }
     tmp.reserve(n_qt);
-    p->klist.reserve(n_tiles);
-    p->tile_map.reserve(4 * n_tiles);
+    p->klist.resize(n_tiles);
+    p->tile_map.resize(4 * n_tiles);
   }
+  visible = p->stats.visible_pairs;
+  uint32_t* kl = p->klist.data();
+  int32_t* tm = p->tile_map.data();
+  int32_t n_emitted = 0, n_full = 0;
   for (int b = 0; b < B; ++b) {
     const ReqInfo& R = p->req[b];
     const int32_t L = R.e0 - R.s0;
-    // visible pairs: rows of Q see [s0, j]; rows of item set a see Q plus [a, j]
-    for (int32_t j = R.s0; j < R.e0; ++j) {
-      const int32_t lo = p->seg_start[j];
-      visible += (j < R.pend) ? (j - R.s0 + 1) : ((int64_t)(R.pend - R.s0) + (j - lo + 1));
-    }
     const int32_t nqt = (L + kBM - 1) / kBM;
     for (int32_t t = 0; t < nqt; ++t) {
       const int32_t r0 = R.s0 + t * kBM;
@@ -152,7 +163,7 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
       // interval 1: keys of Q up to the last row; interval 2: [lo_min, r1)
       const int32_t qa = 0, qb = (std::min(R.pend, r1) - R.s0 + kBN - 1) / kBN;  // [qa, qb)
       const int32_t ba = (lo_min - R.s0) / kBN, bb = (r1 - 1 - R.s0) / kBN + 1;  // [ba, bb)
-      Tmp w{b, r0, (int32_t)p->klist.size(), 0, 0, 0, 0, (int64_t)tmp.size()};
+      Tmp w{b, r0, n_emitted, 0, 0, 0, 0, (int64_t)tmp.size()};
       auto emit = [&](int32_t u) {
         const int32_t c0 = R.s0 + u * kBN;
         const int32_t c1 = std::min(c0 + kBN, R.e0);
@@ -162,9 +173,11 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
         const bool full = (c1 - 1 <= r0) && (c1 <= R.pend || std::max(c0, R.pend) >= lo_max);
         // a clipped key tile loads rows of the next request: mask it too
         const bool need_mask = !full || (c0 + kBN > R.e0);
-        p->klist.push_back((uint32_t)c0 | (need_mask ? kNeedMask : 0u));
-        p->tile_map.insert(p->tile_map.end(), {b, t, u, full ? 1 : 2});
-        if (full) ++p->stats.n_full; else ++p->stats.n_partial;
+        kl[n_emitted] = (uint32_t)c0 | (need_mask ? kNeedMask : 0u);
+        int32_t* q = tm + 4 * (size_t)n_emitted;
+        q[0] = b; q[1] = t; q[2] = u; q[3] = full ? 1 : 2;
+        ++n_emitted;
+        n_full += full ? 1 : 0;
         const int c = need_mask ? 5 : 4;   // masked tiles spend extra ALU in the softmax
         (w.nk % 2 ? w.cost_odd : w.cost_even) += c;
         ++w.nk;
@@ -175,6 +188,9 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
       tmp.push_back(w);
     }
   }
+  if ((size_t)n_emitted != p->klist.size()) return MIS_ERR_SHAPE;   // the pre-count is exact
+  p->stats.n_full = n_full;
+  p->stats.n_partial = n_emitted - n_full;
   return finish_plan(p, tmp, B, T, visible, causal_tiles);
 }
 
@@ -191,11 +207,33 @@ mis_status_t finish_plan(HostPlan* p, std::vector<Tmp>& tmp, int32_t B, int32_t 
   // still start first.
   std::vector<int64_t> req_max(B, 0);
   for (const Tmp& w : tmp) req_max[w.req] = std::max(req_max[w.req], w.cost);
-  std::stable_sort(tmp.begin(), tmp.end(), [&](const Tmp& a, const Tmp& b) {
-    if (req_max[a.req] != req_max[b.req]) return req_max[a.req] > req_max[b.req];
-    if (a.req != b.req) return a.req < b.req;
-    return a.cost > b.cost;
-  });
+  {
+    // the same order as a stable sort by (heaviest tile of the request
+    // descending, request, tile cost descending), as one sort of packed keys:
+    // request rank | inverted cost | list index
+    thread_local std::vector<int32_t> rank, pos_of;
+    thread_local std::vector<uint64_t> key;
+    thread_local std::vector<Tmp> sorted;
+    rank.resize((size_t)B);
+    for (int b = 0; b < B; ++b) rank[(size_t)b] = b;
+    std::stable_sort(rank.begin(), rank.end(),
+                     [&](int32_t a, int32_t b) { return req_max[(size_t)a] > req_max[(size_t)b]; });
+    pos_of.resize((size_t)B);
+    for (int b = 0; b < B; ++b) pos_of[(size_t)rank[(size_t)b]] = b;
+    int64_t cmax = 0;
+    for (const Tmp& w : tmp) cmax = std::max(cmax, w.cost);
+    if (cmax >= ((int64_t)1 << 24) || tmp.size() >= ((size_t)1 << 24) || B >= (1 << 16))
+      return MIS_ERR_SHAPE;
+    key.resize(tmp.size());
+    for (size_t i = 0; i < tmp.size(); ++i)
+      key[i] = ((uint64_t)pos_of[(size_t)tmp[i].req] << 48) |
+               ((uint64_t)(((int64_t)1 << 24) - 1 - tmp[i].cost) << 24) | (uint64_t)i;
+    std::sort(key.begin(), key.end());
+    sorted.clear();
+    sorted.reserve(tmp.size());
+    for (uint64_t k : key) sorted.push_back(tmp[(size_t)(k & 0xFFFFFFu)]);
+    tmp.swap(sorted);
+  }
   p->work.reserve(tmp.size());
   for (const Tmp& w : tmp) p->work.push_back(WorkItem{w.req, w.q0, w.kofs, w.nk});
 
@@ -208,9 +246,9 @@ mis_status_t finish_plan(HostPlan* p, std::vector<Tmp>& tmp, int32_t B, int32_t 
   if (even_group && forced == MIS_SCHEDULE_SPLIT) {
     split = true;
   } else if (even_group && forced == MIS_SCHEDULE_AUTO && !tmp.empty()) {
-    std::vector<double> c_pair, c_split;
-    c_pair.reserve(tmp.size());
-    c_split.reserve(tmp.size());
+    thread_local std::vector<double> c_pair, c_split;
+    c_pair.clear();
+    c_split.clear();
     for (const Tmp& w : tmp) {
       c_pair.push_back(w.cost / 4.0 + kUnitCost);
       c_split.push_back(std::max(w.cost_even, w.cost_odd) / 4.0 + kUnitCost);
@@ -234,34 +272,49 @@ mis_status_t finish_plan(HostPlan* p, std::vector<Tmp>& tmp, int32_t B, int32_t 
     const int64_t n_units = p->stats.n_units;
     const int64_t G = std::min<int64_t>(n_units, num_sms());
     if (n_units > G && G > 0 && n_units < ((int64_t)1 << 30)) {
-      std::vector<double> cost((size_t)n_units);
+      // costs in quarter steps (exact: tile costs are 4 or 5 quarters, a
+      // unit costs kUnitCost more), so loads compare as integers
+      const int64_t unit_q = (int64_t)(4.0 * kUnitCost);
+      thread_local std::vector<int64_t> cost, load;
+      thread_local std::vector<double> costd;
+      thread_local std::vector<uint64_t> ukey, bkey;
+      cost.resize((size_t)n_units);
+      costd.resize((size_t)n_units);
       for (int64_t u = 0; u < n_units; ++u) {
         const Tmp& w = tmp[(size_t)(u / p->n_head_groups)];
-        cost[(size_t)u] = (split ? std::max(w.cost_even, w.cost_odd) : w.cost) / 4.0 + kUnitCost;
+        cost[(size_t)u] = (split ? std::max(w.cost_even, w.cost_odd) : w.cost) + unit_q;
+        costd[(size_t)u] = cost[(size_t)u] / 4.0;
       }
-      const double snake = snake_makespan(cost, 1, (int)G);
+      const double snake = snake_makespan(costd, 1, (int)G);
       const int64_t passes = (n_units + G - 1) / G;
-      std::vector<int32_t> order((size_t)(passes * G), -1);
-      std::vector<double> load((size_t)G, 0.0);
-      std::vector<int32_t> blk((size_t)G), unt;
-      for (int64_t c = 0; c < G; ++c) blk[(size_t)c] = (int32_t)c;
-      for (int64_t kk = 0; kk < passes; ++kk) {
+      std::vector<int32_t>& order = p->order;      // laid out here, kept if it wins
+      order.assign((size_t)(passes * G), -1);
+      load.assign((size_t)G, 0);
+      bkey.resize((size_t)G);
+      bool fits = true;
+      for (int64_t kk = 0; kk < passes && fits; ++kk) {
         const int64_t u0 = kk * G, u1 = std::min(u0 + G, n_units);
-        unt.resize((size_t)(u1 - u0));
-        for (int64_t u = u0; u < u1; ++u) unt[(size_t)(u - u0)] = (int32_t)u;
-        std::stable_sort(unt.begin(), unt.end(),
-                         [&](int32_t a, int32_t b) { return cost[(size_t)a] > cost[(size_t)b]; });
-        std::sort(blk.begin(), blk.end(), [&](int32_t a, int32_t b) {
-          return load[(size_t)a] < load[(size_t)b] || (load[(size_t)a] == load[(size_t)b] && a < b);
-        });
-        for (size_t i = 0; i < unt.size(); ++i) {
-          const int64_t c = blk[i];
-          load[(size_t)c] += cost[(size_t)unt[i]];
-          order[(size_t)(kk * G + ((kk & 1) ? (G - 1 - c) : c))] = unt[i];
+        // units of the pass: cost descending, then list order
+        ukey.resize((size_t)(u1 - u0));
+        for (int64_t u = u0; u < u1; ++u)
+          ukey[(size_t)(u - u0)] = ((uint64_t)(((int64_t)1 << 31) - 1 - cost[(size_t)u]) << 32) |
+                                   (uint64_t)(u - u0);
+        std::sort(ukey.begin(), ukey.end());
+        // blocks: load ascending, then block index
+        for (int64_t c = 0; c < G; ++c) {
+          if (load[(size_t)c] >= ((int64_t)1 << 40)) fits = false;
+          bkey[(size_t)c] = ((uint64_t)load[(size_t)c] << 16) | (uint64_t)c;
+        }
+        std::sort(bkey.begin(), bkey.end());
+        for (size_t i = 0; i < ukey.size(); ++i) {
+          const int64_t c = (int64_t)(bkey[i] & 0xFFFFu);
+          const int64_t u = u0 + (int64_t)(ukey[i] & 0xFFFFFFFFu);
+          load[(size_t)c] += cost[(size_t)u];
+          order[(size_t)(kk * G + ((kk & 1) ? (G - 1 - c) : c))] = (int32_t)u;
         }
       }
-      const double waves = *std::max_element(load.begin(), load.end());
-      if (waves < 0.99 * snake) p->order.swap(order);
+      const double waves = *std::max_element(load.begin(), load.end()) / 4.0;
+      if (!(fits && waves < 0.99 * snake)) order.clear();
     }
   }
 
@@ -323,6 +376,7 @@ mis_status_t build_plan_cached(const mis_cached_desc* d, HostPlan* p) {
   p->qbase = (int32_t)qbase;
   const int32_t Vb = (int32_t)qbase;
 
+  int64_t visible = 0, causal_tiles = 0;
   for (int b = 0; b < B; ++b) {
     const int32_t S = d->cache_len[b], cs = d->cache_start[b];
     if (S < 1 || cs < 0 || (int64_t)cs + S > d->cache_T) return MIS_ERR_SHAPE;
@@ -333,18 +387,20 @@ mis_status_t build_plan_cached(const mis_cached_desc* d, HostPlan* p) {
       const int32_t a = d->item_offsets[i];
       const int32_t e = (i + 1 < i1) ? d->item_offsets[i + 1] : cu[b + 1];
       if (a < cu[b] || e <= a || e > cu[b + 1]) return MIS_ERR_SHAPE;
-      for (int32_t j = a; j < e; ++j) p->seg_start[j] = Vb + a;
+      std::fill(p->seg_start.begin() + a, p->seg_start.begin() + e, Vb + a);
+      // row d of the item set sees the S cached rows and d + 1 rows of its set
+      const int64_t n = e - a;
+      visible += n * S + n * (n + 1) / 2;
     }
     p->req[b] = ReqInfo{cs, Vb + cu[b + 1], cs + S, 0};
   }
 
-  std::vector<Tmp> tmp;
-  int64_t visible = 0, causal_tiles = 0;
+  // per-thread scratch: keeps its capacity from plan to plan
+  thread_local std::vector<Tmp> tmp;
+  tmp.clear();
   for (int b = 0; b < B; ++b) {
     const ReqInfo& R = p->req[b];
     const int32_t S = R.pend - R.s0, base = Vb + cu[b], L = cu[b + 1] - cu[b];
-    for (int32_t r = cu[b]; r < cu[b + 1]; ++r)
-      visible += (int64_t)S + (Vb + r - p->seg_start[r] + 1);
     const int32_t ncache = (S + kBN - 1) / kBN;
     const int32_t nqt = (L + kBM - 1) / kBM;
     for (int32_t t = 0; t < nqt; ++t) {
