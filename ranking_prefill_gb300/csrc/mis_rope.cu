@@ -57,8 +57,11 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
 template <int D>
 __global__ void __launch_bounds__(kRopeThreads)
 mis_rope_kernel(const RopeParams p) {
+  // No early launch of the next kernel: the attention grid that follows is
+  // persistent (one block per SM holding the whole register file), and
+  // blocks of it arriving early took SMs from this pass's later blocks
+  // (measured: decision-256 step 1.61 -> 1.23 ms with the K pass below).
   griddep_wait();
-  griddep_launch_dependents();
   constexpr int HALF = D / 2, NC = HALF / 8;          // 8-pair chunks per head
   const int H = p.Hq + p.Hkv;
   const int NG = (H + p.hpt - 1) / p.hpt;
@@ -119,8 +122,7 @@ struct RopePlanParams {
 template <int D>
 __global__ void __launch_bounds__(kRopeThreads)
 mis_rope_k_plan_kernel(const RopePlanParams p) {
-  griddep_wait();
-  griddep_launch_dependents();
+  griddep_wait();                                     // no early trigger (see mis_rope_kernel)
   constexpr int HALF = D / 2, NC = HALF / 8;          // 8-pair chunks per head
   const WorkItem un = p.units[blockIdx.x];
   const ReqInfo R = p.req[un.req];
