@@ -235,7 +235,7 @@ def run_ours(args, rank, world, dist):
     # further workloads, timed the same way (throughput, per-call split and
     # roofline only; no end-to-end leg, comparators or CPU baseline)
     others = {}
-    for name in [x for x in args.extra_workloads.split(",") if x and x != args.workload]:
+    for name in [x for x in args.extra_workloads.split(",") if x not in ("", "none", args.workload)]:
         r = measure(args, name, rank, world, dist, dev, local, full=False)
         others[name] = {k: r[k] for k in ("value", "unit", "ms_per_step", "roofline", "attention",
                                           "scoring", "clocks")}
@@ -960,7 +960,7 @@ def main():
                          "that fits one GPU)")
     ap.add_argument("--extra-workloads", default="qwen3-0.6b-layer",
                     help="comma-separated workloads also timed (throughput and roofline only); "
-                         "'' for none")
+                         "'none' for none")
     ap.add_argument("--sweep", action="store_true",
                     help="request-size sweep N = 1..200 (prints its own JSON table)")
     ap.add_argument("--sweep-members", type=int, default=16)
