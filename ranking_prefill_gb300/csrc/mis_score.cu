@@ -65,7 +65,9 @@ struct ScoreLayout {       // byte offsets inside the scoring workspace
 
 ScoreLayout score_layout(int32_t M, int32_t d, int32_t V, int32_t K) {
   ScoreLayout L;
-  L.m_pad = (int32_t)align_up((size_t)std::max(M, 1), kItemTile);
+  // several item tiles run on CTA pairs (one 256-row product over two SMs):
+  // an even number of them
+  L.m_pad = M <= kItemTile ? kItemTile : (int32_t)align_up((size_t)M, 2 * kItemTile);
   L.n_vtiles = (V + kVocabTile - 1) / kVocabTile;
   L.max_chunks = L.n_vtiles;
   size_t off = kStatusBytes;
@@ -375,6 +377,223 @@ mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
   }
 }
 
+// ------------------------------------------------------- partial, SM pairs
+// The same (item tile, run of vocabulary tiles) work as the kernel above, on
+// a cluster of two CTAs on two SMs: item tiles 2i and 2i + 1 (one per CTA)
+// against one run of vocabulary tiles. Each 256 x 256 x 16 product is one
+// tcgen05.mma.cta_group::2 issued by the even CTA: A rows (items) and the
+// accumulator rows stay in their own CTA, and each CTA holds half of the
+// W_lm tile (vocabulary rows v0 + 128 r .. v0 + 128 r + 127 in CTA r). Per SM
+// the W_lm tile's shared-memory fills and operand reads are half of the
+// single-SM kernel's, which ran short of shared-memory bandwidth rather than
+// tensor-core rate. Both CTAs' TMA loads of a stage complete on the even
+// CTA's full barrier; its MMA thread's commits arrive on the barriers of both
+// CTAs; each CTA's epilogue reads its own accumulator rows and releases the
+// accumulator with an arrival on the even CTA's barrier.
+constexpr int kPairStages = 6;
+constexpr int kBHalfBytes = (kVocabTile / 2) * kKStep * 2;   // 16 KB
+constexpr int kPairStageBytes = kABytes + kBHalfBytes;
+constexpr int kPairData = kPairStages * kPairStageBytes;
+constexpr int kPairSmem = kPairData + 512 + 1024;
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
+mis_score_partial_pair_kernel(const __grid_constant__ CUtensorMap amap,
+                              const __grid_constant__ CUtensorMap wmap, const ScoreParams p) {
+  griddep_launch_dependents();
+  constexpr int S = kPairStages;
+  constexpr int bF = 0, bE = S, bAF = 2 * S, bAE = bAF + 2, bDR = bAE + 2, bTF = bDR + 1,
+                bTE = bTF + kRing, nBar = bTE + kRing;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPairData);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + nBar);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(tmem_slot + 4);   // kRing entries
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int mt = blockIdx.x;                      // this CTA's item tile
+  const int chunk = blockIdx.y;
+  const int v_first = chunk * p.tiles_per_chunk;
+  const int v_last = min(v_first + p.tiles_per_chunk, p.n_vtiles);
+  const int nkb = p.n_kb;
+  // the even CTA's barrier at the offset of this CTA's `i`
+  auto lbar = [&](int i) { return mapa_shared(bar(i), 0); };
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int st = 0; st < S; ++st) { mbar_init(bar(bF + st), 1); mbar_init(bar(bE + st), 1); }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(bAF + b), 1);
+      mbar_init(bar(bAE + b), 8);                     // the epilogue warps of both CTAs
+    }
+    mbar_init(bar(bDR), 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(bar(bTF + s), 1);
+      mbar_init(bar(bTE + s), leader ? 5 : 4);        // (the MMA thread) and 4 epilogue warps
+    }
+    fence_mbar_init();
+    fence_proxy_async();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&amap);
+    tma_prefetch_desc(&wmap);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), 512);
+    tmem_relinquish_pair();
+  }
+  // both CTAs' barriers are initialised before any arrival or copy crosses
+  cluster_sync_all();
+  griddep_wait();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Waiter W{abort_flag, p.status, p.wait_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int step = 0;
+      for (int j = 0, t = v_first;; ++j, ++t) {
+        const int slot = j % kRing;
+        if (j >= kRing && !wait(bar(bTE + slot), ((j / kRing) - 1) & 1, W, 0x880)) break;
+        const bool valid = t < v_last;
+        ring[slot] = valid ? t : -1;
+        mbar_arrive(bar(bTF + slot));
+        if (!valid) break;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb, ++step) {
+          const int st = step % S;
+          if (step >= S && !wait(bar(bE + st), ((step / S) - 1) & 1, W, 0x900)) {
+            ok = false;
+            break;
+          }
+          // the even CTA's full barrier counts both CTAs' bytes of the stage
+          if (leader) mbar_arrive_expect_tx(bar(bF + st), 2 * kPairStageBytes);
+          uint8_t* sA = smem + st * kPairStageBytes;
+          tma_load_2d_pair(smem_u32(sA), &amap, lbar(bF + st), kb * kKStep, mt * kItemTile);
+          tma_load_2d_pair(smem_u32(sA + kABytes), &wmap, lbar(bF + st), kb * kKStep,
+                           t * kVocabTile + (int)rank * (kVocabTile / 2));
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (leader && lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(2 * kItemTile, kVocabTile, false);
+      bool ok = true;
+      if (p.stall) ok = wait(bar(bDR), 0, W, 0xfff);   // nothing arrives before the drain
+      for (int j = 0; ok; ++j) {
+        const int slot = j % kRing;
+        if (!wait(bar(bTF + slot), (j / kRing) & 1, W, 0x980)) break;
+        const int t = ring[slot];
+        mbar_arrive(bar(bTE + slot));
+        if (t < 0) break;
+        const int buf = j & 1;
+        if (j >= 2 && !wait_cluster(bar(bAE + buf), ((j >> 1) - 1) & 1, W, 0xa00)) break;
+        tc_fence_after();
+        const uint32_t dacc = tmem + buf * kVocabTile;
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int step = j * nkb + kb;
+          const int st = step % S;
+          if (!wait(bar(bF + st), (step / S) & 1, W, 0xb00)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t aA = smem_u32(smem + st * kPairStageBytes);
+          const uint32_t aB = aA + kABytes;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ss_pair(dacc, sdesc_sw128(aA + ks * 32, 16, 1024),
+                        sdesc_sw128(aB + ks * 32, 16, 1024), idesc, (kb | ks) != 0);
+          mma_commit_pair(bar(bE + st), 0x3);         // the stage is free in both CTAs
+        }
+        if (ok) mma_commit_pair(bar(bAF + buf), 0x3); // the accumulators are complete
+      }
+      // drain: every product this thread issued has completed, and every copy
+      // of a stage it waited for has landed
+      mma_commit_pair(bar(bDR), 0x1);
+      wait_drain(bar(bDR), 0);
+    }
+  } else if (warp >= 4) {
+    const int sw = warp - 4;
+    const int row = sw * 32 + lane;
+    const int item = mt * kItemTile + row;
+    const uint32_t tl = tmem + ((uint32_t)(sw * 32) << 16);
+    float m2 = -INFINITY, s = 0.f;
+    bool ok = true;
+    for (int j = 0;; ++j) {
+      const int slot = j % kRing;
+      ok = wait(bar(bTF + slot), (j / kRing) & 1, W, 0xb80);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const int t = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(bTE + slot));
+      if (t < 0) break;
+      const int buf = j & 1;
+      ok = wait(bar(bAF + buf), (j >> 1) & 1, W, 0xc00);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int v0 = t * kVocabTile;
+      const uint32_t tacc = tl + buf * kVocabTile;
+#pragma unroll 1
+      for (int c = 0; c < kVocabTile / 32; ++c) {
+        uint32_t zr[32];
+        tmem_ld32(tacc + c * 32, zr);
+        tmem_ld_wait();
+        reg_fence32(zr);
+        const int vbase = v0 + c * 32;
+        float cm = -INFINITY;
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const float z = (vbase + x < p.V) ? __uint_as_float(zr[x]) * kLog2e : -INFINITY;
+          zr[x] = __float_as_uint(z);
+          cm = fmaxf(cm, z);
+        }
+        if (cm > m2) {
+          s *= ex2(m2 - cm);
+          m2 = cm;
+        }
+        float cs = 0.f;
+#pragma unroll
+        for (int x = 0; x < 32; ++x) cs += ex2(__uint_as_float(zr[x]) - m2);
+        s += cs;
+      }
+      for (int l = 0; l < p.K; ++l) {
+        const int lab = p.labels[l];
+        if (lab >= v0 && lab < v0 + kVocabTile) {
+          uint32_t z = tmem_ld1(tacc + (lab - v0));
+          tmem_ld_wait();
+          reg_fence1(z);
+          if (item < p.M) p.zlab[(int64_t)item * p.K + l] = __uint_as_float(z);
+        }
+      }
+      // the accumulator may be overwritten once both CTAs' epilogues read it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(lbar(bAE + buf));
+    }
+    if (ok) {
+      float* pp = p.part + ((int64_t)item * p.n_chunks + chunk) * 2;
+      pp[0] = m2;
+      pp[1] = s;
+    }
+  }
+  // no CTA of the pair leaves (and frees its tensor memory) while the other
+  // may still issue products into it or copies onto its barriers
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 512);
+  }
+}
+
 // ----------------------------------------------------------------- combine
 // One warp per item: lanes stride over the vocab chunks, then merge their
 // (max, sum) pairs with shuffles.
@@ -512,11 +731,23 @@ mis_status_t launch_score(const ScoreArgs& a, void* stream) {
   p.wait_ns = wait_limit_ns();
   p.stall = (inject_stall_mask() >> 1) & 1u;
 
-  if (!kernel_attr_once(reinterpret_cast<const void*>(mis_score_partial_kernel), kSmem))
-    return MIS_ERR_CUDA;
-  if (launch_pdl(mis_score_partial_kernel, dim3(n_mtiles, p.n_chunks), dim3(256), kSmem, st, am,
-                 wm, p) != cudaSuccess)
-    return MIS_ERR_CUDA;
+  if (n_mtiles >= 2 && !p.dynamic) {
+    // item tiles in pairs on SM pairs; each CTA loads half of a W_lm tile
+    const uint32_t wbox2[2] = {(uint32_t)kKStep, (uint32_t)(kVocabTile / 2)};
+    CUtensorMap wm2 = make_tmap_bf16(a.w_lm, 2, wdims, wstr, wbox2, &ok);
+    if (!ok) return MIS_ERR_CUDA;
+    if (!kernel_attr_once(reinterpret_cast<const void*>(mis_score_partial_pair_kernel), kPairSmem))
+      return MIS_ERR_CUDA;
+    if (launch_pdl(mis_score_partial_pair_kernel, dim3(n_mtiles, p.n_chunks), dim3(256),
+                   kPairSmem, st, am, wm2, p) != cudaSuccess)
+      return MIS_ERR_CUDA;
+  } else {
+    if (!kernel_attr_once(reinterpret_cast<const void*>(mis_score_partial_kernel), kSmem))
+      return MIS_ERR_CUDA;
+    if (launch_pdl(mis_score_partial_kernel, dim3(n_mtiles, p.n_chunks), dim3(256), kSmem, st,
+                   am, wm, p) != cudaSuccess)
+      return MIS_ERR_CUDA;
+  }
   return launch_pdl(mis_score_combine_kernel, dim3((a.M + 3) / 4), dim3(128), 0, st, p,
                     a.out_logprobs, a.out_renorm) == cudaSuccess
              ? MIS_OK
