@@ -250,9 +250,8 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   //   SE_s: the epilogue has read slot s
   constexpr int bQF = 0, bQE = 1, bKF = 2, bKE = bKF + KS, bVF = bKE + KS, bVE = bVF + VS,
                 bSF = bVE + VS, bPF = bSF + 2, bOF = bPF + 2, bOE = bOF + 1, bDR = bOE + 2,
-                bST = bDR + 1, bSE = bST + 4, bQR = bSE + 2, bPG = bQR + 1, nBar = bPG + 2;
+                bST = bDR + 1, bSE = bST + 4, bQR = bSE + 2, nBar = bQR + 1;
   // bQR: the unit's Q tiles rotated in place (rotary embedding on load)
-  // bPF_t / bPG_t: the first / second 64 keys' half of P_t written
 
   griddep_launch_dependents();
 
@@ -287,7 +286,6 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(bSF + s), 1);
       mbar_init(bar(bPF + s), 4);                      // one arrival per softmax warp
-      mbar_init(bar(bPG + s), 4);
       mbar_init(bar(bOE + s), 4);                      // one arrival per epilogue warp
       mbar_init(bar(bST + 2 * s), kBM);                // every thread of stream 0
       mbar_init(bar(bST + 2 * s + 1), kBM);            // ... of stream 1
@@ -395,39 +393,15 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
                      sdesc_sw128(aK + b * C::kBox + ks * 32, 16, 1024), idS, (b | ks) != 0);
           mma_commit(bar(bSF + t));
         };
-        // the first PV of stream t in a unit overwrites O_t: the epilogue of the
-        // previous unit must have read it out of tensor memory. In the split
-        // schedule one barrier covers both accumulators, and stream 0's first
-        // PV always comes first.
-        int first_pv_lu = 0;
-        auto first_pv_of = [&](int t) -> bool {
-          if (first_pv_lu == 0 || (split && t == 1)) return true;
-          if (!wait<true>(bar(bOE + t), (first_pv_lu - 1) & 1, W, 0x280 + t)) return false;
-          tc_fence_after();
-          return true;
-        };
-        // O_t (+)= P_t V over keys [64 half, 64 half + 64) of the tile
-        auto issue_pv_half = [&](int t, int sv, bool acc, int half) {
+        auto issue_pv = [&](int t, int sv, bool acc) {
           const uint32_t aV = smem_u32(sV + sv * C::kTile);
 #pragma unroll
-          for (int kq = 0; kq < kBN / 32; ++kq) {
-            const int ks = half * (kBN / 32) + kq;
+          for (int ks = 0; ks < kBN / 16; ++ks) {
             // V is MN-major (head dim contiguous): 8-key groups 1024 B apart,
             // 64-column boxes kBox apart. P_t sits in the first columns of S_t.
             const uint64_t db = sdesc_sw128(aV + ks * 16 * 128, C::kBox, 1024);
             mma_ts(tmem + colO(t), tmem + colS(t) + ks * 8, db, idO, (acc || ks != 0) ? 1u : 0u);
           }
-        };
-        // both halves, each as soon as the softmax warps have written it
-        auto issue_pv = [&](int t, int sv, bool acc, int phase, bool first) -> bool {
-          if (!wait<true>(bar(bPF + t), phase, W, 0x400 + t)) return false;
-          tc_fence_after();
-          if (first && !first_pv_of(t)) return false;
-          issue_pv_half(t, sv, acc, 0);
-          if (!wait<true>(bar(bPG + t), phase, W, 0x420 + t)) return false;
-          tc_fence_after();
-          issue_pv_half(t, sv, acc, 1);
-          return true;
         };
         // c0, c1: S products issued so far for each stream (the phase of SF_t / PF_t)
         int gk = 0, lu = 0, c0 = 0, c1 = 0;
@@ -441,7 +415,12 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
           // the previous unit must have read it out of tensor memory. In the
           // split schedule one barrier covers both accumulators, and stream 0's
           // first PV always comes first.
-          first_pv_lu = lu;
+          auto first_pv = [&](int t) -> bool {
+            if (lu == 0 || (split && t == 1)) return true;
+            if (!wait<true>(bar(bOE + t), (lu - 1) & 1, W, 0x280 + t)) return false;
+            tc_fence_after();
+            return true;
+          };
           // unit-local key tile of stream t at step s
           const int ns = split ? (nk + 1) / 2 : nk;
           bool pend1 = false;            // stream 1 owes the PV of the previous step
@@ -453,7 +432,10 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
             // the pair schedule PV_0 of the same tile already waited)
             if (split && !wait<true>(bar(bVF + pend1_v), (pend1_g / VS) & 1, W, 0x3c0))
               return false;
-            if (!issue_pv(1, pend1_v, pend1_acc, (c1 - 1) & 1, pend1_first)) return false;
+            if (!wait<true>(bar(bPF + 1), (c1 - 1) & 1, W, 0x400)) return false;
+            tc_fence_after();
+            if (pend1_first && !first_pv(1)) return false;
+            issue_pv(1, pend1_v, pend1_acc);
             mma_commit(bar(bVE + pend1_v));
             pend1 = false;
             return true;
@@ -483,7 +465,10 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
             }
             if (st == ns - 1) mma_commit(bar(bQE));        // Q of this unit no longer read
             if (!(ok = wait<true>(bar(bVF + sv0), (g0 / VS) & 1, W, 0x480))) break;
-            if (!(ok = issue_pv(0, sv0, st > 0, c0 & 1, st == 0))) break;
+            if (!(ok = wait<true>(bar(bPF + 0), c0 & 1, W, 0x500))) break;
+            tc_fence_after();
+            if (st == 0 && !(ok = first_pv(0))) break;
+            issue_pv(0, sv0, st > 0);
             ++c0;
             if (split) mma_commit(bar(bVE + sv0));
           }
@@ -596,9 +581,6 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
         // scale/shift and the row sum run on packed fp32 pairs
         const uint64_t nmbx2 = f2_pack(__float_as_uint(-mb), __float_as_uint(-mb));
         uint64_t rs4[4] = {0ull, 0ull, 0ull, 0ull};
-        // Each 64-key half of P goes to the MMA thread as soon as it is in
-        // tensor memory, so the first half's PV product runs while the second
-        // half's exponentials are computed.
 #pragma unroll
         for (int hf = 0; hf < kBN / 64; ++hf) {        // 64 columns -> 32 packed words
           uint32_t pk[32];
@@ -612,30 +594,30 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
             pk[c] = pack_bf16(p0, p1);
           }
           tmem_st32(tS + hf * 32, pk);
-          if (hf == 0 && any_grow && it > 0) {
-            // O_h holds the products up to tile it-1, all complete (see above),
-            // and no product of this tile runs before the first half's arrival
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t ov[32];
-              tmem_ld32(tO + c * 32, ov);
-              tmem_ld_wait();
-              reg_fence32(ov);
-#pragma unroll
-              for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * alpha);
-              tmem_st32(tO + c * 32, ov);
-            }
-          }
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar((hf == 0 ? bPF : bPG) + t));   // one arrival per warp
         }
         {
           float a0, a1;
           f2_unpack(f2_add(f2_add(rs4[0], rs4[1]), f2_add(rs4[2], rs4[3])), a0, a1);
           l += a0 + a1;
         }
+        if (any_grow && it > 0) {
+          // O_h holds the products up to tile it-1, all complete (see above);
+          // it is rescaled after P so that O and S are never live together
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + c * 32, ov);
+            tmem_ld_wait();
+            reg_fence32(ov);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * alpha);
+            tmem_st32(tO + c * 32, ov);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(bPF + t));       // one arrival per warp
       }
       if (!ok) break;
       cs += nkt;
