@@ -18,17 +18,27 @@ from gpu_helpers import ATTN_TOL, check_attention, f64, forced_schedule, oracle_
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=[lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT], ids=["pair", "split"])
+@pytest.fixture(params=[lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT, lib.SCHEDULE_SM_PAIR],
+                ids=["pair", "split", "smpair"])
 def schedule(request):
     """Run the test under both attention schedules (odd GQA groups are always split)."""
     with forced_schedule(request.param):
         yield request.param
 
 
-def _expect_schedule(st, mode, hq, hkv):
-    want = mode if (hq // hkv) % 2 == 0 else lib.SCHEDULE_SPLIT
+def expected_schedule(mode, hq, hkv, D):
+    """Odd GQA groups always run SPLIT; SM_PAIR also needs D = 128 (else PAIR)."""
+    if (hq // hkv) % 2:
+        return lib.SCHEDULE_SPLIT
+    if mode == lib.SCHEDULE_SM_PAIR and D != 128:
+        return lib.SCHEDULE_PAIR
+    return mode
+
+
+def _expect_schedule(st, mode, hq, hkv, D=128):
+    want = expected_schedule(mode, hq, hkv, D)
     assert st["schedule"] == want
-    assert st["n_units"] == st["n_qtiles"] * (hq // 2 if want == lib.SCHEDULE_PAIR else hq)
+    assert st["n_units"] == st["n_qtiles"] * (hq if want == lib.SCHEDULE_SPLIT else hq // 2)
 
 
 def _sample_rows(lay, n, seed):
@@ -60,7 +70,7 @@ def test_random_small_layouts(seed, schedule):
     hq, hkv = [(4, 2), (8, 2), (2, 2), (8, 8), (16, 4), (4, 1)][seed]
     D = 64 if seed % 2 else 128
     err, st = check_attention(synth.custom_shapes(p, n, lens), hq, hkv, D, 1000 + seed)
-    _expect_schedule(st, schedule, hq, hkv)
+    _expect_schedule(st, schedule, hq, hkv, D)
 
 
 @pytest.mark.parametrize("D", [64, 128])
@@ -76,7 +86,7 @@ def test_odd_gqa_groups_and_single_head(hq, hkv, D, schedule):
     # the split schedule runs them whatever the request
     s = synth.custom_shapes([90, 260], [3, 5], [12, 0, 140, 7, 64, 1, 33, 129])
     err, st = check_attention(s, hq, hkv, D, 40 + hq)
-    _expect_schedule(st, schedule, hq, hkv)
+    _expect_schedule(st, schedule, hq, hkv, D)
 
 
 def test_single_item_and_empty_items(schedule):
@@ -146,16 +156,17 @@ def test_qwen3_layer_full(schedule):
 
 
 def test_schedules_agree_on_a_long_unit_mix():
-    # the two schedules reduce the same terms in different orders: their
-    # outputs differ by rounding only (much less than the oracle tolerance)
+    # the schedules reduce the same terms in different orders: their outputs
+    # differ by rounding only (much less than the oracle tolerance)
     s = synth.custom_shapes([700, 40, 1500], [9, 1, 30], [3 + 3 * i for i in range(40)])
     outs = []
-    for mode in (lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT):
+    for mode in (lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT, lib.SCHEDULE_SM_PAIR):
         with forced_schedule(mode):
             lay, v, o, lse, st, _ = run_attention(s, 8, 2, 128, 21)
             outs.append((o.float(), lse.clone()))
-    assert (outs[0][0] - outs[1][0]).abs().max().item() <= 8e-3
-    assert (outs[0][1] - outs[1][1]).abs().max().item() <= 1e-4
+    for other in outs[1:]:
+        assert (outs[0][0] - other[0]).abs().max().item() <= 8e-3
+        assert (outs[0][1] - other[1]).abs().max().item() <= 1e-4
 
 
 @pytest.mark.parametrize("name", ["8b-large", "decision-256", "varlen-16", "prefix12k-50x150"])

@@ -116,7 +116,8 @@ def test_rotary_mis_equals_single_item_prompts_on_gpu():
 
 # ------------------------------------------------ Q rotated on load (fused) ----
 
-@pytest.fixture(params=[lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT], ids=["pair", "split"])
+@pytest.fixture(params=[lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT, lib.SCHEDULE_SM_PAIR],
+                ids=["pair", "split", "smpair"])
 def schedule(request):
     from gpu_helpers import forced_schedule
     with forced_schedule(request.param):
@@ -175,8 +176,8 @@ def test_q_rotated_on_load_matches_oracle(hq, hkv, D, seed, base, schedule):
     assert status == lib.MIS_OK
     assert np.abs(f64(o) - ro).max() <= ATTN_TOL
     assert np.abs(f64(lse).T - rl).max() <= 2e-3
-    want = schedule if (hq // hkv) % 2 == 0 else lib.SCHEDULE_SPLIT
-    assert st["schedule"] == want
+    from test_gpu_attention import expected_schedule
+    assert st["schedule"] == expected_schedule(schedule, hq, hkv, D)
 
 
 def test_q_rotated_on_load_strided_and_qwen3_layer(schedule):
