@@ -56,7 +56,7 @@ def test_tiny_workload_full(schedule):
     w = synth.WORKLOADS["tiny"]
     err, st = check_attention(synth.draw_shapes(w), w.hq, w.hkv, w.head_dim, w.seed)
     assert st["n_full"] + st["n_partial"] == 6
-    _expect_schedule(st, schedule, w.hq, w.hkv)
+    _expect_schedule(st, schedule, w.hq, w.hkv, w.head_dim)
 
 
 @pytest.mark.parametrize("seed", range(6))
@@ -152,7 +152,7 @@ def test_qwen3_layer_full(schedule):
     w = synth.WORKLOADS["qwen3-0.6b-layer"]
     err, st = check_attention(synth.draw_shapes(w), w.hq, w.hkv, w.head_dim, w.seed)
     assert st["visible_pairs"] == 3120825
-    _expect_schedule(st, schedule, w.hq, w.hkv)
+    _expect_schedule(st, schedule, w.hq, w.hkv, w.head_dim)
 
 
 def test_schedules_agree_on_a_long_unit_mix():
