@@ -156,9 +156,9 @@ typedef struct {
   int64_t n_causal_tiles;  /* blocks a causal mask of the same cu_seqlens keeps */
   int64_t visible_pairs;   /* unmasked (row, key) pairs, per head              */
   int64_t workspace_bytes; /* device workspace the plan occupies               */
-  int64_t schedule;        /* MIS_SCHEDULE_PAIR, _SPLIT or _SM_PAIR            */
+  int64_t schedule;        /* MIS_SCHEDULE_PAIR or MIS_SCHEDULE_SPLIT          */
   int64_t n_units;         /* work units of the attention kernel: query tiles  */
-                           /* x (Hq / 2) for PAIR and SM_PAIR, x Hq for SPLIT  */
+                           /* x (Hq / 2) for pairs, x Hq for split             */
 } mis_plan_stats;
 
 /* Bytes of device workspace mis_plan_create() needs for this descriptor (0
@@ -188,11 +188,9 @@ mis_status_t mis_plan_get_stats(mis_plan_t plan, mis_plan_stats* out);
 mis_status_t mis_plan_tile_map(mis_plan_t plan, int32_t* host_out, size_t cap, size_t* n_out);
 /* The attention kernel's unit walk (for inspection and tests): the unit each
  * walk position hands out, -1 where a block has none. Position kk * G + c
- * belongs to block c in pass kk (odd passes reversed), G = min(units, SMs),
- * or min(units, SMs / 2) SM pairs under MIS_SCHEDULE_SM_PAIR (both CTAs of
- * pair c take the same unit); the plan's unit u is query tile u / g, head
- * group u % g with g = Hq / 2 (PAIR, SM_PAIR) or Hq (SPLIT). Every unit
- * appears exactly once. Writes
+ * belongs to block c in pass kk (odd passes reversed), G = min(units, SMs);
+ * the plan's unit u is query tile u / g, head group u % g with g = Hq / 2
+ * (pair schedule) or Hq (split). Every unit appears exactly once. Writes
  * min(cap, n) entries to host_out (may be NULL when cap is 0); *n_out
  * receives n and *blocks_out (may be NULL) receives G. */
 mis_status_t mis_plan_unit_walk(mis_plan_t plan, int32_t* host_out, size_t cap, size_t* n_out,
@@ -438,21 +436,13 @@ uint32_t mis_inject_stall(uint32_t mask);
  *                        take alternate key tiles and merge their partial
  *                        (max, sum, O) in the epilogue: twice the units at
  *                        half the length, which fills the last wave of SMs
- *                        better, at twice the K/V tile loads per FLOP;
- *   MIS_SCHEDULE_SM_PAIR — a unit is one query tile for two query heads that
- *                        share a kv head, on a cluster of two SMs (one head
- *                        each, 256-row products spanning both); each SM's
- *                        streams take alternate key tiles as in SPLIT. Each
- *                        SM holds half of every K and V tile.
- * AUTO picks SM_PAIR for even groups at D = 128; otherwise it compares PAIR
- * and SPLIT by the largest per-SM sum of unit costs under the kernel's
- * static unit order. PAIR and SM_PAIR need an even Hq / Hkv (SM_PAIR also
- * D = 128); other cases run SPLIT. The result is the same up to float
- * rounding in every case. */
+ *                        better, at twice the K/V tile loads per FLOP.
+ * AUTO compares the two by the largest per-SM sum of unit costs under the
+ * kernel's static unit order. PAIR needs an even Hq / Hkv; odd groups always
+ * run SPLIT. The result is the same up to float rounding either way. */
 #define MIS_SCHEDULE_AUTO 0
 #define MIS_SCHEDULE_PAIR 1
 #define MIS_SCHEDULE_SPLIT 2
-#define MIS_SCHEDULE_SM_PAIR 3
 int32_t mis_set_schedule(int32_t mode);
 
 /* ------------------------------------------------------------------------

@@ -202,8 +202,7 @@ uint64_t mis_set_wait_limit_ns(uint64_t ns) { return g_wait_limit_ns.exchange(ns
 uint32_t mis_inject_stall(uint32_t mask) { return g_inject_stall.exchange(mask); }
 
 int32_t mis_set_schedule(int32_t mode) {
-  if (mode != MIS_SCHEDULE_AUTO && mode != MIS_SCHEDULE_PAIR && mode != MIS_SCHEDULE_SPLIT &&
-      mode != MIS_SCHEDULE_SM_PAIR)
+  if (mode != MIS_SCHEDULE_AUTO && mode != MIS_SCHEDULE_PAIR && mode != MIS_SCHEDULE_SPLIT)
     return -1;
   return g_schedule.exchange(mode);
 }
@@ -420,9 +419,7 @@ mis_status_t mis_plan_unit_walk(mis_plan_t plan, int32_t* host_out, size_t cap, 
   const int64_t units = p.stats.n_units;
   const size_t n = p.order.empty() ? (size_t)units : p.order.size();
   *n_out = n;
-  // walk slots: persistent blocks, or persistent SM pairs (clusters of two)
-  const int64_t slots = p.sm_pair ? std::max(1, num_sms() / 2) : num_sms();
-  if (blocks_out) *blocks_out = (int32_t)std::min<int64_t>(units, slots);
+  if (blocks_out) *blocks_out = (int32_t)std::min<int64_t>(units, num_sms());
   const size_t w = cap < n ? cap : n;
   for (size_t i = 0; i < w; ++i) host_out[i] = p.order.empty() ? (int32_t)i : p.order[i];
   return MIS_OK;

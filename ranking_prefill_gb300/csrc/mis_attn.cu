@@ -814,514 +814,6 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   }
 }
 
-// ---------------------------------------------------------------------------
-// SM-pair schedule (D = 128, even GQA groups). A cluster of two CTAs takes a
-// unit = one query tile for the two query heads that share a kv head: CTA r
-// holds head h0 + r. Every product is one tcgen05.mma.cta_group::2 of
-// M = 256 (the two heads' 128 rows, one half per SM) issued by the even CTA:
-//   S_t = Q K^T: N = 128 keys, each CTA holding 64 of the key tile's rows;
-//   O_t += P_t V: N = D, each CTA holding 64 of V's columns (one TMA box).
-// Per SM a step then moves 96 KB less through shared memory than the
-// single-SM pair schedule (each K and V tile half as large, fills included).
-// Inside a CTA the two softmax streams take alternate key tiles of the unit,
-// as in the split schedule, and the epilogue merges their partial results.
-// The single-head Q tile is double-buffered (slot = unit & 1), so the next
-// unit's Q loads while this unit runs.
-// Cross-CTA protocol: K/V halves (and Q when not rotated on load) complete on
-// the even CTA's full barriers, which expect both CTAs' bytes; the MMA
-// thread's commits multicast to both CTAs (S ready, K/V/Q slot free, all PVs
-// done); softmax and epilogue warps of both CTAs release P_t and O with
-// cluster-scope arrivals on the even CTA's barriers. With Q rotated on load,
-// each CTA's Q completes on its own barrier, its softmax warps turn it, and
-// they arrive on the even CTA's "Q rotated" barrier.
-constexpr int kPairD = 128;
-struct PairCfg {
-  static constexpr int kQTile = kBM * kPairD * 2;          // 32 KB, one head
-  static constexpr int kKBox = 64 * 64 * 2;                // 64 keys x 64 columns
-  static constexpr int kKHalf = 2 * kKBox;                 // 64 keys x 128 columns: 16 KB
-  static constexpr int kVHalf = kBN * 64 * 2;              // 128 keys x 64 columns: 16 KB
-  static constexpr int kKStages = 4, kVStages = 4;
-  static constexpr int kOWarp = 32 * 128;
-  static constexpr int kStats = 2 * 2 * kBM * 8;
-  static constexpr int kData = 2 * kQTile + kKStages * kKHalf + kVStages * kVHalf + 4 * kOWarp + kStats;
-  static constexpr int kSmem = kData + 512 + 1024;
-};
-
-__device__ __forceinline__ int unit_at_pair(const AttnParams& p, int kk) {
-  const int G = gridDim.x >> 1, c = blockIdx.x >> 1;
-  const int pos = kk * G + ((kk & 1) ? (G - 1 - c) : c);
-  if (pos >= p.n_walk) return -1;
-  return p.order ? p.order[pos] : pos;
-}
-
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-mis_attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap qmap,
-                         const __grid_constant__ CUtensorMap kmap,
-                         const __grid_constant__ CUtensorMap vmap,
-                         const __grid_constant__ CUtensorMap omap,
-                         const __grid_constant__ CUtensorMap kcmap,
-                         const __grid_constant__ CUtensorMap vcmap, const AttnParams p) {
-  using C = PairCfg;
-  constexpr int D = kPairD;
-  constexpr int KS = C::kKStages, VS = C::kVStages;
-  constexpr int NB = D / 64;
-  auto colS = [](int t) { return (uint32_t)(t * 128); };
-  auto colO = [](int t) { return (uint32_t)(256 + t * D); };
-  constexpr int bQF = 0, bQE = 2, bKF = 4, bKE = bKF + KS, bVF = bKE + KS, bVE = bVF + VS,
-                bSF = bVE + VS, bPF = bSF + 2, bOF = bPF + 2, bOE = bOF + 1, bDR = bOE + 1,
-                bST = bDR + 1, bSE = bST + 4, bQR = bSE + 2, nBar = bQR + 1;
-
-  griddep_launch_dependents();
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint8_t* sQ = smem;                                  // 2 slots of one head's tile
-  uint8_t* sK = smem + 2 * C::kQTile;                  // KS halves
-  uint8_t* sV = sK + KS * C::kKHalf;                   // VS halves
-  uint8_t* sO = sV + VS * C::kVHalf;                   // O staging of the epilogue warps
-  float2* stats = reinterpret_cast<float2*>(sO + 4 * C::kOWarp);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kData);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + nBar);
-  volatile uint32_t* abort_flag = tmem_slot + 1;
-  auto bar = [&](int i) { return smem_u32(bars + i); };
-  auto lbar = [&](int i) { return mapa_shared(bar(i), 0); };   // the even CTA's
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
-  const int n_hg = p.n_head_groups;                    // head pairs per query tile
-  const int total = p.n_walk;
-  const int G = gridDim.x >> 1;
-  const bool rope = p.rope != 0;
-
-  if (threadIdx.x == 0) {
-    *abort_flag = 0;
-    for (int s = 0; s < 2; ++s) { mbar_init(bar(bQF + s), 1); mbar_init(bar(bQE + s), 1); }
-    for (int s = 0; s < KS; ++s) { mbar_init(bar(bKF + s), 1); mbar_init(bar(bKE + s), 1); }
-    for (int s = 0; s < VS; ++s) { mbar_init(bar(bVF + s), 1); mbar_init(bar(bVE + s), 1); }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(bSF + s), 1);
-      mbar_init(bar(bPF + s), 8);                      // 4 softmax warps of each CTA
-      mbar_init(bar(bST + 2 * s), kBM);
-      mbar_init(bar(bST + 2 * s + 1), kBM);
-      mbar_init(bar(bSE + s), kBM);
-    }
-    mbar_init(bar(bOF), 1);
-    mbar_init(bar(bOE), 8);                            // 4 epilogue warps of each CTA
-    mbar_init(bar(bDR), 1);
-    mbar_init(bar(bQR), 16);                           // 8 softmax warps of each CTA
-    fence_mbar_init();
-    fence_proxy_async();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&qmap); tma_prefetch_desc(&kmap); tma_prefetch_desc(&vmap);
-    tma_prefetch_desc(&omap);
-    if (p.qbase) { tma_prefetch_desc(&kcmap); tma_prefetch_desc(&vcmap); }
-  }
-  if (warp == 1) {
-    tmem_alloc_pair(smem_u32(tmem_slot), 512);
-    tmem_relinquish_pair();
-  }
-  cluster_sync_all();                     // both CTAs' barriers exist before anything crosses
-  griddep_wait();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const Waiter W{abort_flag, p.status, p.wait_ns};
-
-  if (warp < 4) {
-    regs_dec<RegSplit<true>::kCtl>();
-    if (warp == 0) {
-      // ------------------------------------------------------------ producer
-      if (lane == 0) {
-        int gk = 0, lu = 0, q_own = 0;
-        bool ok = true;
-        for (int kk = 0; ok && kk * G < total; ++kk) {
-          const int u = unit_at_pair(p, kk);
-          if (u < 0) continue;
-          const WorkItem un = p.units[u / n_hg];
-          const int h = (u % n_hg) * 2 + (int)rank, g = ((u % n_hg) * 2) / p.group;
-          const int qs = lu & 1;
-          // Q slot qs last held unit lu - 2: free once its S products are done
-          if (lu >= 2 && !(ok = wait<true>(bar(bQE + qs), ((lu >> 1) - 1) & 1, W, 0x880))) break;
-          if (rope) {
-            // each CTA's own barrier: its softmax warps turn the tile
-            mbar_arrive_expect_tx(bar(bQF + qs), C::kQTile);
-            for (int b = 0; b < NB; ++b)
-              tma_load_3d(smem_u32(sQ + qs * C::kQTile + b * (kBM * 128)), &qmap, bar(bQF + qs),
-                          b * 64, h, un.q0 - p.qbase);
-            q_own = lu + 1;
-          } else {
-            if (leader) mbar_arrive_expect_tx(bar(bQF + qs), 2 * C::kQTile);
-            for (int b = 0; b < NB; ++b)
-              tma_load_3d_pair(smem_u32(sQ + qs * C::kQTile + b * (kBM * 128)), &qmap,
-                               lbar(bQF + qs), b * 64, h, un.q0 - p.qbase);
-          }
-          for (int it = 0; it < un.nk; ++it) {
-            const int gi = gk + it;
-            const int32_t c0 = (int32_t)(p.klist[un.kofs + it] & ~kNeedMask);
-            const bool from_cache = c0 < p.qbase;
-            const CUtensorMap* km = from_cache ? &kcmap : &kmap;
-            const CUtensorMap* vm = from_cache ? &vcmap : &vmap;
-            const int32_t kr = from_cache ? c0 : c0 - p.qbase;
-            const int sk = gi % KS, sv = gi % VS;
-            if (gi >= KS && !(ok = wait<true>(bar(bKE + sk), ((gi / KS) - 1) & 1, W, 0x900))) break;
-            if (leader) mbar_arrive_expect_tx(bar(bKF + sk), 2 * C::kKHalf);
-            for (int b = 0; b < NB; ++b)     // keys c0 + 64 r .. + 63, all columns
-              tma_load_3d_pair(smem_u32(sK + sk * C::kKHalf + b * C::kKBox), km, lbar(bKF + sk),
-                               b * 64, g, kr + 64 * (int)rank);
-            if (gi >= VS && !(ok = wait<true>(bar(bVE + sv), ((gi / VS) - 1) & 1, W, 0x980))) break;
-            if (leader) mbar_arrive_expect_tx(bar(bVF + sv), 2 * C::kVHalf);
-            // all 128 keys, columns 64 r .. 64 r + 63
-            tma_load_3d_pair(smem_u32(sV + sv * C::kVHalf), vm, lbar(bVF + sv), 64 * (int)rank, g,
-                             kr);
-          }
-          gk += un.nk;
-          ++lu;
-        }
-        // this CTA's own Q copies (rotary path) have landed before it leaves;
-        // the copies completing on the even CTA's barriers were all consumed
-        // (or waited for) by its MMA thread before the closing cluster barrier
-        for (int i = (q_own > 2 ? q_own - 2 : 0); i < q_own; ++i)
-          wait_drain(bar(bQF + (i & 1)), (i >> 1) & 1);
-      }
-    } else if (warp == 1) {
-      // ----------------------------------------------------------------- MMA
-      if (leader && lane == 0) {
-        constexpr uint32_t idS = idesc_bf16(2 * kBM, kBN, false);
-        constexpr uint32_t idO = idesc_bf16(2 * kBM, D, true);
-        bool ok = true;
-        if (p.stall) ok = wait<true>(bar(bDR), 0, W, 0xfff);
-        auto issue_s = [&](int t, int qs, int sk) {
-          const uint32_t aQ = smem_u32(sQ + qs * C::kQTile);
-          const uint32_t aK = smem_u32(sK + sk * C::kKHalf);
-#pragma unroll
-          for (int b = 0; b < NB; ++b)
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              mma_ss_pair(tmem + colS(t), sdesc_sw128(aQ + b * (kBM * 128) + ks * 32, 16, 1024),
-                          sdesc_sw128(aK + b * C::kKBox + ks * 32, 16, 1024), idS, (b | ks) != 0);
-          mma_commit_pair(bar(bSF + t), 0x3);
-        };
-        auto issue_pv = [&](int t, int sv, bool acc) {
-          const uint32_t aV = smem_u32(sV + sv * C::kVHalf);
-#pragma unroll
-          for (int ks = 0; ks < kBN / 16; ++ks) {
-            const uint64_t db = sdesc_sw128(aV + ks * 16 * 128, kBN * 128, 1024);
-            mma_ts_pair(tmem + colO(t), tmem + colS(t) + ks * 8, db, idO, (acc || ks != 0) ? 1u : 0u);
-          }
-        };
-        int gk = 0, lu = 0, c0 = 0, c1 = 0;
-        for (int kk = 0; ok && kk * G < total; ++kk) {
-          const int u = unit_at_pair(p, kk);
-          if (u < 0) continue;
-          const int nk = p.units[u / n_hg].nk;
-          const int qs = lu & 1;
-          if (rope) {
-            if (!(ok = wait_cluster(bar(bQR), lu & 1, W, 0xa00))) break;
-          } else {
-            if (!(ok = wait<true>(bar(bQF + qs), (lu >> 1) & 1, W, 0xa00))) break;
-          }
-          // the first PV of the unit overwrites O_0 and O_1: both CTAs'
-          // epilogues must have read the previous unit's accumulators
-          auto first_pv = [&]() -> bool {
-            if (lu == 0) return true;
-            if (!wait_cluster(bar(bOE), (lu - 1) & 1, W, 0xa80)) return false;
-            tc_fence_after();
-            return true;
-          };
-          const int ns = (nk + 1) / 2;
-          bool pend1 = false;
-          int pend1_g = 0;
-          bool pend1_acc = false;
-          auto flush_pv1 = [&]() -> bool {
-            const int pend1_v = pend1_g % VS;
-            if (!wait<true>(bar(bVF + pend1_v), (pend1_g / VS) & 1, W, 0xac0)) return false;
-            if (!wait_cluster(bar(bPF + 1), (c1 - 1) & 1, W, 0xb00)) return false;
-            tc_fence_after();
-            issue_pv(1, pend1_v, pend1_acc);
-            mma_commit_pair(bar(bVE + pend1_v), 0x3);
-            pend1 = false;
-            return true;
-          };
-          for (int st = 0; ok && st < ns; ++st) {
-            const int g0 = gk + 2 * st;
-            const int sk0 = g0 % KS, sv0 = g0 % VS;
-            if (!(ok = wait<true>(bar(bKF + sk0), (g0 / KS) & 1, W, 0xb40))) break;
-            tc_fence_after();
-            issue_s(0, qs, sk0);
-            mma_commit_pair(bar(bKE + sk0), 0x3);
-            if (pend1 && !(ok = flush_pv1())) break;
-            const int i1 = 2 * st + 1;
-            if (i1 < nk) {
-              const int g1 = gk + i1, sk1 = g1 % KS;
-              if (!(ok = wait<true>(bar(bKF + sk1), (g1 / KS) & 1, W, 0xb80))) break;
-              tc_fence_after();
-              issue_s(1, qs, sk1);
-              mma_commit_pair(bar(bKE + sk1), 0x3);
-              ++c1;
-              pend1 = true;
-              pend1_g = g1;
-              pend1_acc = st > 0;
-            }
-            if (st == ns - 1) mma_commit_pair(bar(bQE + qs), 0x3);   // Q slot no longer read
-            if (!(ok = wait<true>(bar(bVF + sv0), (g0 / VS) & 1, W, 0xbc0))) break;
-            if (!(ok = wait_cluster(bar(bPF + 0), c0 & 1, W, 0xc00))) break;
-            tc_fence_after();
-            if (st == 0 && !(ok = first_pv())) break;
-            issue_pv(0, sv0, st > 0);
-            ++c0;
-            mma_commit_pair(bar(bVE + sv0), 0x3);
-          }
-          if (ok && pend1) ok = flush_pv1();
-          if (ok) mma_commit_pair(bar(bOF), 0x3);          // every PV of the unit done
-          gk += nk;
-          ++lu;
-        }
-        mma_commit_pair(bar(bDR), 0x1);
-        wait_drain(bar(bDR), 0);
-      }
-    }
-  } else if (warp < 12) {
-    // -------------------------------------------------------------- softmax
-    regs_inc<RegSplit<true>::kSoftmax>();
-    const int t = (warp - 4) / 4;                       // stream
-    const int sw = warp & 3;
-    const int r = sw * 32 + lane;
-    const uint32_t tl = tmem + ((uint32_t)(sw * 32) << 16);
-    const uint32_t tS = tl + colS(t), tO = tl + colO(t);
-    const float sl2 = p.scale_log2;
-    const uint64_t sl2x2 = f2_pack(__float_as_uint(sl2), __float_as_uint(sl2));
-    const uint32_t pf_remote = lbar(bPF + t), qr_remote = lbar(bQR);
-    int lu = 0, cs = 0;
-    bool ok = true;
-    for (int kk = 0; ok && kk * G < total; ++kk) {
-      const int u = unit_at_pair(p, kk);
-      if (u < 0) continue;
-      const WorkItem un = p.units[u / n_hg];
-      const ReqInfo R = p.req[un.req];
-      const int j = un.q0 + r;
-      const bool valid = j < R.e0;
-      const int jj = valid ? j : -1;
-      const int lo = valid ? p.seg_start[j - p.qbase] : 0x7fffffff;
-      const int nk = un.nk;
-      if (rope) {
-        // this CTA's Q tile (one head): stream t turns half the frequencies
-        // of all 128 rows (see the single-SM kernel for the positions)
-        const int pos = !valid ? -1 : (j < R.pend ? j - R.s0 : (R.pend - R.s0) + (j - lo));
-        RopeWarp<D, 2, 1, 32> rw;
-        rw.angles(p.rope_freq, pos, t);
-        ok = wait<true>(bar(bQF + (lu & 1)), (lu >> 1) & 1, W, 0xc40 + t);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        rw.turn(smem_u32(sQ + (lu & 1) * C::kQTile), sw * 32, t);
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(qr_remote);
-      }
-      const int nkt = (nk - t + 1) / 2;                 // key tiles t, t + 2, ...
-      float m_ref = -INFINITY, l = 0.f;
-      uint32_t e_next = nkt > 0 ? p.klist[un.kofs + t] : 0u;
-      for (int it = 0; it < nkt; ++it) {
-        const int gi = cs + it;
-        const uint32_t e = e_next;
-        if (it + 1 < nkt) e_next = p.klist[un.kofs + t + (it + 1) * 2];
-        const int32_t c0 = (int32_t)(e & ~kNeedMask);
-        const bool masked = (e & kNeedMask) != 0;
-        ok = wait<true>(bar(bSF + t), gi & 1, W, 0xc80);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t su[kBN];
-#pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) tmem_ld32(tS + c * 32, su + c * 32);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) reg_fence32(su + c * 32);
-        if (masked) {
-          const int a1 = jj - c0 + 1, q1 = min(a1, R.pend - c0), lc = lo - c0;
-#pragma unroll
-          for (int w = 0; w < kBN / 32; ++w) {
-            const uint32_t vis = bit_range(-32 * w, q1 - 32 * w) | bit_range(lc - 32 * w, a1 - 32 * w);
-#pragma unroll
-            for (int x = 0; x < 32; ++x)
-              if (!((vis >> x) & 1u)) su[w * 32 + x] = 0xff800000u;
-          }
-        }
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c = 0; c < kBN; c += 2)
-          mx4[(c >> 1) & 3] = max3(mx4[(c >> 1) & 3], __uint_as_float(su[c]), __uint_as_float(su[c + 1]));
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        const float m_new = fmaxf(m_ref, mx * sl2);
-        const bool grow = m_new > m_ref + kRescaleThreshold;
-        const bool any_grow = __any_sync(0xffffffffu, grow);
-        const float alpha = grow ? ex2(m_ref - m_new) : 1.f;
-        if (grow) { l *= alpha; m_ref = m_new; }
-        const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
-        const uint64_t nmbx2 = f2_pack(__float_as_uint(-mb), __float_as_uint(-mb));
-        uint64_t rs4[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-        for (int hf = 0; hf < kBN / 64; ++hf) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int k2 = hf * 64 + 2 * c;
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(su[k2], su[k2 + 1]), sl2x2, nmbx2), x0, x1);
-            const float p0 = ex2(x0), p1 = ex2(x1);
-            rs4[c & 3] = f2_add(rs4[c & 3], f2_pack(__float_as_uint(p0), __float_as_uint(p1)));
-            pk[c] = pack_bf16(p0, p1);
-          }
-          tmem_st32(tS + hf * 32, pk);
-        }
-        {
-          float a0, a1;
-          f2_unpack(f2_add(f2_add(rs4[0], rs4[1]), f2_add(rs4[2], rs4[3])), a0, a1);
-          l += a0 + a1;
-        }
-        if (any_grow && it > 0) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(tO + c * 32, ov);
-            tmem_ld_wait();
-            reg_fence32(ov);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * alpha);
-            tmem_st32(tO + c * 32, ov);
-          }
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(pf_remote);  // one arrival per warp, on the even CTA
-      }
-      if (!ok) break;
-      cs += nkt;
-      const int slot = lu & 1;
-      if (lu >= 2) {
-        ok = wait<true>(bar(bSE + slot), ((lu >> 1) - 1) & 1, W, 0xcc0 + t);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-      }
-      stats[(slot * 2 + t) * kBM + r] = make_float2(m_ref, l);
-      mbar_arrive(bar(bST + slot * 2 + t));
-      ++lu;
-    }
-  } else {
-    // ------------------------------------------------------------- epilogue
-    regs_dec<RegSplit<true>::kEpi>();
-    const int sw = warp & 3;
-    const int r = sw * 32 + lane;
-    const uint32_t tl = tmem + ((uint32_t)(sw * 32) << 16);
-    const uint32_t sOw = smem_u32(sO + sw * C::kOWarp);
-    const uint32_t oe_remote = lbar(bOE);
-    int lu = 0;
-    bool ok = true;
-    for (int kk = 0; ok && kk * G < total; ++kk) {
-      const int u = unit_at_pair(p, kk);
-      if (u < 0) continue;
-      const WorkItem un = p.units[u / n_hg];
-      const ReqInfo R = p.req[un.req];
-      const int j = un.q0 + r;
-      const bool valid = j < R.e0;
-      const int slot = lu & 1;
-      ok = wait<true>(bar(bST + slot * 2), (lu >> 1) & 1, W, 0xd00) &&
-           wait<true>(bar(bST + slot * 2 + 1), (lu >> 1) & 1, W, 0xd01);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      const float2 s0 = stats[(slot * 2) * kBM + r], s1 = stats[(slot * 2 + 1) * kBM + r];
-      mbar_arrive(bar(bSE + slot));
-      ok = wait<true>(bar(bOF), lu & 1, W, 0xd40);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      const int row0 = un.q0 + sw * 32;
-      const bool wfull = row0 + 32 <= R.e0;
-      const int h = (u % n_hg) * 2 + (int)rank;
-      // merge the two streams' partial results of this row (split schedule)
-      const float m = fmaxf(s0.x, s1.x);
-      const float a0 = (m == -INFINITY) ? 0.f : ex2(s0.x - m);
-      const float a1 = (m == -INFINITY) ? 0.f : ex2(s1.x - m);
-      const float L = s0.y * a0 + s1.y * a1;
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      const float w0 = a0 * inv, w1 = a1 * inv;
-      const bool has1 = un.nk > 1;
-      const uint32_t tO0 = tl + colO(0), tO1 = tl + colO(1);
-#pragma unroll
-      for (int hh = 0; hh < D / 64; ++hh) {
-        if (wfull) {
-          if (lane == 0) bulk_wait_read0();
-          __syncwarp();
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int c = hh * 64 + q * 16;
-          uint32_t o0[16], o1[16];
-          tmem_ld16(tO0 + c, o0);
-          tmem_ld16(tO1 + c, o1);
-          tmem_ld_wait();
-          reg_fence16(o0);
-          reg_fence16(o1);
-          if (hh == D / 64 - 1 && q == 3) {             // both accumulators read
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(oe_remote);
-          }
-          uint32_t pk[8];
-#pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            float v2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float a = __uint_as_float(o0[2 * x + e]) * w0;
-              v2[e] = has1 ? fmaf(__uint_as_float(o1[2 * x + e]), w1, a) : a;
-            }
-            pk[x] = pack_bf16(v2[0], v2[1]);
-          }
-          if (wfull) {
-            const uint32_t ra = sOw + lane * 128;
-#pragma unroll
-            for (int cc2 = 0; cc2 < 2; ++cc2) {
-              const int cc = q * 2 + cc2;
-              st_shared_v4(ra + ((cc ^ (lane & 7)) << 4), pk[4 * cc2], pk[4 * cc2 + 1],
-                           pk[4 * cc2 + 2], pk[4 * cc2 + 3]);
-            }
-          } else if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(p.o + (int64_t)(j - p.qbase) * p.o_stride +
-                                                  (int64_t)h * D + c);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          }
-        }
-        if (wfull) {
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&omap, sOw, hh * 64, h, row0 - p.qbase);
-            bulk_commit();
-          }
-        }
-      }
-      if (p.lse && valid) p.lse[(int64_t)h * p.T + (j - p.qbase)] = (m + log2f(L)) * kLn2;
-      ++lu;
-    }
-    if (lane == 0) bulk_wait0();
-  }
-  // neither CTA frees its tensor memory (or leaves) while the other may still
-  // issue products into it or arrive on its barriers
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync_all();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc_pair(tmem, 512);
-  }
-}
-
 template <int D>
 mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
                       const void* kc, const void* vc, void* o, float* lse, int64_t qs, int64_t ks,
@@ -1381,31 +873,6 @@ mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
     return MIS_ERR_CUDA;
   }
   if (pl.work.empty()) return MIS_OK;
-  if constexpr (D == kPairD) {
-    if (pl.sm_pair) {
-      // K halves: 64-row boxes; V halves: one 64-column box of the same map
-      const uint32_t kbox[3] = {64, 1, 64};
-      CUtensorMap km2 = make_tmap_bf16(k, 3, kd, kstr, kbox, &ok);
-      CUtensorMap kcm2 = km2;
-      if (pl.cached) {
-        const uint64_t cd[3] = {(uint64_t)D, (uint64_t)pl.Hkv, (uint64_t)pl.cache_T};
-        const uint64_t kcstr[2] = {(uint64_t)D * 2, (uint64_t)kcs * 2};
-        kcm2 = make_tmap_bf16(kc, 3, cd, kcstr, kbox, &ok);
-      }
-      if (!ok) return MIS_ERR_CUDA;
-      if (!kernel_attr_once(reinterpret_cast<const void*>(mis_attn_fwd_pair_kernel),
-                            PairCfg::kSmem))
-        return MIS_ERR_CUDA;
-      const int64_t total = (int64_t)pl.work.size() * pl.n_head_groups;
-      if (total > 0x7fffffff) return MIS_ERR_UNSUPPORTED;
-      prm.n_walk = pl.order.empty() ? (int32_t)total : (int32_t)pl.order.size();
-      const int64_t clusters = std::min<int64_t>(total, std::max(1, num_sms() / 2));
-      return launch_pdl(mis_attn_fwd_pair_kernel, dim3((unsigned)(2 * clusters)), dim3(kThreads),
-                        PairCfg::kSmem, st, qm, km2, vm, om, kcm2, vcm, prm) == cudaSuccess
-                 ? MIS_OK
-                 : MIS_ERR_CUDA;
-    }
-  }
   auto kern = pl.split ? mis_attn_fwd_kernel<D, true> : mis_attn_fwd_kernel<D, false>;
   if (!kernel_attr_once(reinterpret_cast<const void*>(kern), C::kSmem)) return MIS_ERR_CUDA;
   const int64_t total = (int64_t)pl.work.size() * pl.n_head_groups;

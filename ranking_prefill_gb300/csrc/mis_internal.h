@@ -53,8 +53,7 @@ struct HostPlan {
   size_t off_req = 0, off_seg = 0, off_work = 0, off_klist = 0, total = 0;
   bool split = false;              // split schedule (one head per unit, key tiles alternate
                                    // between the block's two softmax streams)
-  int32_t n_head_groups = 1;       // units per query tile: Hq / 2 (pair, SM pair) or Hq (split)
-  bool sm_pair = false;            // SM-pair schedule: a unit runs on a cluster of two CTAs
+  int32_t n_head_groups = 1;       // units per query tile: Hq / 2 (pair) or Hq (split)
   // the unit at each walk position of the kernel's blocks (pass kk, block c
   // at kk * G + c, odd passes reversed), -1 for none; empty: position = unit
   std::vector<int32_t> order;
@@ -79,7 +78,6 @@ struct HostPlan {
     stats = mis_plan_stats{};
     off_req = off_seg = off_work = off_klist = off_order = total = 0;
     split = false;
-    sm_pair = false;
     n_head_groups = 1;
     workspace = nullptr;
     status_clear = false;

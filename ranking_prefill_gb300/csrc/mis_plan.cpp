@@ -243,14 +243,7 @@ mis_status_t finish_plan(HostPlan* p, std::vector<Tmp>& tmp, int32_t B, int32_t 
   const bool even_group = (p->Hq / p->Hkv) % 2 == 0;
   bool split = !even_group;
   const int32_t forced = schedule_override();
-  // two SMs per unit (the two heads of a kv head, one per SM; the key tiles
-  // alternate between each SM's two softmax streams): even groups, D = 128,
-  // by default
-  p->sm_pair = even_group && p->D == 128 &&
-               (forced == MIS_SCHEDULE_AUTO || forced == MIS_SCHEDULE_SM_PAIR);
-  if (p->sm_pair) {
-    split = true;                              // stream-wise: alternate key tiles
-  } else if (even_group && forced == MIS_SCHEDULE_SPLIT) {
+  if (even_group && forced == MIS_SCHEDULE_SPLIT) {
     split = true;
   } else if (even_group && forced == MIS_SCHEDULE_AUTO && !tmp.empty()) {
     thread_local std::vector<double> c_pair, c_split;
@@ -264,12 +257,9 @@ mis_status_t finish_plan(HostPlan* p, std::vector<Tmp>& tmp, int32_t B, int32_t 
     split = snake_makespan(c_split, p->Hq, sms) < snake_makespan(c_pair, p->Hq / 2, sms);
   }
   p->split = split;
-  p->n_head_groups = (split && !p->sm_pair) ? p->Hq : p->Hq / 2;
-  p->stats.schedule = p->sm_pair ? MIS_SCHEDULE_SM_PAIR
-                                 : (split ? MIS_SCHEDULE_SPLIT : MIS_SCHEDULE_PAIR);
+  p->n_head_groups = split ? p->Hq : p->Hq / 2;
+  p->stats.schedule = split ? MIS_SCHEDULE_SPLIT : MIS_SCHEDULE_PAIR;
   p->stats.n_units = (int64_t)p->work.size() * p->n_head_groups;
-  // walk slots: persistent blocks, or persistent SM pairs
-  const int slots = p->sm_pair ? std::max(1, num_sms() / 2) : num_sms();
 
   // ---- unit order: the snake walk over the list, or, when the blocks come
   // out clearly better balanced, a wave-by-wave longest-processing-time
@@ -280,7 +270,7 @@ mis_status_t finish_plan(HostPlan* p, std::vector<Tmp>& tmp, int32_t B, int32_t 
   p->order.clear();
   {
     const int64_t n_units = p->stats.n_units;
-    const int64_t G = std::min<int64_t>(n_units, slots);
+    const int64_t G = std::min<int64_t>(n_units, num_sms());
     if (n_units > G && G > 0 && n_units < ((int64_t)1 << 30)) {
       // costs in quarter steps (exact: tile costs are 4 or 5 quarters, a
       // unit costs kUnitCost more), so loads compare as integers

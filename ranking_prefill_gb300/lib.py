@@ -549,7 +549,7 @@ def mis_inject_stall(mask: int) -> int:
     return int(load().mis_inject_stall(int(mask)))
 
 
-SCHEDULE_AUTO, SCHEDULE_PAIR, SCHEDULE_SPLIT, SCHEDULE_SM_PAIR = 0, 1, 2, 3
+SCHEDULE_AUTO, SCHEDULE_PAIR, SCHEDULE_SPLIT = 0, 1, 2
 
 
 def mis_set_schedule(mode: int) -> int:

@@ -91,10 +91,7 @@ def test_schedule_override_and_units(L):
     try:
         for mode, hq, hkv, want, per_tile in [(lib.SCHEDULE_PAIR, 16, 8, lib.SCHEDULE_PAIR, 8),
                                               (lib.SCHEDULE_SPLIT, 16, 8, lib.SCHEDULE_SPLIT, 16),
-                                              (lib.SCHEDULE_SM_PAIR, 16, 8, lib.SCHEDULE_SM_PAIR, 8),
-                                              (lib.SCHEDULE_AUTO, 16, 8, lib.SCHEDULE_SM_PAIR, 8),
                                               (lib.SCHEDULE_PAIR, 12, 4, lib.SCHEDULE_SPLIT, 12),
-                                              (lib.SCHEDULE_SM_PAIR, 12, 4, lib.SCHEDULE_SPLIT, 12),
                                               (lib.SCHEDULE_AUTO, 6, 6, lib.SCHEDULE_SPLIT, 6)]:
             lib.mis_set_schedule(mode)
             st = lib.Plan.host_only(*args, hq, hkv, 128).stats()
@@ -104,14 +101,7 @@ def test_schedule_override_and_units(L):
             assert np.array_equal(lib.Plan.host_only(*args, hq, hkv, 128).tile_map(), ref_map)
         lib.mis_set_schedule(lib.SCHEDULE_AUTO)
         st = lib.Plan.host_only(*args, 16, 8, 128).stats()
-        assert st["schedule"] == lib.SCHEDULE_SM_PAIR           # even group, D = 128
-        # D = 64: SM pairs need D = 128; AUTO compares the single-SM schedules
-        st = lib.Plan.host_only(*args, 16, 8, 64).stats()
         assert st["schedule"] in (lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT)
-        lib.mis_set_schedule(lib.SCHEDULE_SM_PAIR)
-        st = lib.Plan.host_only(*args, 16, 8, 64).stats()
-        assert st["schedule"] == lib.SCHEDULE_PAIR
-        lib.mis_set_schedule(lib.SCHEDULE_AUTO)
         with pytest.raises(lib.MisError):
             lib.mis_set_schedule(7)
         assert lib.mis_set_schedule(lib.SCHEDULE_AUTO) == lib.SCHEDULE_AUTO   # 7 changed nothing
@@ -321,9 +311,8 @@ def test_cached_plan_tile_map_and_pairs_bit_exact(L):
 
 
 @pytest.mark.parametrize("name", ["tiny", "qwen3-0.6b-layer", "decision-256", "varlen-16"])
-@pytest.mark.parametrize("mode", [lib.SCHEDULE_AUTO, lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT,
-                                  lib.SCHEDULE_SM_PAIR],
-                         ids=["auto", "pair", "split", "smpair"])
+@pytest.mark.parametrize("mode", [lib.SCHEDULE_AUTO, lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT],
+                         ids=["auto", "pair", "split"])
 def test_unit_walk_hands_out_every_unit_once_pass_by_pass(name, mode):
     # The attention kernel's blocks take walk position kk * G + c in pass kk.
     # Whatever the order (the snake over the list, or its wave-by-wave

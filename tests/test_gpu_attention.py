@@ -18,27 +18,17 @@ from gpu_helpers import ATTN_TOL, check_attention, f64, forced_schedule, oracle_
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=[lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT, lib.SCHEDULE_SM_PAIR],
-                ids=["pair", "split", "smpair"])
+@pytest.fixture(params=[lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT], ids=["pair", "split"])
 def schedule(request):
     """Run the test under both attention schedules (odd GQA groups are always split)."""
     with forced_schedule(request.param):
         yield request.param
 
 
-def expected_schedule(mode, hq, hkv, D):
-    """Odd GQA groups always run SPLIT; SM_PAIR also needs D = 128 (else PAIR)."""
-    if (hq // hkv) % 2:
-        return lib.SCHEDULE_SPLIT
-    if mode == lib.SCHEDULE_SM_PAIR and D != 128:
-        return lib.SCHEDULE_PAIR
-    return mode
-
-
-def _expect_schedule(st, mode, hq, hkv, D=128):
-    want = expected_schedule(mode, hq, hkv, D)
+def _expect_schedule(st, mode, hq, hkv):
+    want = mode if (hq // hkv) % 2 == 0 else lib.SCHEDULE_SPLIT
     assert st["schedule"] == want
-    assert st["n_units"] == st["n_qtiles"] * (hq if want == lib.SCHEDULE_SPLIT else hq // 2)
+    assert st["n_units"] == st["n_qtiles"] * (hq // 2 if want == lib.SCHEDULE_PAIR else hq)
 
 
 def _sample_rows(lay, n, seed):
@@ -56,7 +46,7 @@ def test_tiny_workload_full(schedule):
     w = synth.WORKLOADS["tiny"]
     err, st = check_attention(synth.draw_shapes(w), w.hq, w.hkv, w.head_dim, w.seed)
     assert st["n_full"] + st["n_partial"] == 6
-    _expect_schedule(st, schedule, w.hq, w.hkv, w.head_dim)
+    _expect_schedule(st, schedule, w.hq, w.hkv)
 
 
 @pytest.mark.parametrize("seed", range(6))
@@ -70,7 +60,7 @@ def test_random_small_layouts(seed, schedule):
     hq, hkv = [(4, 2), (8, 2), (2, 2), (8, 8), (16, 4), (4, 1)][seed]
     D = 64 if seed % 2 else 128
     err, st = check_attention(synth.custom_shapes(p, n, lens), hq, hkv, D, 1000 + seed)
-    _expect_schedule(st, schedule, hq, hkv, D)
+    _expect_schedule(st, schedule, hq, hkv)
 
 
 @pytest.mark.parametrize("D", [64, 128])
@@ -86,7 +76,7 @@ def test_odd_gqa_groups_and_single_head(hq, hkv, D, schedule):
     # the split schedule runs them whatever the request
     s = synth.custom_shapes([90, 260], [3, 5], [12, 0, 140, 7, 64, 1, 33, 129])
     err, st = check_attention(s, hq, hkv, D, 40 + hq)
-    _expect_schedule(st, schedule, hq, hkv, D)
+    _expect_schedule(st, schedule, hq, hkv)
 
 
 def test_single_item_and_empty_items(schedule):
@@ -152,21 +142,20 @@ def test_qwen3_layer_full(schedule):
     w = synth.WORKLOADS["qwen3-0.6b-layer"]
     err, st = check_attention(synth.draw_shapes(w), w.hq, w.hkv, w.head_dim, w.seed)
     assert st["visible_pairs"] == 3120825
-    _expect_schedule(st, schedule, w.hq, w.hkv, w.head_dim)
+    _expect_schedule(st, schedule, w.hq, w.hkv)
 
 
 def test_schedules_agree_on_a_long_unit_mix():
-    # the schedules reduce the same terms in different orders: their outputs
-    # differ by rounding only (much less than the oracle tolerance)
+    # the two schedules reduce the same terms in different orders: their
+    # outputs differ by rounding only (much less than the oracle tolerance)
     s = synth.custom_shapes([700, 40, 1500], [9, 1, 30], [3 + 3 * i for i in range(40)])
     outs = []
-    for mode in (lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT, lib.SCHEDULE_SM_PAIR):
+    for mode in (lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT):
         with forced_schedule(mode):
             lay, v, o, lse, st, _ = run_attention(s, 8, 2, 128, 21)
             outs.append((o.float(), lse.clone()))
-    for other in outs[1:]:
-        assert (outs[0][0] - other[0]).abs().max().item() <= 8e-3
-        assert (outs[0][1] - other[1]).abs().max().item() <= 1e-4
+    assert (outs[0][0] - outs[1][0]).abs().max().item() <= 8e-3
+    assert (outs[0][1] - outs[1][1]).abs().max().item() <= 1e-4
 
 
 @pytest.mark.parametrize("name", ["8b-large", "decision-256", "varlen-16", "prefix12k-50x150"])

@@ -28,8 +28,7 @@ def _run_cached(cl, cache_T, q, k, v, kc, vc, hq, hkv, D, lse=True):
 
 
 @pytest.mark.parametrize("seed", range(4))
-@pytest.mark.parametrize("mode", [lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT, lib.SCHEDULE_SM_PAIR],
-                         ids=["pair", "split", "smpair"])
+@pytest.mark.parametrize("mode", [lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT], ids=["pair", "split"])
 def test_random_cached_batches(seed, mode):
     rng = np.random.default_rng(800 + seed)
     B = int(rng.integers(1, 4))
