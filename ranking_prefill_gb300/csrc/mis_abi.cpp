@@ -425,6 +425,25 @@ mis_status_t mis_plan_unit_walk(mis_plan_t plan, int32_t* host_out, size_t cap, 
   return MIS_OK;
 }
 
+mis_status_t mis_plan_exec_tiles(mis_plan_t plan, int32_t* host_out, size_t cap, size_t* n_out) {
+  if (!plan || !n_out || (cap && !host_out)) return MIS_ERR_INVALID_ARG;
+  const HostPlan& p = plan->p;
+  size_t n = 0;
+  for (const WorkItem& w : p.work) {
+    for (int32_t i = 0; i < w.nk; ++i, ++n) {
+      if (n >= cap) continue;
+      const uint32_t e = p.klist[(size_t)w.kofs + i];
+      int32_t* q = host_out + 4 * n;
+      q[0] = w.req;
+      q[1] = w.q0;
+      q[2] = (int32_t)(e & kTileRow);
+      q[3] = ((e & kNeedMask) ? 1 : 0) | ((e & kComposite) ? 2 : 0);
+    }
+  }
+  *n_out = n;
+  return MIS_OK;
+}
+
 mis_status_t mis_plan_destroy(mis_plan_t plan) {
   free_plan(plan);
   return MIS_OK;

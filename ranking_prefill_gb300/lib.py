@@ -36,7 +36,8 @@ EXPORTS = ["mis_status_string", "mis_abi_version", "mis_layout_size", "mis_build
            "mis_inject_stall", "mis_planner_create", "mis_planner_plan", "mis_planner_destroy",
            "mis_set_schedule", "mis_setwise_layout_size", "mis_build_setwise_layout",
            "mis_rope_qk", "mis_cached_plan_workspace_size", "mis_cached_plan_create",
-           "mis_attention_fwd_cached", "mis_attention_fwd_plan_rope", "mis_rope_k_plan"]
+           "mis_attention_fwd_cached", "mis_attention_fwd_plan_rope", "mis_rope_k_plan",
+           "mis_plan_exec_tiles"]
 
 
 class MisError(RuntimeError):
@@ -63,7 +64,7 @@ class mis_cached_desc(C.Structure):
 class mis_plan_stats(C.Structure):
     _fields_ = [(n, C.c_int64) for n in ("n_qtiles", "n_tiles", "n_full", "n_partial",
                                            "n_causal_tiles", "visible_pairs", "workspace_bytes",
-                                           "schedule", "n_units")]
+                                           "schedule", "n_units", "n_exec_tiles")]
 
     def as_dict(self):
         return {n: int(getattr(self, n)) for n, _ in self._fields_}
@@ -94,6 +95,7 @@ def load(path: str = LIB_PATH):
         "mis_plan_get_stats": (C.c_int, [vp, C.POINTER(mis_plan_stats)]),
         "mis_plan_tile_map": (C.c_int, [vp, i32p, sz, C.POINTER(sz)]),
         "mis_plan_unit_walk": (C.c_int, [vp, i32p, sz, C.POINTER(sz), C.POINTER(C.c_int32)]),
+        "mis_plan_exec_tiles": (C.c_int, [vp, i32p, sz, C.POINTER(sz)]),
         "mis_plan_destroy": (C.c_int, [vp]),
         "mis_attention_fwd_plan": (C.c_int, [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, vp]),
         "mis_attention_fwd": (C.c_int, [vp, vp, vp, vp, vp, i64, i64, i64, i64,
@@ -335,6 +337,16 @@ class Plan:
         out = np.zeros((max(n.value, 1), 4), np.int32)
         _check(self._L.mis_plan_tile_map(self._h, _ptr_i32(out), n.value, C.byref(n)),
                "mis_plan_tile_map")
+        return out[:n.value]
+
+    def exec_tiles(self) -> np.ndarray:
+        """(request, first query row, first key row, flags) of every key tile
+        the kernel runs; flags bit 0 = masked, bit 1 = composite."""
+        n = C.c_size_t()
+        _check(self._L.mis_plan_exec_tiles(self._h, None, 0, C.byref(n)), "mis_plan_exec_tiles")
+        out = np.zeros((max(n.value, 1), 4), np.int32)
+        _check(self._L.mis_plan_exec_tiles(self._h, _ptr_i32(out), n.value, C.byref(n)),
+               "mis_plan_exec_tiles")
         return out[:n.value]
 
     def destroy(self):

@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(L):
     assert declared == set(lib.EXPORTS), declared ^ set(lib.EXPORTS)
     for name in declared:
         assert hasattr(L, name)
-    assert L.mis_abi_version() == 2
+    assert L.mis_abi_version() == 3
     for st in range(8):
         assert lib.mis_status_string(st) != "unknown status"
 
@@ -374,3 +374,56 @@ def test_attention_calls_refuse_the_wrong_plan_kind_before_any_launch(L):
     assert fwd_cached(cached._h) == lib.MIS_ERR_WORKSPACE
     plain.destroy()
     cached.destroy()
+
+
+def _exec_coverage_ok(lay, p):
+    """Every visible key of every row is in exactly one executed key tile of its
+    query tile, and a tile without the mask flag has only visible entries
+    (keys of composite tiles: their first r rows are the last r keys of the
+    shared set, the others c0 + c)."""
+    et = p.exec_tiles()
+    by_qt = {}
+    for b, q0, c0, fl in et.tolist():
+        by_qt.setdefault((b, q0), []).append((c0, fl))
+    assert len(by_qt) == p.stats()["n_qtiles"]
+    for (b, q0), tiles in by_qt.items():
+        s0, e0 = int(lay.cu_seqlens[b]), int(lay.cu_seqlens[b + 1])
+        S = int(lay.prefix_len[b])
+        rows = np.arange(q0, min(q0 + 128, e0))
+        vis = O.mask_rows(lay, b, rows)                   # [R, L] over keys s0 .. e0 - 1
+        seen = np.zeros_like(vis, dtype=np.int32)
+        for c0, fl in tiles:
+            keys = c0 + np.arange(128)
+            if fl & 2:
+                r = S % 128
+                keys[:r] = s0 + S - r + np.arange(r)
+            inside = (keys >= s0) & (keys < e0)
+            cols = keys[inside] - s0
+            seen[:, cols] += 1
+            if not fl & 1:                                 # unmasked: all entries visible
+                assert inside.all() and vis[:, cols].all()
+        assert (seen[vis] == 1).all()                      # every visible key exactly once
+
+
+def test_executed_tiles_cover_every_visible_key_once(L):
+    # layouts whose shared set leaves 1..5 keys in its last tile, at D = 64
+    # and 128 (composite tiles where a warp-wide copy covers the tail), plus
+    # the benchmark's small workloads
+    rng = np.random.default_rng(2024)
+    cases = []
+    for D in (64, 128):
+        for P in (127, 128, 129, 130, 131, 255, 256, 257, 383):
+            n = int(rng.integers(3, 12))
+            cases.append((synth.custom_shapes([P, P + 128], [n, 2], rng.integers(0, 90, n + 2)), D))
+    for name in ("qwen3-0.6b-layer", "tiny"):
+        w = synth.WORKLOADS[name]
+        cases.append((synth.draw_shapes(w), w.head_dim))
+    n_comp = 0
+    for s, D in cases:
+        lay = O.build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+        p = lib.Plan.host_only(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, 4, 2, D)
+        _exec_coverage_ok(lay, p)
+        st = p.stats()
+        n_comp += st["n_tiles"] - st["n_exec_tiles"]
+        assert np.array_equal(p.tile_map(), O.tile_map(lay, 128, 128))   # the map stays canonical
+    assert n_comp > 0                                      # some tail tiles were merged
