@@ -228,7 +228,7 @@ def test_pointer_and_stride_refusals_launch_nothing():
     plan.destroy()
 
 
-@pytest.mark.parametrize("P,D", [(128, 128), (129, 128), (256, 128), (383, 64), (130, 64),
+@pytest.mark.parametrize("P,D", [(128, 128), (129, 128), (256, 128), (386, 64), (130, 64),
                                  (1024, 128)])
 def test_shared_set_tail_in_composite_tiles(P, D, schedule):
     # the shared set (P tokens + DELIM) leaves 1..4 keys in its last tile:
