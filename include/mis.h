@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define MIS_ABI_VERSION 3
+#define MIS_ABI_VERSION 2
 
 typedef enum {
   MIS_OK = 0,
@@ -159,10 +159,6 @@ typedef struct {
   int64_t schedule;        /* MIS_SCHEDULE_PAIR or MIS_SCHEDULE_SPLIT          */
   int64_t n_units;         /* work units of the attention kernel: query tiles  */
                            /* x (Hq / 2) for pairs, x Hq for split             */
-  int64_t n_exec_tiles;    /* (query tile, key tile) blocks the kernel runs: n_tiles,
-                              less the shared set's last, partly filled tile where
-                              its few keys (S mod 128 <= 2 at D = 128, <= 4 at
-                              D = 64) ride in an item tile's first band tile     */
 } mis_plan_stats;
 
 /* Bytes of device workspace mis_plan_create() needs for this descriptor (0
@@ -202,9 +198,8 @@ mis_status_t mis_plan_unit_walk(mis_plan_t plan, int32_t* host_out, size_t cap, 
 /* The key tiles the attention kernel runs (for inspection and tests), query
  * tile by query tile in the plan's work-list order: quadruples (request,
  * first query row, first key row c0, flags) with flags bit 0 = the tile
- * needs the element mask, bit 1 = composite (its first S mod 128 rows are
- * the request's last shared-set keys, the rest are rows c0 + r .. c0 + 127).
- * Rows are absolute (new-row axis offset by the cache for cached plans).
+ * needs the element mask (128 key rows from c0 each). Rows are absolute
+ * (the new-row axis offset by the cache for cached plans).
  * Writes min(cap, n) quadruples to host_out (may be NULL when cap is 0);
  * *n_out receives n. */
 mis_status_t mis_plan_exec_tiles(mis_plan_t plan, int32_t* host_out, size_t cap, size_t* n_out);

@@ -436,8 +436,8 @@ mis_status_t mis_plan_exec_tiles(mis_plan_t plan, int32_t* host_out, size_t cap,
       int32_t* q = host_out + 4 * n;
       q[0] = w.req;
       q[1] = w.q0;
-      q[2] = (int32_t)(e & kTileRow);
-      q[3] = ((e & kNeedMask) ? 1 : 0) | ((e & kComposite) ? 2 : 0);
+      q[2] = (int32_t)(e & ~kNeedMask);
+      q[3] = (e & kNeedMask) ? 1 : 0;
     }
   }
   *n_out = n;

@@ -121,12 +121,6 @@ struct AttnParams {
   uint32_t* status;
   uint64_t wait_ns;
   uint32_t stall;         // failure injection: wait on a barrier nothing arrives on
-  // composite key tiles (gate != 0): an idle control warp writes the shared
-  // set's last r keys (and values) into their first rows once they land
-  int32_t gate;
-  const __nv_bfloat16* k_raw;
-  const __nv_bfloat16* v_raw;
-  int64_t k_stride, v_stride;   // elements
   // rotary embedding of Q on load (rope == 0: Q arrives rotated)
   int32_t rope;
   float rope_freq[64];      // base^(-2i/D), i < D/2 (fp64 on the host, rounded to fp32)
@@ -256,11 +250,8 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
   //   SE_s: the epilogue has read slot s
   constexpr int bQF = 0, bQE = 1, bKF = 2, bKE = bKF + KS, bVF = bKE + KS, bVE = bVF + VS,
                 bSF = bVE + VS, bPF = bSF + 2, bOF = bPF + 2, bOE = bOF + 1, bDR = bOE + 2,
-                bST = bDR + 1, bSE = bST + 4, bQR = bSE + 2, bKG = bQR + 1, bVG = bKG + KS,
-                nBar = bVG + VS;
+                bST = bDR + 1, bSE = bST + 4, bQR = bSE + 2, nBar = bQR + 1;
   // bQR: the unit's Q tiles rotated in place (rotary embedding on load)
-  // bKG / bVG: a K / V tile landed and, if composite, patched (plans with
-  // composite tiles only; the MMA thread then waits on these instead of bKF / bVF)
 
   griddep_launch_dependents();
 
@@ -303,8 +294,6 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
     mbar_init(bar(bOF), 1);
     mbar_init(bar(bDR), 1);
     mbar_init(bar(bQR), 8);                            // one arrival per softmax warp
-    for (int s = 0; s < KS; ++s) mbar_init(bar(bKG + s), 1);
-    for (int s = 0; s < VS; ++s) mbar_init(bar(bVG + s), 1);
     fence_mbar_init();
     fence_proxy_async();
   }
@@ -355,7 +344,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
           q_issued = lu + 1;
           for (int it = 0; it < un.nk; ++it) {
             const int gi = gk + it;
-            const int32_t c0 = (int32_t)(p.klist[un.kofs + it] & kTileRow);
+            const int32_t c0 = (int32_t)(p.klist[un.kofs + it] & ~kNeedMask);
             // key rows below qbase are cache rows (cached-prefix plans only)
             const bool from_cache = c0 < p.qbase;
             const CUtensorMap* km = from_cache ? &kcmap : &kmap;
@@ -441,7 +430,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
             const int pend1_v = pend1_g % VS;
             // split: stream 1's V tile is not stream 0's, wait for it here (in
             // the pair schedule PV_0 of the same tile already waited)
-            if (split && !wait<true>(bar((p.gate ? bVG : bVF) + pend1_v), (pend1_g / VS) & 1, W, 0x3c0))
+            if (split && !wait<true>(bar(bVF + pend1_v), (pend1_g / VS) & 1, W, 0x3c0))
               return false;
             if (!wait<true>(bar(bPF + 1), (c1 - 1) & 1, W, 0x400)) return false;
             tc_fence_after();
@@ -454,7 +443,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
           for (int st = 0; ok && st < ns; ++st) {
             const int g0 = gk + (split ? 2 * st : st);
             const int sk0 = g0 % KS, sv0 = g0 % VS;
-            if (!(ok = wait<true>(bar((p.gate ? bKG : bKF) + sk0), (g0 / KS) & 1, W, 0x300))) break;
+            if (!(ok = wait<true>(bar(bKF + sk0), (g0 / KS) & 1, W, 0x300))) break;
             tc_fence_after();
             issue_s(0, 0, sk0);
             if (split) mma_commit(bar(bKE + sk0));
@@ -463,7 +452,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
             if (i1 < nk) {
               const int g1 = gk + i1, sk1 = g1 % KS;
               if (split) {
-                if (!(ok = wait<true>(bar((p.gate ? bKG : bKF) + sk1), (g1 / KS) & 1, W, 0x380))) break;
+                if (!(ok = wait<true>(bar(bKF + sk1), (g1 / KS) & 1, W, 0x380))) break;
                 tc_fence_after();
               }
               issue_s(1, split ? 0 : 1, sk1);
@@ -475,7 +464,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
               pend1_first = st == 0;
             }
             if (st == ns - 1) mma_commit(bar(bQE));        // Q of this unit no longer read
-            if (!(ok = wait<true>(bar((p.gate ? bVG : bVF) + sv0), (g0 / VS) & 1, W, 0x480))) break;
+            if (!(ok = wait<true>(bar(bVF + sv0), (g0 / VS) & 1, W, 0x480))) break;
             if (!(ok = wait<true>(bar(bPF + 0), c0 & 1, W, 0x500))) break;
             tc_fence_after();
             if (st == 0 && !(ok = first_pv(0))) break;
@@ -491,53 +480,6 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
         // drain: all tensor-core work of this thread completes before dealloc
         mma_commit(bar(bDR));
         wait_drain(bar(bDR), 0);
-      }
-    } else if (warp == 2 && p.gate) {
-      // ---------------------------------------------------------------- gate
-      // Every K and V tile passes here after it lands: a composite tile gets
-      // its first r rows replaced by the request's last r shared-set keys
-      // (values), one 16-byte chunk per lane, before the MMA thread may read it.
-      constexpr int NCH = D / 8;                        // 16-byte chunks per row
-      int gk = 0;
-      bool ok = true;
-      for (int kk = 0; ok && kk * (int)gridDim.x < total; ++kk) {
-        const int u = unit_at(p, kk);
-        if (u < 0) continue;
-        const WorkItem un = p.units[u / n_hg];
-        const ReqInfo R = p.req[un.req];
-        const int g = ((u % n_hg) * nh) / p.group;
-        const int rt = (R.pend - R.s0) % kBN;
-        const int ti = lane / NCH, cc = lane % NCH;   // this lane's tail row and chunk
-        const bool mine = ti < rt;
-        uint4 kt = make_uint4(0, 0, 0, 0), vt = kt;
-        if (mine) {                                     // the tail rows of this kv head
-          const int64_t row = R.pend - rt + ti;
-          kt = *reinterpret_cast<const uint4*>(p.k_raw + row * p.k_stride + (int64_t)g * D + cc * 8);
-          vt = *reinterpret_cast<const uint4*>(p.v_raw + row * p.v_stride + (int64_t)g * D + cc * 8);
-        }
-        const uint32_t off = (uint32_t)((cc / 8) * C::kBox + ti * 128 + (((cc & 7) ^ (ti & 7)) << 4));
-        for (int it = 0; it < un.nk; ++it) {
-          const int gi = gk + it;
-          const bool composite = (p.klist[un.kofs + it] & kComposite) != 0;
-          const int sk = gi % KS, sv = gi % VS;
-          ok = wait<true>(bar(bKF + sk), (gi / KS) & 1, W, 0x7c0);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          if (composite && mine)
-            st_shared_v4(smem_u32(sK + sk * C::kTile) + off, kt.x, kt.y, kt.z, kt.w);
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(bKG + sk));
-          ok = wait<true>(bar(bVF + sv), (gi / VS) & 1, W, 0x7e0);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          if (composite && mine)
-            st_shared_v4(smem_u32(sV + sv * C::kTile) + off, vt.x, vt.y, vt.z, vt.w);
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(bVG + sv));
-        }
-        gk += un.nk;
       }
     }
   } else if (warp < 12) {
@@ -598,10 +540,8 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
         const int gi = cs + it;
         const uint32_t e = e_next;
         if (it + 1 < nkt) e_next = p.klist[un.kofs + kfirst + (it + 1) * kstep];   // prefetch
-        const int32_t c0 = (int32_t)(e & kTileRow);
+        const int32_t c0 = (int32_t)(e & ~kNeedMask);
         const bool masked = (e & kNeedMask) != 0;
-        // composite tile: its first r columns are the shared set's last keys
-        const int rtail = (e & kComposite) ? (R.pend - R.s0) % kBN : 0;
         ok = wait<true>(bar(bSF + t), gi & 1, W, 0x600);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -619,8 +559,7 @@ mis_attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap,
           const int a1 = jj - c0 + 1, q1 = min(a1, R.pend - c0), lc = lo - c0;
 #pragma unroll
           for (int w = 0; w < kBN / 32; ++w) {
-            uint32_t vis = bit_range(-32 * w, q1 - 32 * w) | bit_range(lc - 32 * w, a1 - 32 * w);
-            if (w == 0 && valid) vis |= bit_range(0, rtail);
+            const uint32_t vis = bit_range(-32 * w, q1 - 32 * w) | bit_range(lc - 32 * w, a1 - 32 * w);
 #pragma unroll
             for (int x = 0; x < 32; ++x)
               if (!((vis >> x) & 1u)) su[w * 32 + x] = 0xff800000u;     // -inf
@@ -923,11 +862,6 @@ mis_status_t launch_d(HostPlan& pl, const void* q, const void* k, const void* v,
   prm.status = reinterpret_cast<uint32_t*>(ws);
   prm.wait_ns = wait_limit_ns();
   prm.stall = inject_stall_mask() & 1u;
-  prm.gate = pl.composite ? 1 : 0;
-  prm.k_raw = static_cast<const __nv_bfloat16*>(k);
-  prm.v_raw = static_cast<const __nv_bfloat16*>(v);
-  prm.k_stride = ks;
-  prm.v_stride = vs;
   prm.rope = rope ? 1 : 0;
   for (int i = 0; i < 64; ++i)
     prm.rope_freq[i] = (rope && i < D / 2) ? (float)std::pow(rope->base, -2.0 * i / D) : 0.f;

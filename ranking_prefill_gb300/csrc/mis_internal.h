@@ -23,13 +23,8 @@ constexpr size_t kStatusBytes = 256;
 constexpr uint32_t kDevTimeout = 1u;
 constexpr uint32_t kDevIndex = 2u;
 
-// Key-tile list entry: absolute first key row | (needs element mask << 31) |
-// (composite << 30). A composite tile holds, in its first r rows, the last r
-// keys of the request's shared set (r = S mod 128) instead of the r rows
-// before its first key row; the rest of the tile is rows c0 + r .. c0 + 127.
+// Key-tile list entry: absolute first key row | (needs element mask << 31).
 constexpr uint32_t kNeedMask = 0x80000000u;
-constexpr uint32_t kComposite = 0x40000000u;
-constexpr uint32_t kTileRow = 0x3FFFFFFFu;
 
 struct ReqInfo {   // one request of the packed batch, absolute rows
   int32_t s0;      // first row
@@ -73,8 +68,6 @@ struct HostPlan {
   bool cached = false;
   int32_t cache_T = 0;
   int32_t qbase = 0;
-  bool composite = false;          // some key tiles are composite (see kComposite)
-  int64_t n_exec_tiles = 0;        // key tiles the kernel runs (composites merge tail tiles)
 
   // Back to the state of a fresh plan; the vectors keep their capacity, so a
   // recycled plan of similar size touches no fresh pages.
@@ -91,8 +84,6 @@ struct HostPlan {
     cached = false;
     cache_T = 0;
     qbase = 0;
-    composite = false;
-    n_exec_tiles = 0;
   }
 };
 

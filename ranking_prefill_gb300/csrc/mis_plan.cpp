@@ -143,18 +143,13 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
       }
     }
     tmp.reserve(n_qt);
-    // executed list: at most one band tile more than the canonical map per
-    // query tile (a composite tile's band starts r rows early)
-    p->klist.resize(n_tiles + n_qt);
+    p->klist.resize(n_tiles);
     p->tile_map.resize(4 * n_tiles);
   }
   visible = p->stats.visible_pairs;
   uint32_t* kl = p->klist.data();
   int32_t* tm = p->tile_map.data();
-  int32_t n_emitted = 0, n_full = 0, n_k = 0;
-  // tail keys one warp-wide copy covers (512 B): 2 rows at D = 128, 4 at D = 64
-  const int32_t rmax = 512 / (p->D * 2);
-  const bool allow_composite = T < (1 << 30);
+  int32_t n_emitted = 0, n_full = 0;
   for (int b = 0; b < B; ++b) {
     const ReqInfo& R = p->req[b];
     const int32_t L = R.e0 - R.s0;
@@ -168,20 +163,7 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
       // interval 1: keys of Q up to the last row; interval 2: [lo_min, r1)
       const int32_t qa = 0, qb = (std::min(R.pend, r1) - R.s0 + kBN - 1) / kBN;  // [qa, qb)
       const int32_t ba = (lo_min - R.s0) / kBN, bb = (r1 - 1 - R.s0) / kBN + 1;  // [ba, bb)
-      Tmp w{b, r0, n_k, 0, 0, 0, 0, (int64_t)tmp.size()};
-      auto emit_k = [&](int32_t c0, bool need_mask, bool comp) {
-        kl[n_k++] = (uint32_t)c0 | (need_mask ? kNeedMask : 0u) | (comp ? kComposite : 0u);
-        const int c = need_mask ? 5 : 4;   // masked tiles spend extra ALU in the softmax
-        (w.nk % 2 ? w.cost_odd : w.cost_even) += c;
-        ++w.nk;
-        w.cost += c;
-      };
-      // a query tile of item rows whose band starts past the shared set's
-      // last, partly filled key tile (r = S mod 128 keys, few enough for one
-      // warp-wide copy): those r keys ride in the band's first tile
-      const int32_t S = R.pend - R.s0, rt = S % kBN, tail_u = (S - 1) / kBN;
-      const bool comp = allow_composite && rt >= 1 && rt <= rmax && r0 >= R.pend && ba > tail_u;
-      // the canonical map: every non-empty 128 x 128 block, aligned to the request
+      Tmp w{b, r0, n_emitted, 0, 0, 0, 0, (int64_t)tmp.size()};
       auto emit = [&](int32_t u) {
         const int32_t c0 = R.s0 + u * kBN;
         const int32_t c1 = std::min(c0 + kBN, R.e0);
@@ -189,28 +171,24 @@ mis_status_t build_plan(const mis_attn_desc* d, HostPlan* p) {
         //   causal part: c1 - 1 <= r0;
         //   set part: keys at or past pend must be >= lo(j) for every row.
         const bool full = (c1 - 1 <= r0) && (c1 <= R.pend || std::max(c0, R.pend) >= lo_max);
+        // a clipped key tile loads rows of the next request: mask it too
+        const bool need_mask = !full || (c0 + kBN > R.e0);
+        kl[n_emitted] = (uint32_t)c0 | (need_mask ? kNeedMask : 0u);
         int32_t* q = tm + 4 * (size_t)n_emitted;
         q[0] = b; q[1] = t; q[2] = u; q[3] = full ? 1 : 2;
         ++n_emitted;
         n_full += full ? 1 : 0;
-        // a clipped key tile loads rows of the next request: mask it too
-        if (!comp) emit_k(c0, !full || (c0 + kBN > R.e0), false);
+        const int c = need_mask ? 5 : 4;   // masked tiles spend extra ALU in the softmax
+        (w.nk % 2 ? w.cost_odd : w.cost_even) += c;
+        ++w.nk;
+        w.cost += c;
       };
       for (int32_t u = qa; u < qb; ++u) emit(u);
       for (int32_t u = std::max(ba, qb); u < bb; ++u) emit(u);
-      if (comp) {
-        // full shared-set tiles, then the composite tile (the r tail keys and
-        // band rows lo_min .. lo_min + 127 - r), then the rest of the band
-        for (int32_t u = 0; u < tail_u; ++u) emit_k(R.s0 + u * kBN, false, false);
-        emit_k(lo_min - rt, true, true);
-        for (int32_t c0 = lo_min - rt + kBN; c0 < r1; c0 += kBN) emit_k(c0, true, false);
-        p->composite = true;
-      }
       tmp.push_back(w);
     }
   }
-  if ((size_t)n_emitted * 4 != p->tile_map.size()) return MIS_ERR_SHAPE;   // the pre-count is exact
-  p->klist.resize((size_t)n_k);
+  if ((size_t)n_emitted != p->klist.size()) return MIS_ERR_SHAPE;   // the pre-count is exact
   p->stats.n_full = n_full;
   p->stats.n_partial = n_emitted - n_full;
   return finish_plan(p, tmp, B, T, visible, causal_tiles);
@@ -221,7 +199,6 @@ namespace {
 mis_status_t finish_plan(HostPlan* p, std::vector<Tmp>& tmp, int32_t B, int32_t T,
                          int64_t visible, int64_t causal_tiles) {
   if (p->klist.size() > (size_t)std::numeric_limits<int32_t>::max()) return MIS_ERR_SHAPE;
-  p->n_exec_tiles = (int64_t)p->klist.size();
   // Order: request by request, requests with the most expensive query tile
   // first, and inside a request the query tiles longest first. Blocks that run
   // at the same time then work on the same request and share its K/V tiles
@@ -283,7 +260,6 @@ mis_status_t finish_plan(HostPlan* p, std::vector<Tmp>& tmp, int32_t B, int32_t 
   p->n_head_groups = split ? p->Hq : p->Hq / 2;
   p->stats.schedule = split ? MIS_SCHEDULE_SPLIT : MIS_SCHEDULE_PAIR;
   p->stats.n_units = (int64_t)p->work.size() * p->n_head_groups;
-  p->stats.n_exec_tiles = p->n_exec_tiles;
 
   // ---- unit order: the snake walk over the list, or, when the blocks come
   // out clearly better balanced, a wave-by-wave longest-processing-time

@@ -64,7 +64,7 @@ class mis_cached_desc(C.Structure):
 class mis_plan_stats(C.Structure):
     _fields_ = [(n, C.c_int64) for n in ("n_qtiles", "n_tiles", "n_full", "n_partial",
                                            "n_causal_tiles", "visible_pairs", "workspace_bytes",
-                                           "schedule", "n_units", "n_exec_tiles")]
+                                           "schedule", "n_units")]
 
     def as_dict(self):
         return {n: int(getattr(self, n)) for n, _ in self._fields_}
@@ -341,7 +341,7 @@ class Plan:
 
     def exec_tiles(self) -> np.ndarray:
         """(request, first query row, first key row, flags) of every key tile
-        the kernel runs; flags bit 0 = masked, bit 1 = composite."""
+        the kernel runs; flags bit 0 = masked."""
         n = C.c_size_t()
         _check(self._L.mis_plan_exec_tiles(self._h, None, 0, C.byref(n)), "mis_plan_exec_tiles")
         out = np.zeros((max(n.value, 1), 4), np.int32)

@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(L):
     assert declared == set(lib.EXPORTS), declared ^ set(lib.EXPORTS)
     for name in declared:
         assert hasattr(L, name)
-    assert L.mis_abi_version() == 3
+    assert L.mis_abi_version() == 2
     for st in range(8):
         assert lib.mis_status_string(st) != "unknown status"
 
@@ -378,9 +378,7 @@ def test_attention_calls_refuse_the_wrong_plan_kind_before_any_launch(L):
 
 def _exec_coverage_ok(lay, p):
     """Every visible key of every row is in exactly one executed key tile of its
-    query tile, and a tile without the mask flag has only visible entries
-    (keys of composite tiles: their first r rows are the last r keys of the
-    shared set, the others c0 + c)."""
+    query tile, and a tile without the mask flag has only visible entries."""
     et = p.exec_tiles()
     by_qt = {}
     for b, q0, c0, fl in et.tolist():
@@ -394,9 +392,6 @@ def _exec_coverage_ok(lay, p):
         seen = np.zeros_like(vis, dtype=np.int32)
         for c0, fl in tiles:
             keys = c0 + np.arange(128)
-            if fl & 2:
-                r = S % 128
-                keys[:r] = s0 + S - r + np.arange(r)
             inside = (keys >= s0) & (keys < e0)
             cols = keys[inside] - s0
             seen[:, cols] += 1
@@ -406,9 +401,10 @@ def _exec_coverage_ok(lay, p):
 
 
 def test_executed_tiles_cover_every_visible_key_once(L):
-    # layouts whose shared set leaves 1..5 keys in its last tile, at D = 64
-    # and 128 (composite tiles where a warp-wide copy covers the tail), plus
-    # the benchmark's small workloads
+    # the executed key-tile lists, checked row by row against the oracle's
+    # eq.-(4) mask: shared sets ending at, just past and well past a tile
+    # edge, at D = 64 and 128, plus the benchmark's small workloads and a
+    # sampled part of decision-256
     rng = np.random.default_rng(2024)
     cases = []
     for D in (64, 128):
@@ -418,12 +414,12 @@ def test_executed_tiles_cover_every_visible_key_once(L):
     for name in ("qwen3-0.6b-layer", "tiny"):
         w = synth.WORKLOADS[name]
         cases.append((synth.draw_shapes(w), w.head_dim))
-    n_comp = 0
+    d = synth.draw_shapes(synth.WORKLOADS["decision-256"])
+    k = int(d.n_items[:12].sum())
+    cases.append((synth.custom_shapes(d.prefix_tokens[:12], d.n_items[:12], d.item_lens[:k]), 128))
     for s, D in cases:
         lay = O.build_layout(s.prefix_tokens, s.n_items, s.item_lens)
         p = lib.Plan.host_only(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, 4, 2, D)
         _exec_coverage_ok(lay, p)
         st = p.stats()
-        n_comp += st["n_tiles"] - st["n_exec_tiles"]
-        assert np.array_equal(p.tile_map(), O.tile_map(lay, 128, 128))   # the map stays canonical
-    assert n_comp > 0                                      # some tail tiles were merged
+        assert len(p.exec_tiles()) == st["n_tiles"]

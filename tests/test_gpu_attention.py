@@ -227,20 +227,3 @@ def test_pointer_and_stride_refusals_launch_nothing():
     assert lib.mis_get_device_status(ws) == lib.MIS_OK
     plan.destroy()
 
-
-@pytest.mark.parametrize("P,D", [(128, 128), (129, 128), (256, 128), (386, 64), (130, 64),
-                                 (1024, 128)])
-def test_shared_set_tail_in_composite_tiles(P, D, schedule):
-    # the shared set (P tokens + DELIM) leaves 1..4 keys in its last tile:
-    # item query tiles far from it run those keys inside their first band
-    # tile (a composite tile patched after it lands); two requests, many items
-    rng = np.random.default_rng(P + D)
-    n = [14, 9]
-    lens = rng.integers(0, 70, sum(n))
-    s = synth.custom_shapes([P, P + 128], n, lens)
-    lay = lib.mis_build_layout(s.prefix_tokens, s.n_items, s.item_lens, with_positions=False)
-    st0 = lib.Plan.host_only(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets,
-                             8, 2, D).stats()
-    assert st0["n_exec_tiles"] < st0["n_tiles"]
-    err, st = check_attention(s, 8, 2, D, 300 + P)
-    _expect_schedule(st, schedule, 8, 2)
