@@ -454,6 +454,8 @@ def measure(args, name, rank, world, dist, dev, local, full):
         "gpu_launches": (5 if args.rope else 4) * args.steps,
         "clocks": clk.summary(),
         "host_plan_ms": round(1e3 * statistics.median(host_s[-args.steps:]), 4),
+        "host_plan_note": "host time of a step's layout + plan + upload call, including any "
+                          "wait for a free pinned staging buffer while the GPU is behind",
         "per_call_split": {"steps": args.steps, "ms_per_step": round(statistics.mean(split_ms), 4),
                            "note": "attention, scoring and roofline times from as many further "
                                    "steps with CUDA events between the calls; value and "
