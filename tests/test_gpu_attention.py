@@ -5,7 +5,9 @@ empty items, D = 64 and 128, GQA groups 1 to 5 and a lone head, strided
 rows, varlen batches), on
 the full qwen3-0.6b-layer workload, and on seeded row samples of the large
 workloads (every readout row plus seeded random rows; rows are independent,
-so each sampled row is still an exact element-by-element check). Tolerances: max-abs 2e-2 on O, 2e-3 on LSE.
+so each sampled row is still an exact element-by-element check). Seeded
+random batches also check that a plan's output repeats bit for bit (a race
+check) and that the two schedules agree. Tolerances: max-abs 2e-2 on O, 2e-3 on LSE.
 """
 import numpy as np
 import pytest
@@ -156,6 +158,57 @@ def test_schedules_agree_on_a_long_unit_mix():
             outs.append((o.float(), lse.clone()))
     assert (outs[0][0] - outs[1][0]).abs().max().item() <= 8e-3
     assert (outs[0][1] - outs[1][1]).abs().max().item() <= 1e-4
+
+
+def test_random_batches_repeat_bit_for_bit_and_schedules_agree():
+    # Seeded random batches (up to 12 requests, prefixes up to 1,500 tokens,
+    # up to 150 items of up to 80 tokens, several head layouts). Each plan runs
+    # twice and must give bit-identical O and LSE: every unit is computed by
+    # one block in a fixed order, so any difference would be a race between
+    # the kernel's warp roles. The two schedules must agree within rounding,
+    # and every fourth batch is held against the oracle on sampled rows.
+    rng = np.random.default_rng(4242)
+    dev = torch.device("cuda")
+    layouts = [(16, 8, 128), (8, 2, 64), (6, 2, 128), (32, 8, 128), (4, 4, 64), (10, 2, 128)]
+    for case in range(16):
+        B = int(rng.integers(1, 13))
+        p = rng.integers(0, 1500, B)
+        n = rng.integers(0, 150, B) * (rng.random(B) < 0.85)
+        lens = rng.integers(0, 80, int(n.sum()))
+        hq, hkv, D = layouts[case % len(layouts)]
+        s = synth.custom_shapes(p, n, lens)
+        lay = lib.mis_build_layout(s.prefix_tokens, s.n_items, s.item_lens)
+        T = lay.T
+        vals = synth.draw_values(500 + case, T, hq, hkv, D, want=("q", "k", "v"))
+        q, k, v = (vals[x].to(dev) for x in ("q", "k", "v"))
+        outs = []
+        for mode in (lib.SCHEDULE_PAIR, lib.SCHEDULE_SPLIT):
+            with forced_schedule(mode):
+                plan = lib.Plan(lay.cu_seqlens, lay.prefix_len, lay.item_ptr, lay.item_offsets, hq, hkv, D)
+            ws = torch.zeros(plan.workspace_size(), dtype=torch.uint8, device=dev)
+            plan.create(ws)
+            runs = []
+            for fill in (7.0, 9.0):
+                o = torch.full((T, hq, D), fill, dtype=torch.bfloat16, device=dev)
+                lse = torch.full((hq, T), fill, dtype=torch.float32, device=dev)
+                lib.mis_attention_fwd_plan(plan, q, k, v, o, lse)
+                runs.append((o, lse))
+            torch.cuda.synchronize()
+            assert lib.mis_get_device_status(ws) == lib.MIS_OK
+            assert torch.equal(runs[0][0], runs[1][0]) and torch.equal(runs[0][1], runs[1][1]), case
+            outs.append(runs[0])
+            plan.destroy()
+        assert (outs[0][0].float() - outs[1][0].float()).abs().max().item() <= ATTN_TOL, case
+        assert (outs[0][1] - outs[1][1]).abs().max().item() <= 2e-3, case
+        if case % 4 == 0:
+            olay = oracle_layout(s)
+            rows = sorted(set(rng.choice(T, size=min(48, T), replace=False).tolist()) |
+                          set(olay.delim_positions[:16].tolist()))
+            ro, rl = O.attention(f64(vals["q"]), f64(vals["k"]), f64(vals["v"]), olay, rows=rows)
+            for o, lse in outs:
+                got = f64(o[torch.as_tensor(rows, device=dev)])
+                assert np.abs(got - ro).max() <= ATTN_TOL, case
+                assert np.abs(f64(lse)[:, rows].T - rl).max() <= 2e-3, case
 
 
 @pytest.mark.parametrize("name", ["8b-large", "decision-256", "varlen-16", "prefix12k-50x150"])
