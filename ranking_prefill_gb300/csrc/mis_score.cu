@@ -81,12 +81,15 @@ ScoreLayout score_layout(int32_t M, int32_t d, int32_t V, int32_t K) {
 
 struct ScoreParams {
   int32_t M, V, K, n_vtiles, tiles_per_chunk, n_chunks, n_kb;
+  int32_t n_parts;         // (max, sum) partials per item: one per chunk, or one per vocabulary
+                           // tile when the tiles come from the counter (a fixed merge order, so
+                           // the scores repeat bit for bit whichever block ran which tile)
   int32_t dynamic;         // one item tile: blocks take vocabulary tiles from a counter
   uint32_t* ctr;           // that counter (a status word, cleared by the gather kernel)
   const uint8_t* w_lm;     // W_lm rows, for the L2 prefetch
   uint32_t pf_bytes;       // W_lm bytes of its range each block prefetches into L2 before its wait
   int32_t labels[16];
-  float* part;        // [m_pad][n_chunks][2] = (max in log2 units, sum of 2^(z*log2e - max))
+  float* part;        // [m_pad][n_parts][2] = (max in log2 units, sum of 2^(z*log2e - max))
   float* zlab;        // [m_pad][K] label logits
   const int32_t* bad; // [m_pad] 1 where the readout row was out of range
   uint32_t* status;
@@ -361,9 +364,16 @@ mis_score_partial_kernel(const __grid_constant__ CUtensorMap amap,
       }
       tc_fence_before();
       mbar_arrive(bar(bAE + buf));
+      if (dyn) {                                      // this tile's own partial
+        float* pp = p.part + ((int64_t)item * p.n_parts + t) * 2;
+        pp[0] = m2;
+        pp[1] = s;
+        m2 = -INFINITY;
+        s = 0.f;
+      }
     }
-    if (ok) {
-      float* pp = p.part + ((int64_t)item * p.n_chunks + chunk) * 2;
+    if (ok && !dyn) {
+      float* pp = p.part + ((int64_t)item * p.n_parts + chunk) * 2;
       pp[0] = m2;
       pp[1] = s;
     }
@@ -577,7 +587,7 @@ mis_score_partial_pair_kernel(const __grid_constant__ CUtensorMap amap,
       if (lane == 0) mbar_arrive_cluster(lbar(bAE + buf));
     }
     if (ok) {
-      float* pp = p.part + ((int64_t)item * p.n_chunks + chunk) * 2;
+      float* pp = p.part + ((int64_t)item * p.n_parts + chunk) * 2;
       pp[0] = m2;
       pp[1] = s;
     }
@@ -607,19 +617,21 @@ mis_score_combine_kernel(const ScoreParams p, float* __restrict__ out,
   if (i >= p.M) return;
   if (lane == 0 && p.bad[i]) raise_status(p.status, kDevIndex, (uint32_t)i);
   if (*(volatile uint32_t*)p.status & kDevTimeout) return;
-  const float2* pp = reinterpret_cast<const float2*>(p.part) + (int64_t)i * p.n_chunks;
+  const float2* pp = reinterpret_cast<const float2*>(p.part) + (int64_t)i * p.n_parts;
   float m = -INFINITY, s = 0.f;
-  // up to 8 chunks per lane are loaded together, then merged: one L2 round
-  // trip per 256 chunks instead of one per 32
-  for (int c0 = lane; c0 < p.n_chunks; c0 += 32 * 8) {
-    float2 e[8];
+  // up to 24 partials per lane are loaded together, then merged: one L2 round
+  // trip per 768 partials (a 151,936-entry vocabulary has 594) instead of one
+  // per 32
+  constexpr int kPer = 24;
+  for (int c0 = lane; c0 < p.n_parts; c0 += 32 * kPer) {
+    float2 e[kPer];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < kPer; ++u) {
       const int c = c0 + 32 * u;
-      e[u] = c < p.n_chunks ? pp[c] : make_float2(-INFINITY, 0.f);
+      e[u] = c < p.n_parts ? pp[c] : make_float2(-INFINITY, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < kPer; ++u) {
       if (e[u].x == -INFINITY) continue;
       if (e[u].x > m) { s = s * exp2f(m - e[u].x) + e[u].y; m = e[u].x; }
       else s += e[u].y * exp2f(e[u].x - m);
@@ -710,6 +722,7 @@ mis_status_t launch_score(const ScoreArgs& a, void* stream) {
   p.ctr = status + 2;
   p.tiles_per_chunk = p.dynamic ? 0 : pick_tiles_per_chunk(n_mtiles, L.n_vtiles, sms);
   p.n_chunks = p.dynamic ? sms : (L.n_vtiles + p.tiles_per_chunk - 1) / p.tiles_per_chunk;
+  p.n_parts = p.dynamic ? L.n_vtiles : p.n_chunks;
   p.n_kb = a.d / kKStep;
   p.w_lm = static_cast<const uint8_t*>(a.w_lm);
   // L2 prefetch of W_lm before the wait: only when the whole grid is one wave

@@ -223,3 +223,23 @@ def test_counter_fed_tiles_across_back_to_back_calls():
     assert lib.mis_get_device_status(ws) == lib.MIS_OK
     lp, _, _ = O.label_scores(f64(hidden), f64(w), rows, lb)
     assert np.abs(f64(out) - lp).max() <= SCORE_TOL
+
+
+def test_scores_repeat_bit_for_bit():
+    # Every path's partial (max, sum) pairs are merged in a fixed order: with
+    # the vocabulary tiles from a counter (one item tile, more tiles than SMs)
+    # each tile keeps its own partial, whichever block ran it; the fixed runs
+    # of tiles (one SM or SM pairs) are fixed by construction. So the same call
+    # gives the same bits every time.
+    g = torch.Generator().manual_seed(33)
+    T = 700
+    for M, d, V, labels in [(100, 1024, 151936, [3, 151935]), (60, 256, 30000, [7, 8, 29999]),
+                            (300, 512, 20000, [0, 19999])]:
+        hidden = torch.randn(T, d, generator=g).to(torch.bfloat16).cuda()
+        w = (torch.randn(V, d, generator=g) * 0.02).to(torch.bfloat16).cuda()
+        rows = torch.as_tensor(np.random.default_rng(M).choice(T, M, replace=False).astype(np.int32)).cuda()
+        runs = [run_scores(hidden, w, rows, labels) for _ in range(3)]
+        for out, ren, ws in runs:
+            assert lib.mis_get_device_status(ws) == lib.MIS_OK
+        for out, ren, _ in runs[1:]:
+            assert torch.equal(out, runs[0][0]) and torch.equal(ren, runs[0][1]), (M, d, V)
