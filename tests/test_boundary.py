@@ -423,3 +423,31 @@ def test_executed_tiles_cover_every_visible_key_once(L):
         _exec_coverage_ok(lay, p)
         st = p.stats()
         assert len(p.exec_tiles()) == st["n_tiles"]
+
+
+def test_reference_arm_prints_the_contract_line_on_the_cpu():
+    # `bench.py --impl reference` (the oracle on the host cores) prints one
+    # JSON line with the main arm's metric, unit, direction and config object,
+    # a cpu_baseline and an e2e entry without host-device copies
+    import json
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny", "--steps", "2", "--warmup", "3", "--cpu-budget-s", "2"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [x for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    sys.path.insert(0, ROOT)
+    import bench
+    w = synth.WORKLOADS["tiny"]
+    s = synth.draw_shapes(w)
+    T, M = bench.oracle_sizes(w, s)
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "items/s"
+    assert d["higher_is_better"] is True and d["steps"] == 2 and d["warmup"] == 3
+    assert d["config"] == bench.workload_config(w, s, T, M, len(s.label_sets[0]), 1)
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "items/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
