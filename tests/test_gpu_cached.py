@@ -22,8 +22,12 @@ def _run_cached(cl, cache_T, q, k, v, kc, vc, hq, hkv, D, lse=True):
     o = torch.full((cl.T, hq, D), 7.0, dtype=torch.bfloat16, device=dev)
     l = torch.full((hq, cl.T), 7.0, dtype=torch.float32, device=dev) if lse else None
     lib.mis_attention_fwd_cached(plan, q, k, v, kc, vc, o, l)
+    o2 = torch.empty_like(o)
+    l2 = torch.empty_like(l) if lse else None
+    lib.mis_attention_fwd_cached(plan, q, k, v, kc, vc, o2, l2)
     torch.cuda.synchronize()
     assert lib.mis_get_device_status(ws) == lib.MIS_OK
+    assert torch.equal(o, o2) and (not lse or torch.equal(l, l2))   # the same bits again
     return o, l, plan.stats()
 
 

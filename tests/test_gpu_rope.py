@@ -148,9 +148,12 @@ def _fused_case(shapes, hq, hkv, D, seed, base=1.0e6, stride_pad=0):
     ws = torch.zeros(plan.workspace_size(), dtype=torch.uint8, device=dev)
     plan.create(ws)
     lib.mis_attention_fwd_plan_rope(plan, q, kr, vv, o, lse, base)
+    o2, lse2 = torch.empty_like(o), torch.empty_like(lse)
+    lib.mis_attention_fwd_plan_rope(plan, q, kr, vv, o2, lse2, base)
     torch.cuda.synchronize()
     status = lib.mis_get_device_status(ws)
     assert torch.equal(q, q_before)                     # Q is rotated in shared memory only
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)   # the same bits on a second launch
     olay = O.build_layout(shapes.prefix_tokens, shapes.n_items, shapes.item_lens)
     # the rotated Q and K are held in bf16 on the GPU (Q in shared memory, K
     # in HBM): the oracle attends over the fp64 rotation rounded to bf16
