@@ -630,12 +630,18 @@ mis_score_combine_kernel(const ScoreParams p, float* __restrict__ out,
       const int c = c0 + 32 * u;
       e[u] = c < p.n_parts ? pp[c] : make_float2(-INFINITY, 0.f);
     }
+    // the batch's max first, then its sum: independent exponentials, no
+    // chain of dependent rescales
+    float mb = -INFINITY;
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      if (e[u].x == -INFINITY) continue;
-      if (e[u].x > m) { s = s * exp2f(m - e[u].x) + e[u].y; m = e[u].x; }
-      else s += e[u].y * exp2f(e[u].x - m);
-    }
+    for (int u = 0; u < kPer; ++u) mb = fmaxf(mb, e[u].x);
+    if (mb == -INFINITY) continue;
+    float sb = 0.f;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) sb += e[u].y * exp2f(e[u].x - mb);    // exp2f(-inf) = 0
+    const float mm = fmaxf(m, mb);
+    s = (m == -INFINITY ? 0.f : s * exp2f(m - mm)) + sb * exp2f(mb - mm);
+    m = mm;
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
