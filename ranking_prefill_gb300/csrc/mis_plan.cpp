@@ -291,24 +291,47 @@ mis_status_t finish_plan(HostPlan* p, std::vector<Tmp>& tmp, int32_t B, int32_t 
       order.assign((size_t)(passes * G), -1);
       load.assign((size_t)G, 0);
       bkey.resize((size_t)G);
+      thread_local std::vector<int32_t> uord, bord, cnt;
+      uord.resize((size_t)G);
+      bord.resize((size_t)G);
+      // Stable counting sort of n values v(i) (i ascending within equal values)
+      // into `out`, ascending or descending; false when their range is too
+      // wide for it (the caller then sorts packed keys).
+      auto counting = [&](int64_t n, auto v, bool descending, std::vector<int32_t>& out) -> bool {
+        int64_t lo = v(0), hi = v(0);
+        for (int64_t i = 1; i < n; ++i) { lo = std::min(lo, v(i)); hi = std::max(hi, v(i)); }
+        if (hi - lo >= 4096) return false;
+        cnt.assign((size_t)(hi - lo + 2), 0);
+        for (int64_t i = 0; i < n; ++i) ++cnt[(size_t)((descending ? hi - v(i) : v(i) - lo) + 1)];
+        for (size_t k = 1; k < cnt.size(); ++k) cnt[k] += cnt[k - 1];
+        for (int64_t i = 0; i < n; ++i)
+          out[(size_t)cnt[(size_t)(descending ? hi - v(i) : v(i) - lo)]++] = (int32_t)i;
+        return true;
+      };
       bool fits = true;
       for (int64_t kk = 0; kk < passes && fits; ++kk) {
-        const int64_t u0 = kk * G, u1 = std::min(u0 + G, n_units);
+        const int64_t u0 = kk * G, u1 = std::min(u0 + G, n_units), nu = u1 - u0;
         // units of the pass: cost descending, then list order
-        ukey.resize((size_t)(u1 - u0));
-        for (int64_t u = u0; u < u1; ++u)
-          ukey[(size_t)(u - u0)] = ((uint64_t)(((int64_t)1 << 31) - 1 - cost[(size_t)u]) << 32) |
-                                   (uint64_t)(u - u0);
-        std::sort(ukey.begin(), ukey.end());
-        // blocks: load ascending, then block index
-        for (int64_t c = 0; c < G; ++c) {
-          if (load[(size_t)c] >= ((int64_t)1 << 40)) fits = false;
-          bkey[(size_t)c] = ((uint64_t)load[(size_t)c] << 16) | (uint64_t)c;
+        if (!counting(nu, [&](int64_t i) { return cost[(size_t)(u0 + i)]; }, true, uord)) {
+          ukey.resize((size_t)nu);
+          for (int64_t i = 0; i < nu; ++i)
+            ukey[(size_t)i] = ((uint64_t)(((int64_t)1 << 31) - 1 - cost[(size_t)(u0 + i)]) << 32) |
+                              (uint64_t)i;
+          std::sort(ukey.begin(), ukey.end());
+          for (int64_t i = 0; i < nu; ++i) uord[(size_t)i] = (int32_t)(ukey[(size_t)i] & 0xFFFFFFFFu);
         }
-        std::sort(bkey.begin(), bkey.end());
-        for (size_t i = 0; i < ukey.size(); ++i) {
-          const int64_t c = (int64_t)(bkey[i] & 0xFFFFu);
-          const int64_t u = u0 + (int64_t)(ukey[i] & 0xFFFFFFFFu);
+        // blocks: load ascending, then block index
+        for (int64_t c = 0; c < G; ++c)
+          if (load[(size_t)c] >= ((int64_t)1 << 40)) fits = false;
+        if (!counting(G, [&](int64_t c) { return load[(size_t)c]; }, false, bord)) {
+          for (int64_t c = 0; c < G; ++c)
+            bkey[(size_t)c] = ((uint64_t)load[(size_t)c] << 16) | (uint64_t)c;
+          std::sort(bkey.begin(), bkey.end());
+          for (int64_t c = 0; c < G; ++c) bord[(size_t)c] = (int32_t)(bkey[(size_t)c] & 0xFFFFu);
+        }
+        for (int64_t i = 0; i < nu; ++i) {
+          const int64_t c = bord[(size_t)i];
+          const int64_t u = u0 + uord[(size_t)i];
           load[(size_t)c] += cost[(size_t)u];
           order[(size_t)(kk * G + ((kk & 1) ? (G - 1 - c) : c))] = (int32_t)u;
         }
