@@ -451,3 +451,34 @@ def test_reference_arm_prints_the_contract_line_on_the_cpu():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "items/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_layout_tile_map_and_walk_on_generated_batches(L):
+    # Property-based: batches hypothesis generates (1 to 6 requests, prefixes
+    # of 0 to 700 tokens, 0 to 30 items of 0 to 300 tokens), layout and tile
+    # map bit-exact against the oracle, pair count against the closed form,
+    # and the unit walk handing out every unit once under either schedule
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+
+    req = st.tuples(st.integers(0, 700), st.lists(st.integers(0, 300), max_size=30))
+
+    @hyp.settings(max_examples=60, deadline=None, derandomize=True)
+    @hyp.given(st.lists(req, min_size=1, max_size=6), st.sampled_from([(4, 2, 64), (16, 8, 128), (6, 2, 128)]))
+    def check(reqs, heads):
+        P = [r[0] for r in reqs]
+        N = [len(r[1]) for r in reqs]
+        lens = [x for r in reqs for x in r[1]]
+        got = lib.mis_build_layout(P, N, lens)
+        ref = O.build_layout(P, N, lens)
+        for f in ("cu_seqlens", "prefix_len", "item_ptr", "item_offsets", "delim_positions",
+                  "position_ids"):
+            assert np.array_equal(getattr(got, f), getattr(ref, f)), f
+        hq, hkv, D = heads
+        p = lib.Plan.host_only(ref.cu_seqlens, ref.prefix_len, ref.item_ptr, ref.item_offsets, hq, hkv, D)
+        assert np.array_equal(p.tile_map(), O.tile_map(ref, 128, 128))
+        assert p.stats()["visible_pairs"] == O.pair_count(ref)
+        walk, G = p.unit_walk()
+        assert np.array_equal(np.sort(walk[walk >= 0]), np.arange(p.stats()["n_units"]))
+
+    check()
